@@ -1,0 +1,515 @@
+"""Pins for the CPU oracle: facts the pages and the mathematics fix, checked
+independently of the oracle's own code paths.
+
+Each ``check_*`` function is a pin; the ``test_*`` functions run them, and the
+``test_plant_*`` functions plant a plausible mistake in the oracle (on the CPU)
+and show that at least one pin fails.
+"""
+
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.moe_oracle as om
+from oracle.moe_oracle import OracleConfig
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")
+LN3 = math.log(3.0)
+
+
+def _cfg(**kw):
+    base = dict(T=16, d_model=8, d_ff=12, E=4, k=2)
+    base.update(kw)
+    return OracleConfig(**base)
+
+
+def _rand_layer(rng, T, d, F, E, S=0, bias=True):
+    x = rng.standard_normal((T, d))
+    w_g = rng.standard_normal((d, E)) / math.sqrt(d)
+    ex = [(rng.standard_normal((F, d)) / math.sqrt(d),
+           rng.standard_normal(F) * 0.1 if bias else None,
+           rng.standard_normal((d, F)) / math.sqrt(F),
+           rng.standard_normal(d) * 0.1 if bias else None) for _ in range(E)]
+    sh = [(rng.standard_normal((F, d)) / math.sqrt(d), None,
+           rng.standard_normal((d, F)) / math.sqrt(F), None) for _ in range(S)]
+    return x, w_g, ex, sh
+
+
+def _torch_ffn(x, w1, b1, w2, b2):
+    """Textbook two-layer MLP through torch's own Linear and exact GELU."""
+    t = lambda a: None if a is None else torch.as_tensor(np.asarray(a), dtype=torch.float64)
+    h = torch.nn.functional.linear(t(x), t(w1), t(b1))
+    h = torch.nn.functional.gelu(h, approximate="none")
+    return torch.nn.functional.linear(h, t(w2), t(b2)).numpy()
+
+
+# ---------------------------------------------------------------- golden
+def check_golden_pages_values():
+    g = json.load(open(GOLDEN))
+    for item in g["expert_combinations"]:
+        assert math.comb(item["E"], item["k"]) == item["count"], item
+        if item["count"] < 10 ** 6:
+            # the brute-force selection enumerates exactly these subsets
+            assert len(_subsets(item["E"], item["k"])) == item["count"]
+    for item in g["activated_fraction"]:
+        assert abs(item["k"] / item["E"] - item["fraction"]) <= item["abs_tol"] + 1e-15
+    for item in g["experts_per_token_with_shared"]:
+        assert item["n_shared"] + item["k"] == item["total"]
+    for item in g["capacity"]:
+        cfg = OracleConfig(T=item["T"], d_model=1, d_ff=1, E=item["E"], k=1,
+                           capacity_factor=item["capacity_factor"])
+        assert om.capacity(cfg) == item["C"], item
+
+
+def test_golden_pages_values():
+    check_golden_pages_values()
+
+
+# ---------------------------------------------------------------- selection
+def _subsets(E, k):
+    return list(itertools.combinations(range(E), k))
+
+
+def _brute_select(score_row, k):
+    """Enumerate every k-subset; keep the largest score sum, breaking equal
+    sums by the lexicographically smallest index tuple."""
+    best, best_sum = None, None
+    for sub in _subsets(len(score_row), k):     # lexicographic order
+        # exact rational sums: float rounding must not break equal sums
+        s = sum(Fraction(float(score_row[i])) for i in sub)
+        if best_sum is None:
+            best, best_sum = sub, s
+        if s > best_sum:
+            best, best_sum = sub, s
+    return best
+
+
+def check_selection_bruteforce(seed=0):
+    rng = np.random.default_rng(seed)
+    for E, k in [(4, 1), (4, 2), (5, 3), (8, 2), (8, 3)]:
+        for trial in range(6):
+            # scores on a coarse grid so that ties occur often
+            l = rng.integers(-3, 4, size=(12, E)).astype(np.float32)
+            for route in (om.ROUTE_SOFTMAX_TOPK, om.ROUTE_TOPK_SOFTMAX, om.ROUTE_BIASED_SOFTMAX):
+                sb = rng.integers(0, 3, size=E) * 0.25 if route == om.ROUTE_BIASED_SOFTMAX else None
+                cfg = _cfg(T=12, E=E, k=k, route=route)
+                g = om.gate(l, cfg, select_bias=sb)
+                p = np.exp(l.astype(np.float64))
+                p /= p.sum(1, keepdims=True)
+                if route == om.ROUTE_SOFTMAX_TOPK:
+                    score = p
+                elif route == om.ROUTE_TOPK_SOFTMAX:
+                    score = l.astype(np.float64)
+                else:
+                    score = p + sb
+                for t in range(12):
+                    want = _brute_select(list(score[t]), k)
+                    got = tuple(sorted(int(i) for i in g.idx[t]))
+                    assert got == want, (route, E, k, t, score[t], got, want)
+                    # order: descending score, ties by ascending index
+                    row = [(-score[t][i], int(i)) for i in g.idx[t]]
+                    assert row == sorted(row), (route, t, row)
+
+
+def test_selection_bruteforce():
+    check_selection_bruteforce()
+
+
+def check_hand_gate_examples():
+    # logits ln[4,2,1,1] -> p = [.5,.25,.125,.125]; top-2 = {0,1}
+    l = np.log(np.array([[4.0, 2.0, 1.0, 1.0]], np.float32)).astype(np.float32)
+    g = om.gate(l, _cfg(T=1, E=4, k=2, route=om.ROUTE_SOFTMAX_TOPK))
+    assert list(g.idx[0]) == [0, 1]
+    np.testing.assert_allclose(g.w[0], [2 / 3, 1 / 3], rtol=1e-6)
+    np.testing.assert_allclose(g.p[0], [0.5, 0.25, 0.125, 0.125], rtol=1e-6)
+    # without renormalisation the weights are the probabilities themselves
+    g = om.gate(l, _cfg(T=1, E=4, k=2, route=om.ROUTE_SOFTMAX_TOPK, renorm=False))
+    np.testing.assert_allclose(g.w[0], [0.5, 0.25], rtol=1e-6)
+    # top-k on logits, softmax over the two: exp(ln4)/(4+2) = 2/3
+    g = om.gate(l, _cfg(T=1, E=4, k=2, route=om.ROUTE_TOPK_SOFTMAX))
+    assert list(g.idx[0]) == [0, 1]
+    np.testing.assert_allclose(g.w[0], [2 / 3, 1 / 3], rtol=1e-6)
+    # selection bias 0.2 on expert 2: scores [.5,.25,.325,.125] -> {0,2};
+    # weights from the unbiased p: .5/.625, .125/.625
+    g = om.gate(l, _cfg(T=1, E=4, k=2, route=om.ROUTE_BIASED_SOFTMAX),
+                select_bias=np.array([0.0, 0.0, 0.2, 0.0]))
+    assert list(g.idx[0]) == [0, 2]
+    np.testing.assert_allclose(g.w[0], [0.8, 0.2], rtol=1e-6)
+    # all-equal logits: lowest indices win, equal weights
+    g = om.gate(np.zeros((1, 4), np.float32), _cfg(T=1, E=4, k=2))
+    assert list(g.idx[0]) == [0, 1]
+    np.testing.assert_allclose(g.w[0], [0.5, 0.5], rtol=0, atol=0)
+
+
+def test_hand_gate_examples():
+    check_hand_gate_examples()
+
+
+def check_softmax_topk_equals_topk_softmax(seed=1):
+    """softmax(l)_i / sum_S softmax(l)_j = exp(l_i) / sum_S exp(l_j): with
+    renormalisation, both gating forms give the same experts and weights."""
+    rng = np.random.default_rng(seed)
+    for E, k in [(8, 2), (64, 1), (16, 4), (256, 8)]:
+        l = (rng.standard_normal((64, E)) * 2).astype(np.float32)
+        a = om.gate(l, _cfg(T=64, E=E, k=k, route=om.ROUTE_SOFTMAX_TOPK, renorm=True))
+        b = om.gate(l, _cfg(T=64, E=E, k=k, route=om.ROUTE_TOPK_SOFTMAX))
+        ok = a.margin > 1e-9
+        assert np.array_equal(a.idx[ok], b.idx[ok])
+        np.testing.assert_allclose(a.w[ok], b.w[ok], rtol=1e-12, atol=1e-15)
+
+
+def test_softmax_topk_equals_topk_softmax():
+    check_softmax_topk_equals_topk_softmax()
+
+
+def check_weights_sum_to_one(seed=2):
+    rng = np.random.default_rng(seed)
+    for route in (om.ROUTE_SOFTMAX_TOPK, om.ROUTE_TOPK_SOFTMAX, om.ROUTE_BIASED_SOFTMAX):
+        for E, k in [(8, 2), (8, 1), (32, 5)]:
+            l = rng.standard_normal((50, E)).astype(np.float32)
+            g = om.gate(l, _cfg(T=50, E=E, k=k, route=route),
+                        select_bias=rng.standard_normal(E) * 0.01)
+            np.testing.assert_allclose(g.w.sum(1), 1.0, rtol=0, atol=1e-12)
+            if k == 1:
+                assert np.all(g.w == 1.0)
+            assert np.all(g.w > 0)
+
+
+def test_weights_sum_to_one():
+    check_weights_sum_to_one()
+
+
+def check_softmax_basic():
+    l = np.array([[1000.0, 1000.0, -1000.0], [0.0, LN3, 0.0]], np.float32)
+    p = om.softmax(l)
+    assert np.all(np.isfinite(p))
+    np.testing.assert_allclose(p[0], [0.5, 0.5, 0.0], atol=1e-300)
+    np.testing.assert_allclose(p[1], [0.2, 0.6, 0.2], rtol=1e-6)
+
+
+def test_softmax_basic():
+    check_softmax_basic()
+
+
+def check_router_logits(seed=3):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((20, 24)).astype(np.float32)
+    w = rng.standard_normal((24, 5)).astype(np.float32)
+    l = om.router_logits(x, w)
+    assert l.dtype == np.float32 and l.shape == (20, 5)
+    ref = (torch.from_numpy(x).double() @ torch.from_numpy(w).double()).float().numpy()
+    assert np.array_equal(l, ref)
+    b = np.arange(5, dtype=np.float32)
+    assert np.array_equal(om.router_logits(x, w, b), (ref + b).astype(np.float32))
+
+
+def test_router_logits():
+    check_router_logits()
+
+
+# ---------------------------------------------------------------- experts
+def check_gelu_closed_form():
+    # GELU(x) = x * Phi(x); Phi(1) and Phi(-1) of the standard normal CDF
+    v = om.gelu(np.array([0.0, 1.0, -1.0, 8.0, -8.0]))
+    np.testing.assert_allclose(v[:3], [0.0, 0.8413447460685429, -0.15865525393145707],
+                               rtol=1e-15, atol=1e-16)
+    np.testing.assert_allclose(v[3], 8.0, rtol=1e-14)
+    assert abs(v[4]) < 1e-13
+
+
+def test_gelu_closed_form():
+    check_gelu_closed_form()
+
+
+def check_dense_reductions(seed=4):
+    rng = np.random.default_rng(seed)
+    T, d, F = 10, 6, 10
+    # E = 1, k = 1: the layer is one dense FFN (weight 1 after renormalising)
+    x, w_g, ex, _ = _rand_layer(rng, T, d, F, 1)
+    r = om.moe_forward(_cfg(T=T, d_model=d, d_ff=F, E=1, k=1), x, w_g, lambda e: ex[e])
+    np.testing.assert_allclose(r.out, _torch_ffn(x, *ex[0]), rtol=1e-12, atol=1e-12)
+    # identical experts + renormalised top-k: FFN(x) whatever the router says
+    E = 6
+    x, w_g, ex, _ = _rand_layer(rng, T, d, F, E)
+    for route in (om.ROUTE_SOFTMAX_TOPK, om.ROUTE_TOPK_SOFTMAX, om.ROUTE_BIASED_SOFTMAX):
+        r = om.moe_forward(_cfg(T=T, d_model=d, d_ff=F, E=E, k=3, route=route),
+                           x, w_g, lambda e: ex[0],
+                           select_bias=rng.standard_normal(E) * 0.01)
+        np.testing.assert_allclose(r.out, _torch_ffn(x, *ex[0]), rtol=1e-12, atol=1e-12)
+    # one shared expert equal to the routed ones: 2 * FFN(x)
+    r = om.moe_forward(_cfg(T=T, d_model=d, d_ff=F, E=E, k=2, n_shared=1,
+                            route=om.ROUTE_BIASED_SOFTMAX),
+                       x, w_g, lambda e: ex[0], shared=lambda s: ex[0],
+                       select_bias=rng.standard_normal(E) * 0.01)
+    np.testing.assert_allclose(r.out, 2 * _torch_ffn(x, *ex[0]), rtol=1e-12, atol=1e-12)
+
+
+def test_dense_reductions():
+    check_dense_reductions()
+
+
+# ---------------------------------------------------------------- aux loss
+def check_aux_uniform_router():
+    """W_g = 0 makes every p = 1/E, so aux = alpha * E * sum f_i / E = k * alpha
+    for any f (sum f = k)."""
+    rng = np.random.default_rng(5)
+    for E, k, route in [(8, 2, om.ROUTE_SOFTMAX_TOPK), (64, 1, om.ROUTE_SOFTMAX_TOPK),
+                        (16, 4, om.ROUTE_TOPK_SOFTMAX), (256, 8, om.ROUTE_BIASED_SOFTMAX)]:
+        T, d = 32, 8
+        x = rng.standard_normal((T, d))
+        cfg = _cfg(T=T, d_model=d, d_ff=4, E=E, k=k, route=route, aux_alpha=0.01)
+        l = om.router_logits(x, np.zeros((d, E)))
+        g = om.gate(l, cfg, select_bias=rng.standard_normal(E) * 0.01)
+        disp = om.dispatch(g.idx, E, None)
+        f, P, aux = om.load_balance(cfg, l, g.p, disp.counts)
+        np.testing.assert_allclose(P, 1.0 / E, rtol=1e-15)
+        assert abs(f.sum() - k) < 1e-12
+        assert abs(aux - k * 0.01) < 1e-15
+
+
+def test_aux_uniform_router():
+    check_aux_uniform_router()
+
+
+def check_aux_hand_example():
+    """T=4, E=2, k=1, W_g = I: logits [0,0], [ln3,0], [0,ln3], [0,-ln3].
+    p = [.5,.5], [.75,.25], [.25,.75], [.75,.25]; argmax (lowest index on the
+    tie) = 0,0,1,0 -> f = [3/4, 1/4]; P = [2.25/4, 1.75/4];
+    aux = 0.01 * 2 * (0.75*0.5625 + 0.25*0.4375) = 0.010625."""
+    x = np.array([[0, 0], [LN3, 0], [0, LN3], [0, -LN3]], np.float64)
+    for aux_f in (om.AUX_ARGMAX, om.AUX_TOPK_COUNT):
+        cfg = OracleConfig(T=4, d_model=2, d_ff=1, E=2, k=1, aux_f=aux_f, aux_alpha=0.01)
+        l = om.router_logits(x, np.eye(2))
+        g = om.gate(l, cfg)
+        assert list(g.idx[:, 0]) == [0, 0, 1, 0]
+        disp = om.dispatch(g.idx, 2, None)
+        f, P, aux = om.load_balance(cfg, l, g.p, disp.counts)
+        np.testing.assert_allclose(f, [0.75, 0.25], rtol=0, atol=0)
+        np.testing.assert_allclose(P, [0.5625, 0.4375], rtol=1e-7)
+        assert abs(aux - 0.010625) < 1e-8
+
+
+def test_aux_hand_example():
+    check_aux_hand_example()
+
+
+def check_aux_nonnegative_and_argmax(seed=6):
+    rng = np.random.default_rng(seed)
+    T, d, E = 200, 16, 8
+    x = rng.standard_normal((T, d))
+    w = rng.standard_normal((d, E))
+    l = om.router_logits(x, w)
+    a = OracleConfig(T=T, d_model=d, d_ff=4, E=E, k=1, aux_f=om.AUX_ARGMAX)
+    b = OracleConfig(T=T, d_model=d, d_ff=4, E=E, k=1, aux_f=om.AUX_TOPK_COUNT)
+    g = om.gate(l, a)
+    disp = om.dispatch(g.idx, E, None)
+    fa, Pa, auxa = om.load_balance(a, l, g.p, disp.counts)
+    fb, Pb, auxb = om.load_balance(b, l, g.p, disp.counts)
+    # top-1 of the softmax is the argmax of the logits: both f forms agree
+    assert np.array_equal(fa, fb) and auxa == auxb and auxa >= 0
+
+
+def test_aux_nonnegative_and_argmax():
+    check_aux_nonnegative_and_argmax()
+
+
+# ---------------------------------------------------------------- dispatch
+def check_capacity_hand_example():
+    """T=8, E=2, k=1, CF=0.5 -> C = floor(0.5*8/2) = 2.  idx = 1,0,1,1,0,1,0,0:
+    expert 0 sees tokens 1,4,6,7 and keeps 1,4; expert 1 sees 0,2,3,5 and
+    keeps 0,2."""
+    cfg = OracleConfig(T=8, d_model=1, d_ff=1, E=2, k=1, capacity_factor=0.5)
+    C = om.capacity(cfg)
+    assert C == 2
+    idx = np.array([1, 0, 1, 1, 0, 1, 0, 0])[:, None]
+    d = om.dispatch(idx, 2, C)
+    assert list(d.counts) == [4, 4] and list(d.kept) == [2, 2]
+    assert list(d.offsets) == [0, 2, 4]
+    assert list(d.perm_token) == [1, 4, 0, 2]
+    assert list(d.slot_of) == [2, 0, 3, -1, 1, -1, -1, -1]
+    # min_capacity raises a small capacity
+    assert om.capacity(OracleConfig(T=8, d_model=1, d_ff=1, E=2, k=1,
+                                    capacity_factor=0.1, min_capacity=4)) == 4
+    assert om.capacity(OracleConfig(T=8, d_model=1, d_ff=1, E=2, k=1)) is None
+
+
+def test_capacity_hand_example():
+    check_capacity_hand_example()
+
+
+def check_dispatch_invariants(seed=7):
+    rng = np.random.default_rng(seed)
+    for T, E, k, C in [(100, 8, 2, None), (100, 8, 2, 7), (64, 16, 4, 3), (50, 4, 1, 0),
+                       (33, 5, 3, 1)]:
+        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)])
+        d = om.dispatch(idx, E, C)
+        flat = idx.reshape(-1)
+        # counts by plain counting
+        for e in range(E):
+            assert d.counts[e] == int(np.sum(flat == e))
+        cap = np.inf if C is None else C
+        assert np.all(d.kept <= cap) and np.all(d.kept == np.minimum(d.counts, cap))
+        assert d.offsets[0] == 0 and np.array_equal(np.diff(d.offsets), d.kept)
+        # walk the assignments in t*k+j order with a running counter per expert
+        seen = np.zeros(E, np.int64)
+        rows_of_e = {e: [] for e in range(E)}
+        for a in range(T * k):
+            e = flat[a]
+            r = seen[e]
+            seen[e] += 1
+            if r < cap:
+                assert d.slot_of[a] == d.offsets[e] + r
+                rows_of_e[e].append(a)
+            else:
+                assert d.slot_of[a] == -1
+        # perm_token is a bijection onto the kept assignments, ordered in t*k+j
+        kept_slots = d.slot_of[d.slot_of >= 0]
+        assert sorted(kept_slots.tolist()) == list(range(int(d.offsets[-1])))
+        for e in range(E):
+            toks = d.perm_token[d.offsets[e]:d.offsets[e + 1]]
+            assert list(toks) == [a // k for a in rows_of_e[e]]
+
+
+def test_dispatch_invariants():
+    check_dispatch_invariants()
+
+
+# ---------------------------------------------------------------- whole layer
+def _brute_forward(cfg, x, w_g, ex, sh, select_bias=None, logit_bias=None):
+    """Token by token: route, count earlier assignments of the same expert in
+    t*k+j order to decide drops, add w * FFN_e(x_t) (torch MLP), add shared."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+    l = om.router_logits(x, w_g, logit_bias)
+    g = om.gate(l, cfg, select_bias)
+    C = om.capacity(cfg)
+    seen = [0] * E
+    out = np.zeros((T, cfg.d_model))
+    for t in range(T):
+        for j in range(k):
+            e = int(g.idx[t, j])
+            r = seen[e]
+            seen[e] += 1
+            if C is not None and r >= C:
+                continue
+            out[t] += g.w[t, j] * _torch_ffn(x[t:t + 1], *ex[e])[0]
+        for s in range(cfg.n_shared):
+            out[t] += _torch_ffn(x[t:t + 1], *sh[s])[0]
+    return out
+
+
+def check_forward_bruteforce(seed=8):
+    rng = np.random.default_rng(seed)
+    cases = [
+        dict(T=24, d_model=8, d_ff=12, E=4, k=2, route=om.ROUTE_SOFTMAX_TOPK),
+        dict(T=24, d_model=8, d_ff=12, E=4, k=1, route=om.ROUTE_SOFTMAX_TOPK,
+             renorm=False, capacity_factor=1.0),
+        dict(T=30, d_model=6, d_ff=10, E=5, k=2, route=om.ROUTE_TOPK_SOFTMAX,
+             capacity_factor=1.5),
+        dict(T=20, d_model=8, d_ff=8, E=8, k=3, n_shared=1, route=om.ROUTE_BIASED_SOFTMAX),
+    ]
+    for kw in cases:
+        cfg = OracleConfig(**kw)
+        x, w_g, ex, sh = _rand_layer(rng, cfg.T, cfg.d_model, cfg.d_ff, cfg.E, cfg.n_shared)
+        sb = rng.standard_normal(cfg.E) * 0.01
+        lb = rng.standard_normal(cfg.E).astype(np.float32)
+        r = om.moe_forward(cfg, x, w_g, lambda e: ex[e], lambda s: sh[s],
+                           select_bias=sb, logit_bias=lb)
+        want = _brute_forward(cfg, x, w_g, ex, sh, select_bias=sb, logit_bias=lb)
+        np.testing.assert_allclose(r.out, want, rtol=1e-11, atol=1e-12)
+        # a row subset gives the same rows
+        rows = [0, 3, cfg.T - 1]
+        rs = om.moe_forward(cfg, x, w_g, lambda e: ex[e], lambda s: sh[s],
+                            select_bias=sb, logit_bias=lb, rows=rows)
+        np.testing.assert_allclose(rs.out, r.out[rows], rtol=0, atol=1e-13)
+
+
+def test_forward_bruteforce():
+    check_forward_bruteforce()
+
+
+def check_dropped_tokens_output_zero():
+    """Capacity 0 (CF tiny) drops everything: the routed part is exactly 0."""
+    rng = np.random.default_rng(9)
+    cfg = OracleConfig(T=16, d_model=4, d_ff=6, E=4, k=1, capacity_factor=0.01)
+    x, w_g, ex, _ = _rand_layer(rng, 16, 4, 6, 4)
+    r = om.moe_forward(cfg, x, w_g, lambda e: ex[e])
+    assert r.C == 0 and np.all(r.disp.slot_of == -1) and np.all(r.out == 0)
+
+
+def test_dropped_tokens_output_zero():
+    check_dropped_tokens_output_zero()
+
+
+# ---------------------------------------------------------------- planted mistakes
+ALL_CHECKS = [check_golden_pages_values, check_selection_bruteforce, check_hand_gate_examples,
+              check_softmax_topk_equals_topk_softmax, check_weights_sum_to_one,
+              check_softmax_basic, check_router_logits, check_gelu_closed_form,
+              check_dense_reductions, check_aux_uniform_router, check_aux_hand_example,
+              check_aux_nonnegative_and_argmax, check_capacity_hand_example,
+              check_dispatch_invariants, check_forward_bruteforce,
+              check_dropped_tokens_output_zero]
+
+
+def _some_pin_fails():
+    failed = []
+    for c in ALL_CHECKS:
+        try:
+            c()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(c.__name__)
+    return failed
+
+
+def test_all_pins_pass_unplanted():
+    assert _some_pin_fails() == []
+
+
+def _tanh_gelu(v):
+    v = np.asarray(v, np.float64)
+    return 0.5 * v * (1 + np.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+
+
+def _ffn_transposed(xe, w1, b1, w2, b2):
+    # plausible slip: second layer multiplied without the transpose of W2 when
+    # d == d_ff would go unnoticed; with d != d_ff this must raise or differ
+    h = om.gelu(np.asarray(xe) @ np.asarray(w1).T + (0 if b1 is None else b1))
+    return h @ np.asarray(w2).reshape(np.asarray(w2).shape[::-1]) + (0 if b2 is None else b2)
+
+
+def _select_highest_index_on_ties(score, k):
+    s = np.asarray(score, np.float64)
+    order = np.argsort(-s[:, ::-1], axis=-1, kind="stable")
+    order = s.shape[1] - 1 - order
+    m = min(k + 1, s.shape[1])
+    top = np.take_along_axis(s, order[:, :m], axis=-1)
+    return order[:, :k], np.min(top[:, :-1] - top[:, 1:], axis=-1)
+
+
+def _capacity_ceil(cfg):
+    if cfg.capacity_factor <= 0:
+        return None
+    return max(int(math.ceil(cfg.capacity_factor * cfg.T / cfg.E)), cfg.min_capacity)
+
+
+_orig_load_balance = om.load_balance
+
+
+@pytest.mark.parametrize("name,patch", [
+    ("tanh GELU", ("gelu", _tanh_gelu)),
+    ("untransposed W2", ("expert_ffn", _ffn_transposed)),
+    ("highest index wins ties", ("select_topk", _select_highest_index_on_ties)),
+    ("ceil capacity", ("capacity", _capacity_ceil)),
+    ("aux without the E factor", ("load_balance",
+                                  lambda c, l, p, n: (lambda r: (r[0], r[1], r[2] / c.E))(
+                                      _orig_load_balance(c, l, p, n)))),
+])
+def test_plant_mistake_is_caught(monkeypatch, name, patch):
+    attr, fn = patch
+    monkeypatch.setattr(om, attr, fn)
+    assert _some_pin_fails(), f"planted mistake '{name}' passed every pin"
