@@ -1,0 +1,174 @@
+/*
+ * moe.h - C ABI of libmoe: the forward pass of a sparse Mixture-of-Experts FFN
+ * layer on one NVIDIA B300 (sm_103a).
+ *
+ * The operation (notation of the pages this library restates):
+ *   logits = x . W_g (+ logit_bias)                  router, no bias by default
+ *   gate   : softmax over E -> top-k -> renormalise   ("SparseMoEGate")
+ *          | top-k on logits -> softmax over the k    ("top_k_gating")
+ *          | top-k on softmax + select_bias, weights from the unbiased
+ *            softmax renormalised                     (DeepSeek-V3 bias)
+ *   C      = max(floor(CF * T / E), min_capacity) when CF > 0; the assignments
+ *            of an expert are ranked in ascending t*k + j and kept iff rank < C
+ *   y      = sum_kept w[t,j] * FFN_{idx[t,j]}(x_t) + sum_s FFN_s(x_t)
+ *   FFN(v) = GELU_erf(v W1^T + b1) W2^T + b2
+ *   f_i, P_i, aux = alpha * E * sum_i f_i P_i          (Switch load balance)
+ *
+ * Sources: "混合专家大模型MoE架构选型与部署实践教程" §五 (SparseMoEGate,
+ * SimpleMoELayer); "[BEE-30064] 混合專家架構與服務", 專家路由工作原理 (routing
+ * steps 1-5, load_balance_loss); "AI-Research-SKILLs MoE 训练实战…全指南" §3.1,
+ * §4.3, §7.1, §8.2; "第7章 Mixture of Experts" §7.1-§7.4.
+ *
+ * Conventions for every entry point
+ *  - Ownership: the caller owns every buffer.  Unless stated otherwise a
+ *    pointer is a DEVICE pointer on the current CUDA device.  The library never
+ *    allocates device memory; scratch comes from the caller's workspace `ws`
+ *    of at least moe_workspace_size() bytes, initialised once with
+ *    moe_workspace_init().
+ *  - Execution: every call validates its arguments on the host first; on an
+ *    error it returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE with NOTHING enqueued.  Otherwise it enqueues kernels on
+ *    `stream` (a cudaStream_t; NULL = legacy default stream) and returns
+ *    without synchronising.  MOE_ERR_CUDA reports a failed launch.
+ *  - Device-side give-ups (a bounded wait inside a kernel that ran out) set a
+ *    status word in `ws`; moe_check_status() synchronises and reports it.
+ *  - Layouts are row-major.  Expert weights use nn.Linear's [out, in]
+ *    (K-contiguous) layout.  W_g is [d_model, E].  Element type of x, W_g,
+ *    expert weights/biases and the activations is cfg->dtype (fp32 or bf16);
+ *    routing weights, logits, f, P and aux are always fp32, indices int32.
+ *  - Determinism: outputs are bitwise reproducible run to run; no output is
+ *    produced with floating-point atomics.
+ *  - Dropped assignments have slot_of = -1 and contribute 0 to the output.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* moe_stream;   /* a cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* bad pointer / size / enum value            */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. bf16 with d % 8 != 0) */
+  MOE_ERR_WORKSPACE = 3,     /* ws NULL, too small or misaligned           */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed       */
+  MOE_ERR_TIMEOUT = 5        /* a device-side bounded wait gave up         */
+} moe_status;
+
+typedef enum {
+  MOE_ROUTE_SOFTMAX_TOPK = 0,    /* softmax over E, top-k, renormalise if cfg.renorm */
+  MOE_ROUTE_TOPK_SOFTMAX = 1,    /* top-k on logits, softmax over the k              */
+  MOE_ROUTE_BIASED_SOFTMAX = 2   /* select on softmax + select_bias; weights = unbiased
+                                    softmax renormalised over the k                  */
+} moe_route_kind;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  MOE_AUX_TOPK_COUNT = 0,   /* f_i = (#assignments to i) / T, sum f = k   */
+  MOE_AUX_ARGMAX = 1        /* f_i = (#tokens whose largest logit is i) / T */
+} moe_aux_f;
+
+/* The problem statement.  All fields are read by every entry point. */
+typedef struct {
+  int32_t T;               /* tokens, >= 0                                  */
+  int32_t d_model;         /* d, > 0                                        */
+  int32_t d_ff;            /* F, > 0                                        */
+  int32_t E;               /* routed experts, 1..256                        */
+  int32_t k;               /* experts per token, 1..min(E, 16)              */
+  int32_t n_shared;        /* always-on shared experts, 0..4                */
+  float capacity_factor;   /* CF; <= 0 means no capacity limit              */
+  int32_t min_capacity;    /* lower bound on C when CF > 0, >= 0            */
+  int32_t route;           /* moe_route_kind                                */
+  int32_t renorm;          /* MOE_ROUTE_SOFTMAX_TOPK: 1 = renormalise over k */
+  int32_t dtype;           /* moe_dtype                                     */
+  int32_t has_bias;        /* 1: expert biases b1 [E,F], b2 [E,d] are given  */
+  float aux_alpha;         /* alpha of the aux loss                         */
+  int32_t aux_f;           /* moe_aux_f                                     */
+} moe_config;
+
+/* Bytes of workspace the entry points below need for `cfg` (host only). */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Clears the device status word at the head of `ws` (stream-ordered).  Call
+ * once after allocating `ws`. */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Router + gating + load-balance statistics.
+ *   x [T,d] dtype; w_g [d,E] dtype; logit_bias [E] fp32 or NULL (added to the
+ *   logits); select_bias [E] fp32 or NULL (MOE_ROUTE_BIASED_SOFTMAX only).
+ *   Outputs: logits [T,E] fp32 or NULL; topk_idx [T,k] int32 (descending
+ *   selection score, lower expert index first on equal scores); topk_w [T,k]
+ *   fp32; f [E], P [E] fp32; aux [1] fp32.  f and P count all T tokens
+ *   before any capacity drop. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
+                     const float* logit_bias, const float* select_bias,
+                     float* logits, int32_t* topk_idx, float* topk_w,
+                     float* f, float* P, float* aux,
+                     void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Dispatch: histogram, exclusive scan, capacity cut and row gather.
+ *   topk_idx [T,k] int32 from moe_route.
+ *   Outputs: counts [E] (assignments before the cut), kept [E] (= min(counts,
+ *   C)), offsets [E+1] (exclusive scan of kept), perm_token [T*k] (token of
+ *   each expert-ordered row; entries >= offsets[E] are unspecified), slot_of
+ *   [T*k] (row of assignment t*k+j in x_perm, or -1 when dropped), x_perm
+ *   [T*k, d] dtype (rows >= offsets[E] unspecified). */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       int32_t* counts, int32_t* kept, int32_t* offsets,
+                       int32_t* perm_token, int32_t* slot_of, void* x_perm,
+                       void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Expert MLPs as a grouped GEMM over the expert-contiguous rows.
+ *   x_perm [T*k, d], offsets [E+1] (device; read on the device only).
+ *   w1 [E,F,d], b1 [E,F] or NULL, w2 [E,d,F], b2 [E,d] or NULL.
+ *   Shared experts (cfg.n_shared > 0): x [T,d], ws1 [S,F,d], wsb1 [S,F] or
+ *   NULL, ws2 [S,d,F], wsb2 [S,d] or NULL, output y_shared [S,T,d].
+ *   Output y_perm [T*k, d] dtype: row r = FFN_e(x_perm[r]) for the expert e
+ *   whose range holds r; rows >= offsets[E] unspecified. */
+moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                           const void* w1, const void* b1, const void* w2, const void* b2,
+                           const void* x, const void* ws1, const void* wsb1,
+                           const void* ws2, const void* wsb2,
+                           void* y_perm, void* y_shared,
+                           void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Gate-weighted un-permute: out[t] = sum_{j: slot_of[t*k+j] >= 0}
+ * topk_w[t,j] * y_perm[slot_of[t*k+j]] + sum_s y_shared[s,t], accumulated in
+ * fp32 in ascending j then s, stored once in dtype.  y_shared may be NULL
+ * when n_shared = 0. */
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_of,
+                       const float* topk_w, const void* y_shared, void* out,
+                       moe_stream stream);
+
+/* The whole layer: route -> permute -> grouped FFN -> combine, all stream
+ * ordered with no host synchronisation.  Intermediates live in `ws`.
+ *   Outputs: out [T,d] dtype; topk_idx [T,k]; topk_w [T,k]; counts [E];
+ *   f [E]; P [E]; aux [1].  Any of topk_idx .. aux may be NULL except
+ *   out. */
+moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
+                       const float* logit_bias, const float* select_bias,
+                       const void* w1, const void* b1, const void* w2, const void* b2,
+                       const void* ws1, const void* wsb1, const void* ws2, const void* wsb2,
+                       void* out, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                       float* f, float* P, float* aux,
+                       void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Synchronises `stream`, reads and clears the device status word of `ws`.
+ * Returns MOE_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * check, MOE_ERR_CUDA if the stream reports an error, else MOE_OK. */
+moe_status moe_check_status(void* ws, moe_stream stream);
+
+/* Static string for a status code (host only). */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,207 @@
+"""Comparison of a device run of the MoE layer with the oracle.
+
+TEST INFRASTRUCTURE ONLY (used by ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py``).  It imports nothing from the product
+package: device results arrive as torch tensors or numpy arrays.
+
+Acceptance rules:
+* expert indices, per-expert counts, kept counts, offsets, the permutation and
+  the dropped set are bit-exact, except for tokens whose neighbouring
+  selection scores (among the k+1 best) are closer than NEAR_TIE; those are
+  reported, and the oracle is re-run with the device's choice for them so
+  that everything downstream is still compared exactly;
+* f is exact (a ratio of integers, compared after rounding the oracle's value
+  to float32), P and aux within 1e-5 relative, gate weights within 1e-5;
+* layer output: relative L2 <= 1e-2 and max-abs <= 5e-2 x RMS(reference) for
+  bf16 layers; relative L2 <= 1e-4 for fp32 layers.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import moe_oracle as om
+
+NEAR_TIE = 1e-5
+TOL_BF16_REL_L2 = 1e-2
+TOL_BF16_MAX_ABS_RMS = 5e-2
+TOL_F32_REL_L2 = 1e-4
+TOL_P_REL = 1e-5
+TOL_AUX_REL = 1e-5
+TOL_W_ABS = 1e-5
+
+
+def oracle_config(cfg: dict) -> om.OracleConfig:
+    """The oracle's view of a workload dict.  The capacity factor is rounded to
+    float32 first: that is the value the library receives."""
+    return om.OracleConfig(
+        T=int(cfg["T"]), d_model=int(cfg["d_model"]), d_ff=int(cfg["d_ff"]), E=int(cfg["E"]),
+        k=int(cfg["k"]), n_shared=int(cfg.get("n_shared", 0)),
+        capacity_factor=float(np.float32(cfg.get("capacity_factor", 0.0))),
+        min_capacity=int(cfg.get("min_capacity", 0)), route=cfg["route"],
+        renorm=bool(cfg.get("renorm", 1)),
+        aux_alpha=float(np.float32(cfg.get("aux_alpha", 0.01))),
+        aux_f=cfg.get("aux_f", om.AUX_TOPK_COUNT))
+
+
+def np64(t) -> Optional[np.ndarray]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def np32(t) -> Optional[np.ndarray]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float32)
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+class LazyExperts:
+    """expert e -> (w1, b1, w2, b2) in float64, copied from the (device)
+    tensors one expert at a time, so full-size layers never hold every
+    expert in float64 on the host at once."""
+
+    def __init__(self, w1, b1, w2, b2):
+        self.w1, self.b1, self.w2, self.b2 = w1, b1, w2, b2
+
+    def __call__(self, e: int):
+        return (np64(self.w1[e]), None if self.b1 is None else np64(self.b1[e]),
+                np64(self.w2[e]), None if self.b2 is None else np64(self.b2[e]))
+
+
+def run_oracle(cfg: dict, inputs: dict, rows: Optional[Sequence[int]] = None,
+               idx_override: Optional[dict] = None) -> om.ForwardResult:
+    ocfg = oracle_config(cfg)
+    experts = LazyExperts(inputs["w1"], inputs.get("b1"), inputs["w2"], inputs.get("b2"))
+    shared = None
+    if ocfg.n_shared:
+        shared = LazyExperts(inputs["ws1"], inputs.get("wsb1"), inputs["ws2"], inputs.get("wsb2"))
+    return om.moe_forward(ocfg, np64(inputs["x"]), np64(inputs["w_g"]), experts, shared,
+                          logit_bias=np32(inputs.get("logit_bias")),
+                          select_bias=np64(inputs.get("select_bias")),
+                          rows=rows, idx_override=idx_override)
+
+
+@dataclass
+class Report:
+    near_tie: list = field(default_factory=list)       # tokens within NEAR_TIE
+    overridden: list = field(default_factory=list)     # near-tie tokens whose choice differs
+    rel_l2: float = 0.0
+    max_abs_over_rms: float = 0.0
+    checked_rows: int = 0
+    notes: list = field(default_factory=list)
+
+    def summary(self) -> str:
+        return (f"rows={self.checked_rows} rel_l2={self.rel_l2:.3e} "
+                f"maxabs/rms={self.max_abs_over_rms:.3e} near_tie={len(self.near_tie)} "
+                f"overridden={len(self.overridden)}")
+
+
+def _near_tie_and_override(ref: om.ForwardResult, gpu_idx: np.ndarray):
+    nt = np.nonzero(ref.gate.margin < NEAR_TIE)[0]
+    override = {}
+    for t in nt:
+        if not np.array_equal(gpu_idx[t], ref.gate.idx[t]):
+            override[int(t)] = gpu_idx[t].astype(np.int64)
+    return [int(t) for t in nt], override
+
+
+def compare_routing(cfg: dict, ref: om.ForwardResult, gpu: dict, rep: Report) -> None:
+    """idx / w / counts / f / P / aux (the dict holds numpy arrays)."""
+    idx = np.asarray(gpu["topk_idx"]).astype(np.int64)
+    T = idx.shape[0]
+    ok = np.ones(T, bool)
+    ok[list(rep.overridden)] = False
+    bad = np.nonzero(np.any(idx != ref.gate.idx, axis=1) & ok)[0]
+    assert bad.size == 0, (f"expert indices differ on {bad.size} tokens outside the near-tie "
+                           f"set, e.g. t={bad[:5].tolist()}: gpu={idx[bad[:3]].tolist()} "
+                           f"oracle={ref.gate.idx[bad[:3]].tolist()} "
+                           f"margin={ref.gate.margin[bad[:3]].tolist()}")
+    if "topk_w" in gpu:
+        dw = np.abs(np.asarray(gpu["topk_w"], np.float64) - ref.gate.w)
+        assert dw.max() <= TOL_W_ABS, f"gate weights differ by {dw.max():.3e}"
+    if "counts" in gpu:
+        assert np.array_equal(np.asarray(gpu["counts"]).astype(np.int64), ref.disp.counts), \
+            "per-expert counts differ"
+    if "f" in gpu:
+        f_ref = ref.f.astype(np.float32)
+        f_gpu = np.asarray(gpu["f"], np.float32)
+        if ref.gate is not None and oracle_config(cfg).aux_f == om.AUX_ARGMAX and rep.near_tie:
+            slack = len(rep.near_tie) / T
+            assert np.max(np.abs(f_gpu - f_ref)) <= slack + 1e-7, "f differs"
+        else:
+            assert np.array_equal(f_gpu, f_ref), \
+                f"f differs: max {np.max(np.abs(f_gpu - f_ref))}"
+    if "P" in gpu:
+        P = np.asarray(gpu["P"], np.float64)
+        err = np.abs(P - ref.P) / np.maximum(np.abs(ref.P), 1e-30)
+        assert err.max() <= TOL_P_REL, f"P relative error {err.max():.3e}"
+    if "aux" in gpu:
+        a = float(np.asarray(gpu["aux"]).reshape(-1)[0])
+        slack = 0.0
+        if oracle_config(cfg).aux_f == om.AUX_ARGMAX and rep.near_tie:
+            slack = cfg["aux_alpha"] * cfg["E"] * len(rep.near_tie) / T
+        assert abs(a - ref.aux) <= TOL_AUX_REL * abs(ref.aux) + slack + 1e-12, \
+            f"aux {a} vs {ref.aux}"
+
+
+def compare_dispatch(ref: om.ForwardResult, gpu: dict) -> None:
+    """kept / offsets / perm_token / slot_of bit-exact; x_perm rows = x[perm_token]."""
+    d = ref.disp
+    if "kept" in gpu:
+        assert np.array_equal(np.asarray(gpu["kept"]).astype(np.int64), d.kept), "kept differs"
+    if "offsets" in gpu:
+        assert np.array_equal(np.asarray(gpu["offsets"]).astype(np.int64), d.offsets), \
+            "offsets differ"
+    n = int(d.offsets[-1])
+    if "perm_token" in gpu:
+        assert np.array_equal(np.asarray(gpu["perm_token"])[:n].astype(np.int64),
+                              d.perm_token), "perm_token differs"
+    if "slot_of" in gpu:
+        assert np.array_equal(np.asarray(gpu["slot_of"]).astype(np.int64), d.slot_of), \
+            "slot_of (kept rows / dropped set) differs"
+
+
+def compare_output(cfg: dict, ref: om.ForwardResult, out_gpu: np.ndarray, rep: Report) -> None:
+    o = np.asarray(out_gpu, np.float64)[ref.rows]
+    r = ref.out
+    diff = o - r
+    rms = float(np.sqrt(np.mean(r * r))) if r.size else 0.0
+    rel = float(np.linalg.norm(diff) / max(np.linalg.norm(r), 1e-300)) if r.size else 0.0
+    mx = float(np.max(np.abs(diff)) / max(rms, 1e-300)) if r.size else 0.0
+    rep.rel_l2, rep.max_abs_over_rms, rep.checked_rows = rel, mx, len(ref.rows)
+    if not r.size or np.linalg.norm(r) == 0.0:
+        assert np.max(np.abs(o), initial=0.0) == 0.0, "output should be exactly zero"
+        return
+    if cfg["dtype"] == "f32":
+        assert rel <= TOL_F32_REL_L2, f"fp32 rel-L2 {rel:.3e} > {TOL_F32_REL_L2}"
+    else:
+        assert rel <= TOL_BF16_REL_L2, f"bf16 rel-L2 {rel:.3e} > {TOL_BF16_REL_L2}"
+        assert mx <= TOL_BF16_MAX_ABS_RMS, f"bf16 max-abs/RMS {mx:.3e} > {TOL_BF16_MAX_ABS_RMS}"
+
+
+def check_layer(cfg: dict, inputs: dict, gpu: dict, rows: Optional[Sequence[int]] = None
+                ) -> Report:
+    """Full acceptance check of one device run against the oracle.
+
+    ``gpu`` maps output names to numpy arrays: topk_idx, topk_w, counts, f, P,
+    aux, out (and optionally kept, offsets, perm_token, slot_of)."""
+    rep = Report()
+    ref = run_oracle(cfg, inputs, rows=rows)
+    rep.near_tie, override = _near_tie_and_override(ref, np.asarray(gpu["topk_idx"]))
+    if override:
+        rep.overridden = sorted(override)
+        ref = run_oracle(cfg, inputs, rows=rows, idx_override=override)
+    compare_routing(cfg, ref, gpu, rep)
+    compare_dispatch(ref, gpu)
+    if "out" in gpu:
+        compare_output(cfg, ref, gpu["out"], rep)
+    return rep

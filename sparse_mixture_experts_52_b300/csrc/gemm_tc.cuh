@@ -1,0 +1,313 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   out[row, n] = epilogue( sum_k A[a_row, k] * B_g[n, k] )   for every group g
+//
+// A is [rows, K] bf16 (K-major), B_g is expert g's nn.Linear weight [N, K]
+// bf16 (K-major), accumulation is fp32 in tensor memory.  One persistent CTA
+// per SM walks the tile list derived on the device from the dispatch offsets
+// (groups.cuh).  Warp roles inside a CTA (192 threads):
+//   warp 0     : TMA producer (one lane) - A and B tiles into a STAGES-deep ring
+//   warp 1     : TMEM owner and MMA issuer (one lane) - 128 x BN x 16 MMAs
+//   warps 2..5 : epilogue - tcgen05.ld, bias / GELU, convert, store
+// The accumulator is double-buffered in TMEM (2 x BN fp32 columns) so the
+// epilogue of one tile overlaps the main loop of the next.
+//
+// Every wait is bounded: a wait that runs out records MOE_DEV_ERR_* in the
+// status word, raises the CTA abort flag, drains what this CTA has in flight
+// and returns, so a bad launch can never hang the GPU.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+#include "groups.cuh"
+#include "ptx_sm100.cuh"
+
+namespace moe {
+
+enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_BF16 = 2 };
+enum : int { DEV_ERR_WAIT_PRODUCER = 1, DEV_ERR_WAIT_MMA = 2, DEV_ERR_WAIT_EPILOGUE = 4 };
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: any single wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s: draining after a give-up
+
+struct TcArgs {
+  GroupSpec gs;
+  int N, K;
+  void* out;                   // routed groups' rows
+  void* out1;                  // shared groups' rows (row 0 of shared group 0)
+  int64_t ldo;                 // elements between output rows
+  const __nv_bfloat16* bias0;  // [E, N] or null
+  const __nv_bfloat16* bias1;  // [n_shared, N] or null
+  int* err;                    // device status word
+};
+
+__device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uint64_t limit) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > limit) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float gelu_erf(float v) {
+  return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+}
+
+template <int BN, int STAGES>
+struct TcSmem {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  struct Ctrl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    GroupTable tb;
+  };
+  static constexpr size_t bytes() {
+    return 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+  }
+};
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(192, 1)
+k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+          const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
+          const TcArgs args) {
+  using L = TcSmem<BN, STAGES>;
+  constexpr int BM = L::BM, BK = L::BK;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  static_assert((BN & (BN - 1)) == 0, "TMEM columns must be a power of two");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * L::A_BYTES;
+  auto& c = *reinterpret_cast<typename L::Ctrl*>(smem + STAGES * L::STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const GroupSpec& gs = args.gs;
+  const int G = gs.E + gs.n_shared;
+  const int n_tiles = (args.N + BN - 1) / BN;
+  const int KB = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&c.tfull[a], 1);
+      mbar_init(&c.tempty[a], 4);
+    }
+    mbar_init(&c.drain, 1);
+    c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mA0);
+    tma_prefetch_desc(&mB0);
+    if (gs.n_shared > 0) {
+      tma_prefetch_desc(&mA1);
+      tma_prefetch_desc(&mB1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  build_group_table<BM>(gs, n_tiles, c.tb);   // synchronises the block
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  const int total = c.tb.tile_start[G];
+  volatile int* abort_flag = &c.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) armed[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int g, m_blk, n_blk;
+        decode_tile<BM>(c.tb, G, t, g, m_blk, n_blk);
+        const bool routed = g < gs.E;
+        const CUtensorMap* ma = (routed || gs.shared_a_sel == 0) ? &mA0 : &mA1;
+        const CUtensorMap* mb = routed ? &mB0 : &mB1;
+        const int bz = routed ? (gs.offsets ? g : 0) : g - gs.E;
+        const int arow = c.tb.a_row0[g] + m_blk * BM;
+        const int ncol = n_blk * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&c.empty[stage], phase ^ 1u, abort_flag, args.err,
+                                 DEV_ERR_WAIT_PRODUCER, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&c.full[stage], L::STAGE_BYTES);
+          tma_load_2d(sA + stage * L::A_BYTES, ma, &c.full[stage], kb * BK, arow);
+          tma_load_3d(sB + stage * L::B_BYTES, mb, &c.full[stage], kb * BK, ncol, bz);
+#pragma unroll
+          for (int s = 0; s < STAGES; ++s) armed[s] += (s == stage) ? 1u : 0u;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every load already issued land before the CTA exits
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s)
+          if (armed[s]) wait_timeout(&c.full[s], (armed[s] - 1u) & 1u, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait_bounded(&c.tempty[acc], acc_phase ^ 1u, abort_flag, args.err,
+                               DEV_ERR_WAIT_MMA, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(&c.full[stage], phase, abort_flag, args.err, DEV_ERR_WAIT_MMA,
+                                 kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * L::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * L::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            umma_bf16_f32(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32),
+                          sdesc_kmajor_sw128(b0 + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&c.empty[stage]);   // frees this smem stage once read
+          issued = true;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&c.tfull[acc]);       // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok && issued) {  // wait for the MMAs in flight before TMEM is freed
+        umma_commit(&c.drain);
+        wait_timeout(&c.drain, 0, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int g, m_blk, n_blk;
+      decode_tile<BM>(c.tb, G, t, g, m_blk, n_blk);
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait_bounded(&c.tfull[acc], acc_phase, abort_flag, args.err,
+                               DEV_ERR_WAIT_EPILOGUE, kWaitLimitNs)
+                 ? 1
+                 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+
+      const bool routed = g < gs.E;
+      const int row_in_grp = m_blk * BM + q * 32 + lane;
+      const bool valid = row_in_grp < c.tb.rows[g];
+      const int64_t orow = static_cast<int64_t>(c.tb.out_row0[g]) + row_in_grp;
+      const __nv_bfloat16* bias = nullptr;
+      if (EPI != EPI_F32) {
+        if (routed && args.bias0) bias = args.bias0 + static_cast<int64_t>(gs.offsets ? g : 0) * args.N;
+        if (!routed && args.bias1) bias = args.bias1 + static_cast<int64_t>(g - gs.E) * args.N;
+      }
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 16; ++cc) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(trow + cc * 16, r);
+        tmem_wait_ld();
+        const int col = n_blk * BN + cc * 16;
+        if (!valid || col >= args.N) continue;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+        if (EPI == EPI_F32) {
+          float* o = static_cast<float*>(routed ? args.out : args.out1) + orow * args.ldo + col;
+          if (col + 16 <= args.N) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(o + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+            for (int i = 0; i < 16 && col + i < args.N; ++i) o[i] = v[i];
+          }
+        } else {
+          if (bias) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (col + i < args.N) v[i] += __bfloat162float(bias[col + i]);
+          }
+          if (EPI == EPI_GELU_BF16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+          }
+          __nv_bfloat16* o =
+              static_cast<__nv_bfloat16*>(routed ? args.out : args.out1) + orow * args.ldo + col;
+          if (col + 16 <= args.N) {
+            uint32_t p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+              p[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(o) = make_uint4(p[0], p[1], p[2], p[3]);
+            *reinterpret_cast<uint4*>(o + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+          } else {
+            for (int i = 0; i < 16 && col + i < args.N; ++i) o[i] = __float2bfloat16_rn(v[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,282 @@
+"""ctypes binding of libmoe (include/moe.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; torch supplies device
+memory and the current stream.  Calls raise ``MoEError`` on any non-OK status,
+and loading fails loudly when ``libmoe.so`` has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+ROUTES = {"softmax_topk": 0, "topk_softmax": 1, "biased_softmax": 2}
+DTYPES = {"f32": 0, "bf16": 1}
+AUX_F = {"topk_count": 0, "argmax": 1}
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        self.fn = fn
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+class Config(ctypes.Structure):
+    """moe_config of include/moe.h (field order and types must match)."""
+    _fields_ = [
+        ("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+        ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+        ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
+        ("route", ctypes.c_int32), ("renorm", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("has_bias", ctypes.c_int32), ("aux_alpha", ctypes.c_float), ("aux_f", ctypes.c_int32),
+    ]
+
+
+def make_config(cfg: dict) -> Config:
+    """Config from a workload dict (keys as in ``synth.WORKLOADS``)."""
+    c = Config()
+    c.T, c.d_model, c.d_ff = int(cfg["T"]), int(cfg["d_model"]), int(cfg["d_ff"])
+    c.E, c.k, c.n_shared = int(cfg["E"]), int(cfg["k"]), int(cfg.get("n_shared", 0))
+    c.capacity_factor = float(cfg.get("capacity_factor", 0.0))
+    c.min_capacity = int(cfg.get("min_capacity", 0))
+    r = cfg.get("route", "softmax_topk")
+    c.route = ROUTES[r] if isinstance(r, str) else int(r)
+    c.renorm = int(cfg.get("renorm", 1))
+    dt = cfg.get("dtype", "bf16")
+    c.dtype = DTYPES[dt] if isinstance(dt, str) else int(dt)
+    c.has_bias = int(cfg.get("has_bias", 0))
+    c.aux_alpha = float(cfg.get("aux_alpha", 0.01))
+    af = cfg.get("aux_f", "topk_count")
+    c.aux_f = AUX_F[af] if isinstance(af, str) else int(af)
+    return c
+
+
+_lib = None
+_P = ctypes.c_void_p
+_CFG = ctypes.POINTER(Config)
+_SIGNATURES = {
+    "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
+    "moe_workspace_init": [_P, ctypes.c_size_t, _P],
+    "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_permute": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                        ctypes.c_size_t, _P],
+    "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P],
+    "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                    _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_check_status": [_P, _P],
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmoe (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoEError("load libmoe.so", -1) from FileNotFoundError(
+                f"{LIB_PATH} missing: run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.moe_status_string.argtypes = [ctypes.c_int]
+        L.moe_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().moe_status_string(int(s)).decode()
+
+
+def _call(name: str, *args) -> None:
+    s = getattr(lib(), name)(*args)
+    if s != 0:
+        raise MoEError(name, s)
+
+
+def _p(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _want(t: Optional[torch.Tensor], name: str, shape, dtype, allow_none=False):
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+# ------------------------------------------------------------------ workspace
+def workspace_size(cfg: dict) -> int:
+    n = ctypes.c_size_t(0)
+    _call("moe_workspace_size", ctypes.byref(make_config(cfg)), ctypes.byref(n))
+    return int(n.value)
+
+
+def new_workspace(cfg: dict, device="cuda", stream=None) -> torch.Tensor:
+    """Allocates (through torch) and initialises a workspace for ``cfg``."""
+    n = workspace_size(cfg)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _call("moe_workspace_init", _p(ws), ws.numel(), _stream(stream))
+    return ws
+
+
+def check_status(ws: torch.Tensor, stream=None) -> None:
+    _call("moe_check_status", _p(ws), _stream(stream))
+
+
+# ------------------------------------------------------------------ steps
+def route(cfg, x, w_g, topk_idx, topk_w, f, P, aux, ws, logit_bias=None, select_bias=None,
+          logits=None, stream=None):
+    T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x, "x", (T, d), dt)
+    _want(w_g, "w_g", (d, E), dt)
+    _want(topk_idx, "topk_idx", (T, k), torch.int32)
+    _want(topk_w, "topk_w", (T, k), torch.float32)
+    _want(f, "f", (E,), torch.float32)
+    _want(P, "P", (E,), torch.float32)
+    _want(aux, "aux", (1,), torch.float32)
+    _want(logit_bias, "logit_bias", (E,), torch.float32, allow_none=True)
+    _want(select_bias, "select_bias", (E,), torch.float32, allow_none=True)
+    _want(logits, "logits", (T, E), torch.float32, allow_none=True)
+    _call("moe_route", ctypes.byref(make_config(cfg)), _p(x), _p(w_g), _p(logit_bias),
+          _p(select_bias), _p(logits), _p(topk_idx), _p(topk_w), _p(f), _p(P), _p(aux),
+          _p(ws), ws.numel(), _stream(stream))
+
+
+def permute(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm, ws,
+            stream=None):
+    T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x, "x", (T, d), dt)
+    _want(topk_idx, "topk_idx", (T, k), torch.int32)
+    _want(counts, "counts", (E,), torch.int32)
+    _want(kept, "kept", (E,), torch.int32)
+    _want(offsets, "offsets", (E + 1,), torch.int32)
+    _want(perm_token, "perm_token", (T * k,), torch.int32)
+    _want(slot_of, "slot_of", (T * k,), torch.int32)
+    _want(x_perm, "x_perm", (T * k, d), dt)
+    _call("moe_permute", ctypes.byref(make_config(cfg)), _p(x), _p(topk_idx), _p(counts),
+          _p(kept), _p(offsets), _p(perm_token), _p(slot_of), _p(x_perm), _p(ws), ws.numel(),
+          _stream(stream))
+
+
+def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=None, ws1=None,
+                wsb1=None, ws2=None, wsb2=None, y_shared=None, stream=None):
+    T, d, F, E, k, S = (cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"], cfg["k"],
+                        cfg.get("n_shared", 0))
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x_perm, "x_perm", (T * k, d), dt)
+    _want(offsets, "offsets", (E + 1,), torch.int32)
+    _want(w1, "w1", (E, F, d), dt)
+    _want(w2, "w2", (E, d, F), dt)
+    _want(b1, "b1", (E, F), dt, allow_none=not cfg.get("has_bias", 0))
+    _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
+    _want(y_perm, "y_perm", (T * k, d), dt)
+    if S:
+        _want(x, "x", (T, d), dt)
+        _want(ws1, "ws1", (S, F, d), dt)
+        _want(ws2, "ws2", (S, d, F), dt)
+        _want(y_shared, "y_shared", (S, T, d), dt)
+    _call("moe_grouped_ffn", ctypes.byref(make_config(cfg)), _p(x_perm), _p(offsets), _p(w1),
+          _p(b1), _p(w2), _p(b2), _p(x), _p(ws1), _p(wsb1), _p(ws2), _p(wsb2), _p(y_perm),
+          _p(y_shared), _p(ws), ws.numel(), _stream(stream))
+
+
+def combine(cfg, y_perm, slot_of, topk_w, out, y_shared=None, stream=None):
+    T, d, k, S = cfg["T"], cfg["d_model"], cfg["k"], cfg.get("n_shared", 0)
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(y_perm, "y_perm", (T * k, d), dt)
+    _want(slot_of, "slot_of", (T * k,), torch.int32)
+    _want(topk_w, "topk_w", (T, k), torch.float32)
+    _want(out, "out", (T, d), dt)
+    if S:
+        _want(y_shared, "y_shared", (S, T, d), dt)
+    _call("moe_combine", ctypes.byref(make_config(cfg)), _p(y_perm), _p(slot_of), _p(topk_w),
+          _p(y_shared), _p(out), _stream(stream))
+
+
+def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None, ws2=None,
+            wsb2=None, logit_bias=None, select_bias=None, topk_idx=None, topk_w=None,
+            counts=None, f=None, P=None, aux=None, stream=None):
+    """The whole layer in one call (route -> permute -> grouped FFN -> combine)."""
+    T, d, F, E, k, S = (cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"], cfg["k"],
+                        cfg.get("n_shared", 0))
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x, "x", (T, d), dt)
+    _want(w_g, "w_g", (d, E), dt)
+    _want(w1, "w1", (E, F, d), dt)
+    _want(w2, "w2", (E, d, F), dt)
+    _want(out, "out", (T, d), dt)
+    _want(topk_idx, "topk_idx", (T, k), torch.int32, allow_none=True)
+    _want(topk_w, "topk_w", (T, k), torch.float32, allow_none=True)
+    _want(counts, "counts", (E,), torch.int32, allow_none=True)
+    for n, t in (("f", f), ("P", P)):
+        _want(t, n, (E,), torch.float32, allow_none=True)
+    _want(aux, "aux", (1,), torch.float32, allow_none=True)
+    if S:
+        _want(ws1, "ws1", (S, F, d), dt)
+        _want(ws2, "ws2", (S, d, F), dt)
+    _call("moe_forward", ctypes.byref(make_config(cfg)), _p(x), _p(w_g), _p(logit_bias),
+          _p(select_bias), _p(w1), _p(b1), _p(w2), _p(b2), _p(ws1), _p(wsb1), _p(ws2),
+          _p(wsb2), _p(out), _p(topk_idx), _p(topk_w), _p(counts), _p(f), _p(P), _p(aux),
+          _p(ws), ws.numel(), _stream(stream))
+
+
+class MoELayer:
+    """One MoE FFN layer whose weights stay resident on the device.
+
+    ``inputs`` holds the weight tensors named as in ``synth.make_inputs``
+    (x is ignored).  ``__call__(x)`` runs ``moe_forward`` and returns the
+    output plus the routing statistics, all as device tensors.
+    """
+
+    def __init__(self, cfg: dict, inputs: dict, device="cuda"):
+        self.cfg = dict(cfg)
+        self.w = {k: v for k, v in inputs.items() if k != "x"}
+        self.device = torch.device(device)
+        self.ws = new_workspace(self.cfg, self.device)
+        T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
+        dt = TORCH_DTYPES[cfg["dtype"]]
+        self.out = torch.empty((T, d), dtype=dt, device=self.device)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=self.device)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        self.counts = torch.empty((E,), dtype=torch.int32, device=self.device)
+        self.f = torch.empty((E,), dtype=torch.float32, device=self.device)
+        self.P = torch.empty((E,), dtype=torch.float32, device=self.device)
+        self.aux = torch.empty((1,), dtype=torch.float32, device=self.device)
+
+    def __call__(self, x: torch.Tensor, stream=None) -> dict:
+        w = self.w
+        forward(self.cfg, x, w["w_g"], w["w1"], w["w2"], self.out, self.ws, b1=w.get("b1"),
+                b2=w.get("b2"), ws1=w.get("ws1"), wsb1=w.get("wsb1"), ws2=w.get("ws2"),
+                wsb2=w.get("wsb2"), logit_bias=w.get("logit_bias"),
+                select_bias=w.get("select_bias"), topk_idx=self.topk_idx, topk_w=self.topk_w,
+                counts=self.counts, f=self.f, P=self.P, aux=self.aux, stream=stream)
+        return dict(out=self.out, topk_idx=self.topk_idx, topk_w=self.topk_w,
+                    counts=self.counts, f=self.f, P=self.P, aux=self.aux)

@@ -1,0 +1,115 @@
+"""Host-only checks of the C-ABI library: it loads, exports every entry point
+include/moe.h declares, and validates arguments without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mixture_experts_52_b300 import moe, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^(?:moe_status|const char\*)\s+(moe_\w+)\s*\(", text, re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        from sparse_mixture_experts_52_b300 import build
+        build.build()
+    return moe.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    for n in ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute",
+              "moe_grouped_ffn", "moe_combine", "moe_forward", "moe_check_status",
+              "moe_status_string"):
+        assert n in names, n
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), f"{n} declared in moe.h but not exported"
+
+
+def test_config_struct_layout(lib):
+    # 14 four-byte fields, no padding
+    assert ctypes.sizeof(moe.Config) == 56
+    assert moe.Config.capacity_factor.offset == 24
+    assert moe.Config.aux_f.offset == 52
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert moe.status_string(s)
+    assert moe.status_string(0) == "ok"
+
+
+@pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
+def test_workspace_size_of_every_workload(lib, name):
+    cfg = synth.workload(name)
+    n = moe.workspace_size(cfg)
+    T, d, F, k, S = cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["k"], cfg["n_shared"]
+    eb = 2 if cfg["dtype"] == "bf16" else 4
+    # x_perm + H + Y must fit
+    assert n >= (T * k * d + (T * k + S * T) * F + T * k * d) * eb
+    assert n < 4 * (T * k * d + (T * k + S * T) * F + T * k * d) * eb + (1 << 24)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("E", 0, 1), ("E", 257, 1), ("k", 0, 1), ("k", 9, 1), ("T", -1, 1),
+    ("d_model", 0, 1), ("n_shared", 5, 1), ("route", 3, 1), ("dtype", 2, 1),
+    ("aux_f", 2, 1), ("renorm", 2, 1), ("min_capacity", -1, 1),
+    ("d_model", 100, 2), ("d_ff", 36, 2),
+])
+def test_invalid_configs_are_rejected_on_the_host(lib, field, value, status):
+    cfg = synth.workload("mixtral_top2", T=16, d_model=64, d_ff=128, k=2, E=8)
+    cfg[field] = value
+    with pytest.raises(moe.MoEError) as ei:
+        moe.workspace_size(cfg)
+    assert ei.value.status == status
+
+
+def test_fp32_wide_router_unsupported(lib):
+    cfg = synth.workload("tiny_fp32_top2", E=128)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.workspace_size(cfg)
+    assert ei.value.status == 2
+
+
+def test_missing_workspace_is_rejected_before_any_launch(lib):
+    cfg = synth.workload("tiny_fp32_top2")
+    c = moe.make_config(cfg)
+    # no CUDA call happens: the workspace check fails first
+    s = lib.moe_route(ctypes.byref(c), 1, 1, None, None, None, 1, 1, 1, 1, 1, None, 0, None)
+    assert s == 3
+    big = moe.workspace_size(cfg)
+    s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, 1, 1, 1, None, None, None, None,
+                        1, None, None, None, None, None, None, 256, big - 1, None)
+    assert s == 3  # too small
+    s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, 1, 1, 1, None, None, None, None,
+                        1, None, None, None, None, None, None, 257, big, None)
+    assert s == 3  # misaligned
+
+
+def test_null_required_pointers_rejected(lib):
+    cfg = synth.workload("tiny_fp32_top2")
+    c = moe.make_config(cfg)
+    big = moe.workspace_size(cfg)
+    # out == NULL
+    s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, 1, 1, 1, None, None, None, None,
+                        None, None, None, None, None, None, None, 256, big, None)
+    assert s == 1
+    # missing expert biases while has_bias = 1
+    s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, None, 1, None, None, None, None,
+                        None, 1, None, None, None, None, None, None, 256, big, None)
+    assert s == 1
+    s = lib.moe_combine(ctypes.byref(c), None, 1, 1, None, 1, None)
+    assert s == 1

@@ -1,0 +1,242 @@
+"""Device parity: the CUDA path through the C ABI against the CPU oracle, on
+the same seeded inputs.  Small cases cover every routing form, the capacity
+drop, shared experts, biases, ragged tails and several tiles; the full-size
+workloads run in the launch configuration the benchmark times, checked on all
+tokens for routing/dispatch and on all (or sampled) tokens for the output."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import compare, moe_oracle as om
+from sparse_mixture_experts_52_b300 import moe, synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _np(t):
+    if t is None:
+        return None
+    return t.detach().cpu().numpy() if t.dtype not in (torch.bfloat16,) else \
+        t.detach().float().cpu().numpy()
+
+
+def run_forward(cfg, inp):
+    layer = moe.MoELayer(cfg, inp, device=DEV)
+    r = layer(inp["x"])
+    moe.check_status(layer.ws)
+    return {k: _np(v) for k, v in r.items()}
+
+
+def run_steps(cfg, inp):
+    """route -> permute -> grouped_ffn -> combine through the four entry points."""
+    T, d, E, k, S = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"], cfg.get("n_shared", 0)
+    dt = moe.TORCH_DTYPES[cfg["dtype"]]
+    ws = moe.new_workspace(cfg, DEV)
+    z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
+    o = dict(logits=z((T, E), torch.float32), topk_idx=z((T, k), torch.int32),
+             topk_w=z((T, k), torch.float32), f=z((E,), torch.float32),
+             P=z((E,), torch.float32), aux=z((1,), torch.float32), counts=z((E,), torch.int32),
+             kept=z((E,), torch.int32), offsets=z((E + 1,), torch.int32),
+             perm_token=z((T * k,), torch.int32), slot_of=z((T * k,), torch.int32),
+             x_perm=z((T * k, d), dt), y_perm=z((T * k, d), dt), out=z((T, d), dt))
+    o["y_shared"] = z((S, T, d), dt) if S else None
+    moe.route(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["f"], o["P"], o["aux"],
+              ws, logit_bias=inp.get("logit_bias"), select_bias=inp.get("select_bias"),
+              logits=o["logits"])
+    moe.permute(cfg, inp["x"], o["topk_idx"], o["counts"], o["kept"], o["offsets"],
+                o["perm_token"], o["slot_of"], o["x_perm"], ws)
+    moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws,
+                    b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
+                    wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
+                    y_shared=o["y_shared"])
+    moe.combine(cfg, o["y_perm"], o["slot_of"], o["topk_w"], o["out"], y_shared=o["y_shared"])
+    moe.check_status(ws)
+    return {kk: (v if kk in ("x_perm", "y_perm", "out", "y_shared") else _np(v))
+            for kk, v in o.items() if v is not None}
+
+
+def check_steps(cfg, inp, st, rep_ref):
+    """Intermediates of the step-wise path against the oracle."""
+    ref = compare.run_oracle(cfg, inp, rows=[0])
+    if rep_ref.overridden:
+        ov = {t: st["topk_idx"][t].astype(np.int64) for t in rep_ref.overridden}
+        ref = compare.run_oracle(cfg, inp, rows=[0], idx_override=ov)
+    # logits in fp32 on both sides (the oracle rounds its float64 sum once)
+    lg = st["logits"].astype(np.float64)
+    err = np.abs(lg - ref.logits) / (np.abs(ref.logits) + 1e-3)
+    assert err.max() < 1e-4, f"logits differ: {err.max():.3e}"
+    compare.compare_dispatch(ref, st)
+    n = int(ref.disp.offsets[-1])
+    # x_perm rows are exact copies of x[perm_token]
+    xp = st["x_perm"][:n]
+    want = inp["x"][torch.as_tensor(ref.disp.perm_token, device=DEV)]
+    assert torch.equal(xp, want), "x_perm is not x[perm_token]"
+    # y_perm rows are FFN_e of those rows (bf16 / fp32 tolerances)
+    experts = compare.LazyExperts(inp["w1"], inp.get("b1"), inp["w2"], inp.get("b2"))
+    yp = compare.np64(st["y_perm"][:n])
+    x64 = compare.np64(inp["x"])
+    for e in range(cfg["E"]):
+        a, b = int(ref.disp.offsets[e]), int(ref.disp.offsets[e + 1])
+        if a == b:
+            continue
+        yr = om.expert_ffn(x64[ref.disp.perm_token[a:b]], *experts(e))
+        rel = np.linalg.norm(yp[a:b] - yr) / max(np.linalg.norm(yr), 1e-30)
+        tol = compare.TOL_F32_REL_L2 if cfg["dtype"] == "f32" else compare.TOL_BF16_REL_L2
+        assert rel <= tol, f"expert {e}: y_perm rel-L2 {rel:.3e}"
+
+
+SMALL = {
+    "fp32_top2_bias": dict(name="tiny_fp32_top2", T=300, d_model=64, d_ff=96, E=8, k=2,
+                           nonzero_bias=True),
+    "switch_cap_small": dict(name="switch_top1_cap", T=1000, d_model=128, d_ff=384, E=16, k=1),
+    "switch_cap_renorm": dict(name="switch_top1_cap", T=600, d_model=64, d_ff=128, E=8, k=1,
+                              renorm=1, aux_f="topk_count"),
+    "mixtral_small_tc_router": dict(name="mixtral_top2", T=600, d_model=256, d_ff=512),
+    "mixtral_small_warp_router": dict(name="mixtral_top2", T=200, d_model=256, d_ff=512),
+    "softmax_topk_k3_ragged": dict(name="mixtral_top2", route="softmax_topk", T=333,
+                                   d_model=200, d_ff=328, E=12, k=3),
+    "deepseek_small_e256": dict(name="deepseek_v3_top8", T=256, d_model=128, d_ff=64),
+    "deepseek_small_e64_s2": dict(name="deepseek_v3_top8", T=300, d_model=256, d_ff=128,
+                                  E=64, k=6, n_shared=2),
+    "bf16_bias_shared": dict(name="deepseek_v3_top8", T=300, d_model=128, d_ff=256, E=8, k=2,
+                             has_bias=1, nonzero_bias=True),
+    "decode_small": dict(name="decode_zipf_top2", T=64, d_model=512, d_ff=1024),
+    "cap_min_capacity": dict(name="switch_top1_cap", T=512, d_model=64, d_ff=64, E=16, k=2,
+                             capacity_factor=0.25, min_capacity=5, route="softmax_topk",
+                             renorm=1, aux_f="topk_count"),
+}
+
+
+def _case(spec):
+    spec = dict(spec)
+    name = spec.pop("name")
+    nz = spec.pop("nonzero_bias", False)
+    cfg = synth.workload(name, **spec)
+    inp = synth.make_inputs(cfg, device=DEV, nonzero_bias=nz)
+    return cfg, inp
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_small_case_forward_and_steps(case):
+    cfg, inp = _case(SMALL[case])
+    fw = run_forward(cfg, inp)
+    rep = compare.check_layer(cfg, inp, fw)
+    st = run_steps(cfg, inp)
+    check_steps(cfg, inp, st, rep)
+    # the step-wise path and moe_forward run the same kernels in the same order
+    assert np.array_equal(_np(st["out"]), fw["out"]), "steps and forward differ"
+    assert np.array_equal(st["topk_idx"], fw["topk_idx"])
+    print(case, rep.summary())
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32_top2", "switch_top1_cap", "decode_zipf_top2"])
+def test_full_workload_all_tokens(name):
+    cfg = synth.workload(name)
+    inp = synth.make_inputs(cfg, device=DEV)
+    fw = run_forward(cfg, inp)
+    rep = compare.check_layer(cfg, inp, fw)
+    if name == "switch_top1_cap":
+        ref = compare.run_oracle(cfg, inp, rows=[0])
+        assert ref.C == 80
+    print(name, rep.summary())
+
+
+@pytest.mark.parametrize("name,nrows", [("mixtral_top2", 48), ("deepseek_v3_top8", 24)])
+def test_full_workload_sampled_tokens(name, nrows):
+    """Routing, statistics and dispatch on every token; the layer output on a
+    fixed sample of tokens (no capacity limit, so each token's output depends
+    only on its own routing)."""
+    cfg = synth.workload(name)
+    inp = synth.make_inputs(cfg, device=DEV)
+    layer = moe.MoELayer(cfg, inp, device=DEV)
+    r = layer(inp["x"])
+    moe.check_status(layer.ws)
+    fw = {k: _np(v) for k, v in r.items()}
+    T = cfg["T"]
+    rows = sorted(set(np.linspace(0, T - 1, nrows).astype(int).tolist()))
+    rep = compare.check_layer(cfg, inp, fw, rows=rows)
+    print(name, rep.summary())
+    del layer, inp
+    torch.cuda.empty_cache()
+
+
+def test_determinism_bitwise():
+    cfg, inp = _case(SMALL["deepseek_small_e64_s2"])
+    a = run_forward(cfg, inp)
+    b = run_forward(cfg, inp)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_exact_ties_lowest_index_and_capacity_in_token_order():
+    """W_g = 0: every logit is exactly 0 on both sides, so every token ties;
+    the lowest indices win and the capacity keeps the first tokens."""
+    cfg = synth.workload("switch_top1_cap", T=512, d_model=64, d_ff=64, E=8, k=2,
+                         capacity_factor=1.0, renorm=1, aux_f="topk_count")
+    inp = synth.make_inputs(cfg, device=DEV)
+    inp["w_g"].zero_()
+    fw = run_forward(cfg, inp)
+    assert np.all(fw["topk_idx"] == np.array([0, 1]))
+    assert np.all(fw["topk_w"] == 0.5)
+    rep = compare.check_layer(cfg, inp, fw)
+    C = int(np.floor(1.0 * 512 / 8))
+    assert list(fw["counts"][:2]) == [512, 512]
+    st = run_steps(cfg, inp)
+    assert list(st["kept"]) == [C, C] + [0] * 6
+    sl = st["slot_of"].reshape(512, 2)
+    assert np.all(sl[:C] >= 0) and np.all(sl[C:] == -1)
+    assert abs(float(fw["aux"][0]) - 2 * 0.01) < 1e-7     # aux = k * alpha (uniform P)
+    print(rep.summary())
+
+
+@pytest.mark.parametrize("mode", ["empty_experts", "all_to_one", "capacity_zero"])
+def test_skewed_routing_edges(mode):
+    cfg = synth.workload("deepseek_v3_top8", T=400, d_model=128, d_ff=128, E=16, k=2,
+                         n_shared=1, route="softmax_topk", select_bias_std=0.0)
+    if mode == "capacity_zero":
+        cfg["capacity_factor"] = 0.01
+    if mode == "all_to_one":
+        cfg["capacity_factor"] = 2.0
+    inp = synth.make_inputs(cfg, device=DEV)
+    lb = torch.zeros(16, device=DEV)
+    if mode == "empty_experts":
+        lb[3] = -30.0
+        lb[9:] = -30.0
+    elif mode == "all_to_one":
+        lb[5] = 30.0
+    inp["logit_bias"] = lb
+    fw = run_forward(cfg, inp)
+    rep = compare.check_layer(cfg, inp, fw)
+    if mode == "empty_experts":
+        assert fw["counts"][3] == 0 and np.all(fw["counts"][9:] == 0)
+    if mode == "all_to_one":
+        assert fw["counts"][5] == 400
+    print(mode, rep.summary())
+
+
+@pytest.mark.parametrize("T", [0, 1, 7])
+def test_tiny_token_counts(T):
+    cfg = synth.workload("deepseek_v3_top8", T=max(T, 1), d_model=128, d_ff=64, E=32, k=4)
+    inp = synth.make_inputs(cfg, device=DEV)
+    if T == 0:
+        cfg["T"] = 0
+        inp["x"] = inp["x"][:0].contiguous()
+    fw = run_forward(cfg, inp)
+    if T == 0:
+        assert np.all(fw["counts"] == 0) and float(fw["aux"][0]) == 0.0
+        return
+    compare.check_layer(cfg, inp, fw)
+
+
+def test_invalid_argument_enqueues_nothing():
+    cfg = synth.workload("tiny_fp32_top2")
+    inp = synth.make_inputs(cfg, device=DEV)
+    layer = moe.MoELayer(cfg, inp, device=DEV)
+    bad = dict(cfg, k=9)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.forward(bad, inp["x"], inp["w_g"], inp["w1"], inp["w2"], layer.out, layer.ws)
+    assert ei.value.status in (1,)
+    moe.check_status(layer.ws)
