@@ -1,0 +1,474 @@
+"""Benchmark of the MoE-layer forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one pass of the whole layer (route -> permute -> grouped FFN ->
+combine) over one batch of seeded synthetic tokens, through the C ABI.  The
+default workload is the Switch-style top-1 layer with capacity (T=4096,
+768 -> 3072 -> 768, E=64, CF=1.25, bf16).  Prints one JSON line (rank 0).
+
+Timing: W untimed warm-up steps; then K steps bracketed by a barrier and a
+device synchronise.  L2 is flushed (a 256 MB write) before every step, outside
+the per-step CUDA events whose sum gives the device time.  The grouped FFN is
+bracketed by its own events on the same stream (the roofline figure).  The
+end-to-end figure repeats the step through moe_forward with the tokens copied
+in from pinned host memory and the output (and aux) copied back every step.
+
+N > 1 (torchrun): every rank runs an independent replica of the layer on its
+own GPU (the path has no exchange step); value = all ranks' tokens / the
+slowest rank's time.
+
+--impl reference times the CPU oracle (the plain float64 restatement of the
+pages) on the host cores, on a bounded token sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "switch_top1_cap"
+METRIC = "MoE-layer fwd tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+GEMM_SOURCES = ["gemm_tc.cuh", "ptx_sm100.cuh", "groups.cuh"]
+# oracle rows (tokens whose FFN output the CPU baseline computes) per workload
+CPU_SAMPLE_ROWS = {"tiny_fp32_top2": 256, "switch_top1_cap": 4096, "mixtral_top2": 128,
+                   "deepseek_v3_top8": 16, "decode_zipf_top2": 64}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps; 0 = enough for >= 1.5 s of timed device work")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=None)
+    return ap.parse_args()
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_PATH):
+        with open(PEAKS_PATH) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "sparse_mixture_experts_52_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per grouped-FFN call from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"gffn_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_gffn_call:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != gemm_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi every 100 ms in the background; keeps the samples whose
+    arrival falls inside [begin(), end()]."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        import threading
+        self.lines, self.t0, self.t1, self.proc = [], None, None, None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self):
+        self.t1 = time.perf_counter()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.lines:
+            if self.t0 is None or not (self.t0 <= t <= self.t1 + 0.1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def algorithmic_ffn(cfg, kept, elem):
+    """Bytes and FLOPs the grouped FFN must move / do at least, for this batch."""
+    d, F, S, T = cfg["d_model"], cfg["d_ff"], cfg.get("n_shared", 0), cfg["T"]
+    n_a = int(sum(kept))
+    active = int(sum(1 for v in kept if v > 0))
+    weights = (active + S) * 2 * d * F * elem
+    acts = (n_a + S * T) * (d + F + F + d) * elem
+    flops = 2 * 2 * (n_a + S * T) * d * F
+    return weights + acts, flops, n_a, active
+
+
+def kernel_launches_per_step(cfg) -> int:
+    """Kernels moe_forward enqueues (see moe_api.cu): route, dispatch, FFN, combine."""
+    tc_router = cfg["dtype"] == "bf16" and (cfg["E"] > 64 or cfg["T"] >= 256)
+    route = 4 if tc_router else 2          # [transpose + GEMM] + gate/fused + finalize
+    return route + 2 + 2 + 1               # rank + permute, up + down, combine
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from sparse_mixture_experts_52_b300 import moe, synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = synth.workload(args.workload)
+    inp = synth.make_inputs(cfg, device=dev, seed=cfg.get("seed", 0) + rank)
+    T, d, E, k, S = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"], cfg.get("n_shared", 0)
+    dt = moe.TORCH_DTYPES[cfg["dtype"]]
+    elem = 2 if cfg["dtype"] == "bf16" else 4
+    stream = torch.cuda.current_stream(dev)
+
+    ws = moe.new_workspace(cfg, dev)
+    z = lambda shape, t: torch.empty(shape, dtype=t, device=dev)
+    o = dict(topk_idx=z((T, k), torch.int32), topk_w=z((T, k), torch.float32),
+             f=z((E,), torch.float32), P=z((E,), torch.float32), aux=z((1,), torch.float32),
+             counts=z((E,), torch.int32), kept=z((E,), torch.int32),
+             offsets=z((E + 1,), torch.int32), perm_token=z((T * k,), torch.int32),
+             slot_of=z((T * k,), torch.int32), x_perm=z((T * k, d), dt),
+             y_perm=z((T * k, d), torch.float32), out=z((T, d), dt))
+    y_sh = z((S, T, d), torch.float32) if S else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def part_route():
+        moe.route(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["f"], o["P"],
+                  o["aux"], ws, logit_bias=inp.get("logit_bias"),
+                  select_bias=inp.get("select_bias"))
+        moe.permute(cfg, inp["x"], o["topk_idx"], o["counts"], o["kept"], o["offsets"],
+                    o["perm_token"], o["slot_of"], o["x_perm"], ws)
+
+    def part_ffn():
+        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws,
+                        b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
+                        wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
+                        y_shared=y_sh)
+
+    def part_combine():
+        moe.combine(cfg, o["y_perm"], o["slot_of"], o["topk_w"], o["out"], y_shared=y_sh)
+
+    # eager warm-up (kernel attributes, tensor-map encoder), then one CUDA graph
+    # per part so the host never gates the device inside the timed region
+    for fn in (part_route, part_ffn, part_combine):
+        fn()
+    torch.cuda.synchronize(dev)
+    moe.check_status(ws)
+    graphs = []
+    for fn in (part_route, part_ffn, part_combine):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    g_route, g_ffn, g_comb = graphs
+
+    def step(ev=None, evf=None):
+        if ev:
+            ev[0].record(stream)
+        g_route.replay()
+        if evf:
+            evf[0].record(stream)
+        g_ffn.replay()
+        if evf:
+            evf[1].record(stream)
+        g_comb.replay()
+        if ev:
+            ev[1].record(stream)
+
+    wev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    w_ms = []
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step(wev)
+        torch.cuda.synchronize(dev)
+        w_ms.append(wev[0].elapsed_time(wev[1]))
+    moe.check_status(ws)
+    if args.steps <= 0:
+        t_step = max(min(w_ms), 1e-3)
+        args.steps = int(min(20000, max(20, math.ceil(1500.0 / t_step))))
+    args.warmup = max(3, args.warmup)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.5)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    sampler.begin()
+    for i in range(args.steps):
+        flush.zero_()
+        step(ev[i], evf[i])
+    torch.cuda.synchronize(dev)
+    sampler.end()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    moe.check_status(ws)
+    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
+    ffn_ms = sum(a.elapsed_time(b) for a, b in evf) / args.steps
+
+    kept = o["kept"].cpu().tolist()
+    byt, flops, n_a, active = algorithmic_ffn(cfg, kept, elem)
+
+    # ---- end to end through the public API (graphed moe_forward), host buffers
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty((T, d), dtype=dt).pin_memory()
+    aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
+    layer = moe.GraphedMoELayer(cfg, inp, device=dev)
+
+    def e2e_step():
+        r = layer(x_host)
+        out_host.copy_(r["out"], non_blocking=True)
+        aux_host.copy_(r["aux"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    moe.check_status(layer.ws)
+
+    # ---- max over ranks
+    times = torch.tensor([dev_ms, e2e_ms, ffn_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    dev_ms, e2e_ms, ffn_ms = [float(v) for v in times.tolist()]
+
+    res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms, bytes=byt, flops=flops,
+               n_a=n_a, active=active, clocks=clocks, wall_s=t_wall,
+               counts=o["counts"].cpu().tolist(), aux=float(o["aux"].cpu()[0]),
+               h2d=x_host.numel() * x_host.element_size(),
+               d2h=out_host.numel() * out_host.element_size() + 4)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu"] = cpu_baseline(cfg, inp, args)
+    return res
+
+
+def cpu_baseline(cfg, inp, args, reps: int = 1):
+    """The oracle as it stands, on the host cores, on a bounded token sample."""
+    import numpy as np
+    import torch
+    from oracle import compare
+
+    rows_n = args.cpu_rows or CPU_SAMPLE_ROWS.get(cfg["name"], 256)
+    rows_n = min(rows_n, cfg["T"])
+    rows = np.arange(rows_n)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=None)
+    except Exception:
+        threads = None
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        compare.run_oracle(cfg, host, rows=rows)
+        times.append(time.perf_counter() - t0)
+    t = min(times)
+    return {"value": rows_n / t, "unit": "tokens/s", "cores": threads or os.cpu_count(),
+            "kind": "oracle", "seconds": t,
+            "sample": (f"float64 numpy oracle: routing, statistics and dispatch of all "
+                       f"{cfg['T']} tokens, expert FFNs of the first {rows_n} tokens; "
+                       f"value = {rows_n} tokens / wall time")}
+
+
+def emit_ours(args, res, world):
+    cfg = res["cfg"]
+    peaks, peak_src = load_peaks()
+    T = cfg["T"]
+    ms = res["dev_ms"] / args.steps
+    tokens_s = world * T * args.steps / (res["dev_ms"] / 1e3)
+    ffn_s = res["ffn_ms"] / 1e3
+    gbs = res["bytes"] / ffn_s / 1e9
+    tfl = res["flops"] / ffn_s / 1e12
+    t_hbm = res["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    long_region = res["dev_ms"] > 1000.0
+    tc_peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    t_tc = res["flops"] / (tc_peak * 1e12)
+    traffic = profiled_traffic(cfg["name"])
+    if cfg["dtype"] == "bf16" and t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": round(tfl, 2), "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": round(tfl / tc_peak, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    roof["traffic"] = traffic
+    roof["kernel"] = "grouped FFN (tcgen05 up-proj+GELU and down-proj launches)"
+    roof["peak_source"] = f"{peak_src} ({'sustained' if long_region and roof['unit'] == 'TFLOP/s' else 'burst'})"
+    roof["algorithmic_bytes"] = res["bytes"]
+    roof["algorithmic_flops"] = res["flops"]
+    roof["ms_per_launch"] = round(res["ffn_ms"], 4)
+    e2e_val = world * T * args.steps / (res["e2e_ms"] / 1e3)
+    counts = res["counts"]
+    line = {
+        "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg["dtype"], "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))",
+        "config": {"workload": cfg["name"], "T": T, "d_model": cfg["d_model"],
+                   "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"],
+                   "n_shared": cfg.get("n_shared", 0), "capacity_factor": cfg["capacity_factor"],
+                   "route": cfg["route"], "parallelism": f"replicas x{world}",
+                   "l2": "flushed (256 MB write) before every step, outside the step events"},
+        "roofline": roof,
+        "grouped_ffn": {"tflops": round(tfl, 2), "gbs": round(gbs, 1),
+                        "tensor_frac": round(tfl / tc_peak, 4),
+                        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "rows": res["n_a"], "active_experts": res["active"]},
+        "routing_stats": {"aux": res["aux"], "max_count": max(counts),
+                          "min_count": min(counts),
+                          "imbalance_ratio": round(max(counts) / (sum(counts) / len(counts)), 3)},
+        "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"],
+                "api": "GraphedMoELayer (moe_forward captured in a CUDA graph), pinned host x in, out+aux back"},
+        "gpu_launches": kernel_launches_per_step(cfg) * args.steps,
+        "clocks": res["clocks"],
+        "wall_s_timed": round(res["wall_s"], 3),
+    }
+    if "cpu" in res:
+        line["cpu_baseline"] = res["cpu"]
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    """The oracle timed as it stands on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import torch
+    from sparse_mixture_experts_52_b300 import synth
+
+    cfg = synth.workload(args.workload)
+    inp = synth.make_inputs(cfg, device="cpu")
+    cpu = None
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(cfg, inp, args)
+        if i >= args.warmup:
+            samples.append(r["seconds"])
+            cpu = r
+    t = sum(samples)
+    rows = cpu["value"] * cpu["seconds"]
+    value = rows * args.steps / t
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))",
+            "config": {"workload": cfg["name"], "T": cfg["T"], "d_model": cfg["d_model"],
+                       "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"]},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
+                             "cores": cpu["cores"], "kind": "oracle", "sample": cpu["sample"]},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        res = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            emit_ours(args, res, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

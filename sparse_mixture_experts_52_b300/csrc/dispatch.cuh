@@ -8,7 +8,8 @@
 //             k assignments (or -1 past the capacity), perm_token, and the row
 //             gather x -> x_perm (x read once, written k times, 16-byte vectors).
 //  k_combine  out[t] = sum_j w[t,j] * y[slot_of[t,j]] + sum_s y_shared[s,t],
-//             a gather in fixed order (no atomics), fp32 accumulation.
+//             a gather in fixed order (no atomics); y is fp32, the sum is fp32
+//             and out is rounded once to its dtype.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -158,8 +159,8 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
 
 template <typename TE, int KMAX>
 __global__ void __launch_bounds__(256)
-k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
-          const float* __restrict__ w, const TE* __restrict__ y_shared, int n_shared, int T,
+k_combine(const float* __restrict__ y, const int32_t* __restrict__ slot_of,
+          const float* __restrict__ w, const float* __restrict__ y_shared, int n_shared, int T,
           int k, int d, TE* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = gridDim.x * (blockDim.x >> 5);

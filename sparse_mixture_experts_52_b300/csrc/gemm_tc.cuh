@@ -9,6 +9,7 @@
 //   warp 0     : TMA producer (one lane) - A and B tiles into a STAGES-deep ring
 //   warp 1     : TMEM owner and MMA issuer (one lane) - 128 x BN x 16 MMAs
 //   warps 2..5 : epilogue - tcgen05.ld, bias / GELU, convert, store
+//                (GELU output in bf16: the next GEMM's A operand; others in fp32)
 // The accumulator is double-buffered in TMEM (2 x BN fp32 columns) so the
 // epilogue of one tile overlaps the main loop of the next.
 //
@@ -23,7 +24,7 @@
 
 namespace moe {
 
-enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_BF16 = 2 };
+enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_F32 = 2 };
 enum : int { DEV_ERR_WAIT_PRODUCER = 1, DEV_ERR_WAIT_MMA = 2, DEV_ERR_WAIT_EPILOGUE = 4 };
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: any single wait
@@ -259,7 +260,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-        if (EPI == EPI_F32) {
+        if (EPI != EPI_F32 && bias) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (col + i < args.N) v[i] += __bfloat162float(bias[col + i]);
+        }
+        if (EPI == EPI_F32 || EPI == EPI_BIAS_F32) {
           float* o = static_cast<float*>(routed ? args.out : args.out1) + orow * args.ldo + col;
           if (col + 16 <= args.N) {
 #pragma unroll
@@ -269,15 +275,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
             for (int i = 0; i < 16 && col + i < args.N; ++i) o[i] = v[i];
           }
         } else {
-          if (bias) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (col + i < args.N) v[i] += __bfloat162float(bias[col + i]);
-          }
-          if (EPI == EPI_GELU_BF16) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
-          }
+          for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
           __nv_bfloat16* o =
               static_cast<__nv_bfloat16*>(routed ? args.out : args.out1) + orow * args.ldo + col;
           if (col + 16 <= args.N) {

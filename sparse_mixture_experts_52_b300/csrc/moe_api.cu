@@ -109,8 +109,8 @@ Layout make_layout(const moe_config& c) {
   L.aux = take(4);
   L.x_perm = take(T * k * d * eb);
   L.H = take((T * k + S * T) * F * eb);
-  L.Y = take(T * k * d * eb);
-  L.Ys = take(S * T * d * eb);
+  L.Y = take(T * k * d * 4);
+  L.Ys = take(S * T * d * 4);
   L.total = off;
   return L;
 }
@@ -234,17 +234,17 @@ moe_status launch_tc(int epi, const CUtensorMap& a0, const CUtensorMap& a1,
       case 128: return launch_tc_inst<128, 6, EPI_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
       case 256: return launch_tc_inst<256, 4, EPI_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
     }
+  } else if (epi == EPI_BIAS_F32) {
+    switch (BN) {
+      case 64: return launch_tc_inst<64, 8, EPI_BIAS_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 128: return launch_tc_inst<128, 6, EPI_BIAS_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 256: return launch_tc_inst<256, 4, EPI_BIAS_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
+    }
   } else if (epi == EPI_GELU_BF16) {
     switch (BN) {
       case 64: return launch_tc_inst<64, 8, EPI_GELU_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
       case 128: return launch_tc_inst<128, 6, EPI_GELU_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
       case 256: return launch_tc_inst<256, 4, EPI_GELU_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-    }
-  } else if (epi == EPI_BIAS_BF16) {
-    switch (BN) {
-      case 64: return launch_tc_inst<64, 8, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 128: return launch_tc_inst<128, 6, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 256: return launch_tc_inst<256, 4, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
     }
   }
   return MOE_ERR_UNSUPPORTED;
@@ -412,7 +412,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     dn.bias0 = static_cast<const __nv_bfloat16*>(b2);
     dn.bias1 = static_cast<const __nv_bfloat16*>(wsb2);
     dn.err = at<int>(ws, L.status);
-    return launch_tc(EPI_BIAS_BF16, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
+    return launch_tc(EPI_BIAS_F32, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
   }
   // fp32: CUDA-core grouped GEMMs
   const int64_t tiles_ub = (Tk + S * T + 63) / 64 + c.E + S;
@@ -459,8 +459,8 @@ moe_status do_combine(const moe_config& c, const void* y_perm, const int32_t* sl
   const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
   const int S = y_shared ? c.n_shared : 0;
 #define MOE_COMBINE(TE, KM)                                                                  \
-  k_combine<TE, KM><<<grid, 256, 0, st>>>(static_cast<const TE*>(y_perm), slot_of, w,      \
-                                          static_cast<const TE*>(y_shared), S, c.T, c.k,    \
+  k_combine<TE, KM><<<grid, 256, 0, st>>>(static_cast<const float*>(y_perm), slot_of, w,   \
+                                          static_cast<const float*>(y_shared), S, c.T, c.k, \
                                           c.d_model, static_cast<TE*>(out))
   const int km = kmax_of(c.k);
   if (c.dtype == MOE_BF16) {

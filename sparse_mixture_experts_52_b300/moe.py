@@ -197,12 +197,12 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
     _want(w2, "w2", (E, d, F), dt)
     _want(b1, "b1", (E, F), dt, allow_none=not cfg.get("has_bias", 0))
     _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
-    _want(y_perm, "y_perm", (T * k, d), dt)
+    _want(y_perm, "y_perm", (T * k, d), torch.float32)
     if S:
         _want(x, "x", (T, d), dt)
         _want(ws1, "ws1", (S, F, d), dt)
         _want(ws2, "ws2", (S, d, F), dt)
-        _want(y_shared, "y_shared", (S, T, d), dt)
+        _want(y_shared, "y_shared", (S, T, d), torch.float32)
     _call("moe_grouped_ffn", ctypes.byref(make_config(cfg)), _p(x_perm), _p(offsets), _p(w1),
           _p(b1), _p(w2), _p(b2), _p(x), _p(ws1), _p(wsb1), _p(ws2), _p(wsb2), _p(y_perm),
           _p(y_shared), _p(ws), ws.numel(), _stream(stream))
@@ -211,12 +211,12 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
 def combine(cfg, y_perm, slot_of, topk_w, out, y_shared=None, stream=None):
     T, d, k, S = cfg["T"], cfg["d_model"], cfg["k"], cfg.get("n_shared", 0)
     dt = TORCH_DTYPES[cfg["dtype"]]
-    _want(y_perm, "y_perm", (T * k, d), dt)
+    _want(y_perm, "y_perm", (T * k, d), torch.float32)
     _want(slot_of, "slot_of", (T * k,), torch.int32)
     _want(topk_w, "topk_w", (T, k), torch.float32)
     _want(out, "out", (T, d), dt)
     if S:
-        _want(y_shared, "y_shared", (S, T, d), dt)
+        _want(y_shared, "y_shared", (S, T, d), torch.float32)
     _call("moe_combine", ctypes.byref(make_config(cfg)), _p(y_perm), _p(slot_of), _p(topk_w),
           _p(y_shared), _p(out), _stream(stream))
 
@@ -278,5 +278,38 @@ class MoELayer:
                 wsb2=w.get("wsb2"), logit_bias=w.get("logit_bias"),
                 select_bias=w.get("select_bias"), topk_idx=self.topk_idx, topk_w=self.topk_w,
                 counts=self.counts, f=self.f, P=self.P, aux=self.aux, stream=stream)
+        return dict(out=self.out, topk_idx=self.topk_idx, topk_w=self.topk_w,
+                    counts=self.counts, f=self.f, P=self.P, aux=self.aux)
+
+
+class GraphedMoELayer(MoELayer):
+    """MoELayer whose forward is captured once in a CUDA graph.
+
+    ``__call__(x)`` copies x into the graph's static input buffer (stream
+    ordered, so a pinned host tensor is copied asynchronously) and replays the
+    captured moe_forward: one graph launch per layer call instead of one
+    ctypes call plus ~9 kernel launches.  The weights and outputs are the
+    same device tensors as the eager layer's.
+    """
+
+    def __init__(self, cfg: dict, inputs: dict, device="cuda"):
+        super().__init__(cfg, inputs, device)
+        T, d = cfg["T"], cfg["d_model"]
+        self.x_static = torch.zeros((T, d), dtype=TORCH_DTYPES[cfg["dtype"]], device=self.device)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):          # warm-up: kernel attributes, tensor-map encoder
+            MoELayer.__call__(self, self.x_static)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        torch.cuda.synchronize(self.device)
+        check_status(self.ws)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            MoELayer.__call__(self, self.x_static)
+
+    def __call__(self, x: Optional[torch.Tensor] = None, stream=None) -> dict:
+        if x is not None:
+            self.x_static.copy_(x, non_blocking=True)
+        self.graph.replay()
         return dict(out=self.out, topk_idx=self.topk_idx, topk_w=self.topk_w,
                     counts=self.counts, f=self.f, P=self.P, aux=self.aux)

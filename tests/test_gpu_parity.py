@@ -41,8 +41,8 @@ def run_steps(cfg, inp):
              P=z((E,), torch.float32), aux=z((1,), torch.float32), counts=z((E,), torch.int32),
              kept=z((E,), torch.int32), offsets=z((E + 1,), torch.int32),
              perm_token=z((T * k,), torch.int32), slot_of=z((T * k,), torch.int32),
-             x_perm=z((T * k, d), dt), y_perm=z((T * k, d), dt), out=z((T, d), dt))
-    o["y_shared"] = z((S, T, d), dt) if S else None
+             x_perm=z((T * k, d), dt), y_perm=z((T * k, d), torch.float32), out=z((T, d), dt))
+    o["y_shared"] = z((S, T, d), torch.float32) if S else None
     moe.route(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["f"], o["P"], o["aux"],
               ws, logit_bias=inp.get("logit_bias"), select_bias=inp.get("select_bias"),
               logits=o["logits"])
