@@ -280,6 +280,9 @@ def run_ours(args, rank, world, local_rank):
     moe.check_status(ws)
     dev_ms = sum(a.elapsed_time(b) for a, b in ev)
     ffn_ms = sum(a.elapsed_time(b) for a, b in evf) / args.steps
+    # ev and evf share boundaries: route+permute = ev0..evf0, combine = evf1..ev1
+    rp_ms = sum(a[0].elapsed_time(b[0]) for a, b in zip(ev, evf)) / args.steps
+    cb_ms = sum(b[1].elapsed_time(a[1]) for a, b in zip(ev, evf)) / args.steps
 
     kept = o["kept"].cpu().tolist()
     byt, flops, n_a, active = algorithmic_ffn(cfg, kept, elem)
@@ -316,7 +319,8 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     dev_ms, e2e_ms, ffn_ms = [float(v) for v in times.tolist()]
 
-    res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms, bytes=byt, flops=flops,
+    res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms, rp_ms=rp_ms, cb_ms=cb_ms,
+               bytes=byt, flops=flops,
                n_a=n_a, active=active, clocks=clocks, wall_s=t_wall,
                counts=o["counts"].cpu().tolist(), aux=float(o["aux"].cpu()[0]),
                h2d=x_host.numel() * x_host.element_size(),
@@ -405,6 +409,8 @@ def emit_ours(args, res, world):
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"],
                 "api": "GraphedMoELayer (moe_forward captured in a CUDA graph), pinned host x in, out+aux back"},
+        "parts_ms": {"route+permute": round(res["rp_ms"], 4),
+                     "grouped_ffn": round(res["ffn_ms"], 4), "combine": round(res["cb_ms"], 4)},
         "gpu_launches": kernel_launches_per_step(cfg) * args.steps,
         "clocks": res["clocks"],
         "wall_s_timed": round(res["wall_s"], 3),

@@ -36,9 +36,9 @@ struct RouteArgs {
   float* logits_out;          // [T, E] or null
   int32_t* idx;               // [T, k]
   float* w;                   // [T, k]
-  float* p_part;              // [nb, E]
-  int32_t* c_part;            // [nb, E] top-k counts
-  int32_t* a_part;            // [nb, E] arg-max counts
+  float* p_part;              // [E, nb] (expert-major: one row per expert)
+  int32_t* c_part;            // [E, nb] top-k counts
+  int32_t* a_part;            // [E, nb] arg-max counts
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -226,9 +226,9 @@ __device__ __forceinline__ void flush_stats(const LaneStats<NPL>& st, int E, flo
       cs += s_c[w][e];
       as += s_a[w][e];
     }
-    p_part[static_cast<int64_t>(blockIdx.x) * E + e] = ps;
-    c_part[static_cast<int64_t>(blockIdx.x) * E + e] = cs;
-    a_part[static_cast<int64_t>(blockIdx.x) * E + e] = as;
+    p_part[static_cast<int64_t>(e) * gridDim.x + blockIdx.x] = ps;
+    c_part[static_cast<int64_t>(e) * gridDim.x + blockIdx.x] = cs;
+    a_part[static_cast<int64_t>(e) * gridDim.x + blockIdx.x] = as;
   }
 }
 
@@ -320,24 +320,36 @@ k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__
   flush_stats<NPL>(st, E, a.p_part, a.c_part, a.a_part);
 }
 
-// f_i, P_i and aux from the per-block partials (one block, fixed order).
+// f_i, P_i and aux from the per-block partials (one block, fixed order): warp w
+// reduces experts w, w+8, ...; lane l sums blocks l, l+32, ... in float64,
+// then a butterfly finishes the row, so the result is bitwise reproducible.
 __global__ void __launch_bounds__(256)
 k_route_finalize(int nb, int T, int E, int aux_f, float alpha, const float* p_part,
                  const int32_t* c_part, const int32_t* a_part, float* f, float* P, float* aux) {
   __shared__ double s_fp[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += blockDim.x >> 5) {
+    const int64_t row = static_cast<int64_t>(e) * nb;
     double ps = 0.0;
     int cs = 0, as = 0;
-    for (int b = 0; b < nb; ++b) {
-      ps += static_cast<double>(p_part[static_cast<int64_t>(b) * E + e]);
-      cs += c_part[static_cast<int64_t>(b) * E + e];
-      as += a_part[static_cast<int64_t>(b) * E + e];
+    for (int b = lane; b < nb; b += 32) {
+      ps += static_cast<double>(p_part[row + b]);
+      cs += c_part[row + b];
+      as += a_part[row + b];
     }
-    const float Pe = static_cast<float>(ps / static_cast<double>(T));
-    const float fe = static_cast<float>(aux_f == AUXF_ARGMAX ? as : cs) / static_cast<float>(T);
-    if (P) P[e] = Pe;
-    if (f) f[e] = fe;
-    s_fp[e] = static_cast<double>(fe) * static_cast<double>(Pe);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      cs += __shfl_xor_sync(0xffffffffu, cs, o);
+      as += __shfl_xor_sync(0xffffffffu, as, o);
+    }
+    if (lane == 0) {
+      const float Pe = static_cast<float>(ps / static_cast<double>(T));
+      const float fe = static_cast<float>(aux_f == AUXF_ARGMAX ? as : cs) / static_cast<float>(T);
+      if (P) P[e] = Pe;
+      if (f) f[e] = fe;
+      s_fp[e] = static_cast<double>(fe) * static_cast<double>(Pe);
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0 && aux) {
