@@ -13,7 +13,10 @@ constexpr int kMaxGroups = kMaxExperts + kMaxShared;
 // Groups 0..E-1 are the routed experts: rows [offsets[g], offsets[g+1]) of A
 // and of the output (or one dense group of `dense_rows` rows when offsets is
 // null).  Groups E..E+n_shared-1 are the shared experts: `shared_rows` rows
-// each, starting at shared_a_row0 / shared_out_row0 and stacked.
+// each.  Shared group s reads A rows from shared_a_row0 + s * shared_a_stride
+// (stride 0 when every shared expert reads the same tokens, shared_rows when
+// each has its own stacked hidden rows) and writes output rows from
+// shared_out_row0 + s * shared_rows.
 struct GroupSpec {
   const int32_t* offsets;
   int E;
@@ -23,6 +26,7 @@ struct GroupSpec {
   int shared_a_sel;     // A operand of shared groups: 0 = map/pointer 0, 1 = map/pointer 1
   int shared_a_row0;
   int shared_out_row0;
+  int shared_a_stride;
 };
 
 struct GroupTable {
@@ -56,7 +60,7 @@ __device__ __forceinline__ void build_group_table(const GroupSpec& gs, int n_til
     } else {
       const int s = g - gs.E;
       rows = gs.shared_rows;
-      arow = gs.shared_a_row0 + s * gs.shared_rows;
+      arow = gs.shared_a_row0 + s * gs.shared_a_stride;
       orow = gs.shared_out_row0 + s * gs.shared_rows;
     }
     rows = rows < 0 ? 0 : rows;

@@ -23,6 +23,9 @@ namespace {
 // ---------------------------------------------------------------- config
 constexpr int kTcRouterMinT = 256;     // bf16 routers with T below this use the FFMA kernel
 constexpr size_t kAlign = 256;
+// workspace header (64 bytes, zeroed by moe_workspace_init): the device status
+// word at byte 0 and the finalize kernel's self-resetting block counter here
+constexpr size_t kCounterOffset = 16;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -71,7 +74,7 @@ bool use_tc_router(const moe_config& c) {
 
 struct Layout {
   size_t status, logits, wgT, p_part, c_part, a_part, rank;
-  size_t idx, w, counts, kept, offsets, perm_token, slot_of, f, P, aux;
+  size_t idx, w, counts, kept, offsets, perm_token, slot_of, fin, f, P, aux;
   size_t x_perm, H, Y, Ys, total;
   int nb, E_pad;
   bool tc_router;
@@ -104,6 +107,7 @@ Layout make_layout(const moe_config& c) {
   L.offsets = take((E + 1) * 4);
   L.perm_token = take(T * k * 4);
   L.slot_of = take(T * k * 4);
+  L.fin = take(E * 8);
   L.f = take(E * 4);
   L.P = take(E * 4);
   L.aux = take(4);
@@ -215,6 +219,34 @@ moe_status launch_tc_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   return launch_ok();
 }
 
+int pick_bn_small(int N) { return N >= 64 ? 64 : 64; }
+
+// Row tiles (128 rows) of a grouped GEMM over n_rows expert-ordered rows in
+// E groups, estimated on the host: the per-expert counts stay on the device.
+int64_t est_row_tiles(int64_t n_rows, int E) {
+  const int64_t dense = (n_rows + 127) / 128 + E / 2;    // plus ragged group tails
+  return std::max<int64_t>(dense, std::min<int64_t>(E, n_rows));
+}
+
+// Tile width for a weight-streaming grouped GEMM: the persistent grid runs
+// ceil(tiles / SMs) rounds, each as long as one tile, whose cost grows with
+// BN (the B slab) plus a fixed share for A and the epilogue.  Picks the BN
+// with the smallest estimated makespan, preferring the wider tile on ties.
+int pick_bn_waves(int N, int64_t row_tiles, int sms) {
+  int best = 256;
+  int64_t best_cost = INT64_MAX;
+  for (int bn : {256, 128}) {
+    const int64_t tiles = row_tiles * ((N + bn - 1) / bn);
+    const int64_t rounds = (tiles + sms - 1) / sms;
+    const int64_t cost = rounds * (bn + 64);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return N < 128 ? pick_bn_small(N) : best;
+}
+
 int pick_bn(int N, bool allow_small) {
   if (N >= 256) return 256;
   if (N >= 128) return 128;
@@ -291,7 +323,7 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
     if (!map_a(&ma, x, c.d_model, c.T) || !map_b(&mb, wgT, c.d_model, L.E_pad, 1, L.E_pad))
       return MOE_ERR_CUDA;
     TcArgs ta{};
-    ta.gs = GroupSpec{nullptr, 1, c.T, 0, 0, 0, 0, 0};
+    ta.gs = GroupSpec{nullptr, 1, c.T, 0, 0, 0, 0, 0, 0};
     ta.N = L.E_pad;
     ta.K = c.d_model;
     ta.out = logits_ws;
@@ -322,8 +354,10 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
     else k_route_warp<float, 64><<<nb, kRouteWarps * 32, 0, st>>>(ra, xf, wf);
   }
   if ((s = launch_ok()) != MOE_OK) return s;
-  k_route_finalize<<<1, 256, 0, st>>>(nb, c.T, c.E, c.aux_f, c.aux_alpha, ra.p_part, ra.c_part,
-                                       ra.a_part, o.f, o.P, o.aux);
+  k_route_finalize<<<c.E, 256, 0, st>>>(nb, c.T, c.E, c.aux_f, c.aux_alpha, ra.p_part,
+                                         ra.c_part, ra.a_part, o.f, o.P, o.aux,
+                                         at<double>(ws, L.fin),
+                                         at<unsigned int>(ws, L.status + kCounterOffset));
   return launch_ok();
 }
 
@@ -372,7 +406,8 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     CUtensorMap ma0, ma1, mb0, mb1;
     // up-projection + GELU:  H = GELU(x_perm W1^T + b1)
     if (!map_a(&ma0, in.x_perm, d, std::max<int64_t>(Tk, 1))) return MOE_ERR_CUDA;
-    const int bn_up = pick_bn(F, false);
+    const int64_t rt = est_row_tiles(Tk, c.E) + S * ((T + 127) / 128);
+    const int bn_up = pick_bn_waves(F, rt, num_sms());
     if (!map_b(&mb0, in.w1, d, F, c.E, bn_up)) return MOE_ERR_CUDA;
     if (S > 0) {
       if (!map_a(&ma1, in.x, d, T) || !map_b(&mb1, in.ws1, d, F, S, bn_up)) return MOE_ERR_CUDA;
@@ -381,7 +416,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
       mb1 = mb0;
     }
     TcArgs up{};
-    up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0};
+    up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0, 0};
     up.N = F;
     up.K = d;
     up.out = H;
@@ -395,7 +430,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     // down-projection:  y = H W2^T + b2
     CUtensorMap ha, hb0, hb1;
     if (!map_a(&ha, H, F, Tk + S * T)) return MOE_ERR_CUDA;
-    const int bn_dn = pick_bn(d, false);
+    const int bn_dn = pick_bn_waves(d, rt, num_sms());
     if (!map_b(&hb0, in.w2, F, d, c.E, bn_dn)) return MOE_ERR_CUDA;
     if (S > 0) {
       if (!map_b(&hb1, in.ws2, F, d, S, bn_dn)) return MOE_ERR_CUDA;
@@ -403,7 +438,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
       hb1 = hb0;
     }
     TcArgs dn{};
-    dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0};
+    dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0, c.T};
     dn.N = d;
     dn.K = F;
     dn.out = y_perm;
@@ -417,7 +452,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   // fp32: CUDA-core grouped GEMMs
   const int64_t tiles_ub = (Tk + S * T + 63) / 64 + c.E + S;
   SimtArgs up{};
-  up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0};
+  up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0, 0};
   up.N = F;
   up.K = d;
   up.A0 = static_cast<const float*>(in.x_perm);
@@ -435,7 +470,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   k_gemm_simt_f32<<<std::max(grid, 1), 256, 0, st>>>(up);
   if ((s = launch_ok()) != MOE_OK) return s;
   SimtArgs dn{};
-  dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0};
+  dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0, c.T};
   dn.N = d;
   dn.K = F;
   dn.A0 = static_cast<const float*>(H);

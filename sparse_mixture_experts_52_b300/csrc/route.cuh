@@ -320,42 +320,65 @@ k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__
   flush_stats<NPL>(st, E, a.p_part, a.c_part, a.a_part);
 }
 
-// f_i, P_i and aux from the per-block partials (one block, fixed order): warp w
-// reduces experts w, w+8, ...; lane l sums blocks l, l+32, ... in float64,
-// then a butterfly finishes the row, so the result is bitwise reproducible.
+// f_i, P_i and aux from the per-block partials.  Block e reduces expert e's
+// row (thread t sums partial rows t, t+256, ... in float64; warps then combine
+// in a fixed tree), writes f[e] and P[e], and the last block to finish (a
+// counter in the workspace header, reset by that block) sums f_e * P_e in
+// expert order for aux.  Every sum has a fixed order: bitwise reproducible.
 __global__ void __launch_bounds__(256)
 k_route_finalize(int nb, int T, int E, int aux_f, float alpha, const float* p_part,
-                 const int32_t* c_part, const int32_t* a_part, float* f, float* P, float* aux) {
-  __shared__ double s_fp[kMaxExperts];
+                 const int32_t* c_part, const int32_t* a_part, float* f, float* P, float* aux,
+                 double* fp_scratch, unsigned int* done_counter) {
+  __shared__ double s_p[8];
+  __shared__ int s_c[8], s_a[8];
+  __shared__ int s_last;
+  const int e = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += blockDim.x >> 5) {
-    const int64_t row = static_cast<int64_t>(e) * nb;
-    double ps = 0.0;
-    int cs = 0, as = 0;
-    for (int b = lane; b < nb; b += 32) {
-      ps += static_cast<double>(p_part[row + b]);
-      cs += c_part[row + b];
-      as += a_part[row + b];
-    }
+  const int64_t row = static_cast<int64_t>(e) * nb;
+  double ps = 0.0;
+  int cs = 0, as = 0;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    ps += static_cast<double>(p_part[row + b]);
+    cs += c_part[row + b];
+    as += a_part[row + b];
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      ps += __shfl_xor_sync(0xffffffffu, ps, o);
-      cs += __shfl_xor_sync(0xffffffffu, cs, o);
-      as += __shfl_xor_sync(0xffffffffu, as, o);
-    }
-    if (lane == 0) {
-      const float Pe = static_cast<float>(ps / static_cast<double>(T));
-      const float fe = static_cast<float>(aux_f == AUXF_ARGMAX ? as : cs) / static_cast<float>(T);
-      if (P) P[e] = Pe;
-      if (f) f[e] = fe;
-      s_fp[e] = static_cast<double>(fe) * static_cast<double>(Pe);
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    cs += __shfl_xor_sync(0xffffffffu, cs, o);
+    as += __shfl_xor_sync(0xffffffffu, as, o);
+  }
+  if (lane == 0) {
+    s_p[warp] = ps;
+    s_c[warp] = cs;
+    s_a[warp] = as;
   }
   __syncthreads();
-  if (threadIdx.x == 0 && aux) {
-    double s = 0.0;
-    for (int e = 0; e < E; ++e) s += s_fp[e];
-    *aux = static_cast<float>(static_cast<double>(alpha) * E * s);
+  if (threadIdx.x == 0) {
+    ps = 0.0;
+    cs = 0;
+    as = 0;
+    for (int w = 0; w < (blockDim.x >> 5); ++w) {
+      ps += s_p[w];
+      cs += s_c[w];
+      as += s_a[w];
+    }
+    const float Pe = static_cast<float>(ps / static_cast<double>(T));
+    const float fe = static_cast<float>(aux_f == AUXF_ARGMAX ? as : cs) / static_cast<float>(T);
+    P[e] = Pe;
+    f[e] = fe;
+    fp_scratch[e] = static_cast<double>(fe) * static_cast<double>(Pe);
+    __threadfence();
+    s_last = (atomicAdd(done_counter, 1u) == static_cast<unsigned int>(E - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_last && threadIdx.x == 0) {
+    __threadfence();
+    const volatile double* fp = fp_scratch;
+    double sum = 0.0;
+    for (int i = 0; i < E; ++i) sum += fp[i];
+    *aux = static_cast<float>(static_cast<double>(alpha) * E * sum);
+    *done_counter = 0u;   // ready for the next call on this workspace
   }
 }
 
