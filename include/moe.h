@@ -125,6 +125,32 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        int32_t* perm_token, int32_t* slot_of, void* x_perm,
                        void* ws, size_t ws_bytes, moe_stream stream);
 
+/* moe_permute without a workspace: the same dispatch (same kernels, same
+ * outputs, bit for bit), with its one scratch array -- the stable rank of
+ * each assignment inside its expert, T*k int32 -- held in a fixed array that
+ * the library declares at file scope in device memory.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory themselves, e.g. a plugin living inside a host program that
+ * owns every device allocation through its own pool, or code on a latency
+ * path where a cudaMalloc (which may synchronise the device) is forbidden.
+ *   Limit: T*k <= MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS (1,048,576 entries,
+ *   4 MiB).  Larger sizes return MOE_ERR_UNSUPPORTED with nothing enqueued.
+ *   Memory: every GPU that loads the library holds the 4 MiB array until the
+ *   process exits.  Nothing in it needs to start at zero: each call writes
+ *   every entry it later reads.
+ *   Set-up: the first call on a device (with that device current) looks up
+ *   the array's device address once; make that first call before any stream
+ *   capture.  No call allocates (no cudaMalloc, no cudaFree).
+ *   Concurrency: all calls on one device share the one array, so calls whose
+ *   kernels may overlap on the GPU (different streams without ordering) race
+ *   and give wrong results; serialise them on one stream.
+ *   Arguments, outputs and errors are those of moe_permute, without ws. */
+#define MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS 1048576
+moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                               int32_t* counts, int32_t* kept, int32_t* offsets,
+                               int32_t* perm_token, int32_t* slot_of, void* x_perm,
+                               moe_stream stream);
+
 /* Expert MLPs as a grouped GEMM over the expert-contiguous rows.
  *   x_perm [T*k, d], offsets [E+1] (device; read on the device only).
  *   w1 [E,F,d], b1 [E,F] or NULL, w2 [E,d,F], b2 [E,d] or NULL.

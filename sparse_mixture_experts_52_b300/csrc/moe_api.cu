@@ -384,6 +384,54 @@ moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void
   return launch_ok();
 }
 
+// ---------------------------------------------------------------- fixed scratch
+// Rank array of moe_permute_noalloc: a file-scope device array, so that entry
+// point needs no caller workspace and allocates nothing.  Host code must not
+// pass `g_noalloc_rank` itself to a kernel (in host code the name is only a
+// host-side stand-in): the device address comes from cudaGetSymbolAddress,
+// looked up once per device with that device current.
+constexpr int64_t kNoallocRankEntries = MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS;
+static __device__ __align__(256) int32_t g_noalloc_rank[kNoallocRankEntries];
+
+// Device address of g_noalloc_rank on the current device, or null when the
+// lookup fails.  The first call on each device does the lookup.
+int32_t* noalloc_rank_address() {
+  constexpr int kMaxDevices = 64;
+  static int32_t* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || !p) return nullptr;
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  return addr[dev];
+}
+
+// The dispatch of do_permute with the rank scratch passed in directly.
+moe_status permute_with_rank(const moe_config& c, int32_t* rank, const void* x,
+                             const int32_t* idx, int32_t* counts, int32_t* kept,
+                             int32_t* offsets, int32_t* perm_token, int32_t* slot_of,
+                             void* x_perm, cudaStream_t st) {
+  const int Tk = c.T * c.k;
+  k_rank<<<c.E, 1024, 0, st>>>(idx, Tk, capacity_of(c), rank, counts, kept);
+  moe_status s;
+  if ((s = launch_ok()) != MOE_OK) return s;
+  const int row_bytes = c.d_model * static_cast<int>(elem_bytes(c));
+  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
+  const auto* xb = static_cast<const uint8_t*>(x);
+  auto* xp = static_cast<uint8_t*>(x_perm);
+  switch (kmax_of(c.k)) {
+    case 2: k_permute<2><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
+    case 4: k_permute<4><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
+    case 8: k_permute<8><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
+    default: k_permute<16><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
+  }
+  return launch_ok();
+}
+
 struct FfnIn {
   const void *x_perm, *w1, *b1, *w2, *b2, *x, *ws1, *wsb1, *ws2, *wsb2;
   const int32_t* offsets;
@@ -578,6 +626,24 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   if (!x || !topk_idx || !perm_token || !slot_of || !x_perm) return MOE_ERR_INVALID_ARG;
   return do_permute(c, L, ws, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm,
                     st);
+}
+
+moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                               int32_t* counts, int32_t* kept, int32_t* offsets,
+                               int32_t* perm_token, int32_t* slot_of, void* x_perm,
+                               moe_stream stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (static_cast<int64_t>(c.T) * c.k > kNoallocRankEntries) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !kept || !offsets) return MOE_ERR_INVALID_ARG;
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) return zero_stats(c, counts, nullptr, nullptr, nullptr, offsets, kept, st);
+  if (!x || !topk_idx || !perm_token || !slot_of || !x_perm) return MOE_ERR_INVALID_ARG;
+  int32_t* rank = noalloc_rank_address();
+  if (!rank) return MOE_ERR_CUDA;
+  return permute_with_rank(c, rank, x, topk_idx, counts, kept, offsets, perm_token, slot_of,
+                           x_perm, st);
 }
 
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,

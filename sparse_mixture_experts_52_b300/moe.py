@@ -70,6 +70,7 @@ _SIGNATURES = {
     "moe_workspace_init": [_P, ctypes.c_size_t, _P],
     "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_permute": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                         ctypes.c_size_t, _P],
     "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P],
@@ -183,6 +184,35 @@ def permute(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm
     _want(x_perm, "x_perm", (T * k, d), dt)
     _call("moe_permute", ctypes.byref(make_config(cfg)), _p(x), _p(topk_idx), _p(counts),
           _p(kept), _p(offsets), _p(perm_token), _p(slot_of), _p(x_perm), _p(ws), ws.numel(),
+          _stream(stream))
+
+
+# T*k limit of moe_permute_noalloc (MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS in moe.h)
+PERMUTE_NOALLOC_MAX_ASSIGNMENTS = 1 << 20
+
+
+def permute_noalloc(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm,
+                    stream=None):
+    """moe_permute_noalloc: the dispatch of ``permute`` without a workspace.
+
+    For callers that cannot allocate device memory themselves: its scratch is a
+    fixed 4 MiB array inside the library.  The first call on a device must come
+    before any stream capture; calls that may overlap on the GPU race, because
+    they share that array.  Raises MoEError (MOE_ERR_UNSUPPORTED) when
+    T*k > PERMUTE_NOALLOC_MAX_ASSIGNMENTS.
+    """
+    T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x, "x", (T, d), dt)
+    _want(topk_idx, "topk_idx", (T, k), torch.int32)
+    _want(counts, "counts", (E,), torch.int32)
+    _want(kept, "kept", (E,), torch.int32)
+    _want(offsets, "offsets", (E + 1,), torch.int32)
+    _want(perm_token, "perm_token", (T * k,), torch.int32)
+    _want(slot_of, "slot_of", (T * k,), torch.int32)
+    _want(x_perm, "x_perm", (T * k, d), dt)
+    _call("moe_permute_noalloc", ctypes.byref(make_config(cfg)), _p(x), _p(topk_idx),
+          _p(counts), _p(kept), _p(offsets), _p(perm_token), _p(slot_of), _p(x_perm),
           _stream(stream))
 
 
