@@ -3,15 +3,17 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-cpu-baseline]
 
-A step is one pass of the whole layer (route -> permute -> grouped FFN ->
-combine) over one batch of seeded synthetic tokens, through the C ABI.  The
+A step is one pass of the whole layer (moe_forward: route -> permute ->
+grouped FFN -> combine) over one batch of seeded synthetic tokens, through
+the C ABI, replayed from one CUDA graph.  The
 default workload is the Switch-style top-1 layer with capacity (T=4096,
 768 -> 3072 -> 768, E=64, CF=1.25, bf16).  Prints one JSON line (rank 0).
 
 Timing: W untimed warm-up steps; then K steps bracketed by a barrier and a
 device synchronise.  L2 is flushed (a 256 MB write) before every step, outside
-the per-step CUDA events whose sum gives the device time.  The grouped FFN is
-bracketed by its own events on the same stream (the roofline figure).  The
+the per-step CUDA events whose sum gives the device time.  The grouped FFN
+(the dominant kernel pair, the roofline figure) and the combine are then timed
+the same way from graphs of their own entry points on the same stream.  The
 end-to-end figure repeats the step through moe_forward with the tokens copied
 in from pinned host memory and the output (and aux) copied back every step.
 
@@ -171,10 +173,29 @@ def algorithmic_ffn(cfg, kept, elem):
 
 
 def kernel_launches_per_step(cfg) -> int:
-    """Kernels moe_forward enqueues (see moe_api.cu): route, dispatch, FFN, combine."""
-    tc_router = cfg["dtype"] == "bf16" and (cfg["E"] > 64 or cfg["T"] >= 256)
-    route = 4 if tc_router else 2          # [transpose + GEMM] + gate/fused + finalize
-    return route + 2 + 2 + 1               # rank + permute, up + down, combine
+    """Kernels one moe_forward enqueues (see moe_api.cu): routing grid (plus the
+    W_g transpose and tensor-core router GEMM ahead of it for bf16 layers with
+    E > 64 or T > 512), permute, up-projection, down-projection, combine."""
+    tc_router = cfg["dtype"] == "bf16" and (cfg["E"] > 64 or cfg["T"] > 512)
+    route = 3 if tc_router else 1
+    return route + 1 + 2 + 1
+
+
+def _timed_graph_loop(graph, flush, stream, steps, before=None):
+    """Replays `graph` `steps` times, flushing L2 before each replay outside the
+    replay's event pair; returns the per-replay device times in ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        if before is not None:
+            before()
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def run_ours(args, rank, world, local_rank):
@@ -189,78 +210,55 @@ def run_ours(args, rank, world, local_rank):
     dt = moe.TORCH_DTYPES[cfg["dtype"]]
     elem = 2 if cfg["dtype"] == "bf16" else 4
     stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
-    ws = moe.new_workspace(cfg, dev)
+    # ---- the step: moe_forward on device-resident tokens, one CUDA graph
+    layer = moe.MoELayer(cfg, inp, device=dev)
+    layer(inp["x"])                        # eager warm-up: kernel attributes, tensor maps
+    torch.cuda.synchronize(dev)
+    moe.check_status(layer.ws)
+    g_fwd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fwd):
+        layer(inp["x"])
+
+    # ---- the dominant kernel pair (grouped FFN) and the combine on the same
+    # workspace state, each in its own graph, for the roofline and the split
     z = lambda shape, t: torch.empty(shape, dtype=t, device=dev)
-    o = dict(topk_idx=z((T, k), torch.int32), topk_w=z((T, k), torch.float32),
-             f=z((E,), torch.float32), P=z((E,), torch.float32), aux=z((1,), torch.float32),
-             counts=z((E,), torch.int32), kept=z((E,), torch.int32),
+    o = dict(counts=z((E,), torch.int32), kept=z((E,), torch.int32),
              offsets=z((E + 1,), torch.int32), perm_token=z((T * k,), torch.int32),
              slot_of=z((T * k,), torch.int32), x_perm=z((T * k, d), dt),
              y_perm=z((T * k, d), torch.float32), out=z((T, d), dt))
     y_sh = z((S, T, d), torch.float32) if S else None
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    def part_route():
-        moe.route(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["f"], o["P"],
-                  o["aux"], ws, logit_bias=inp.get("logit_bias"),
-                  select_bias=inp.get("select_bias"))
-        moe.permute(cfg, inp["x"], o["topk_idx"], o["counts"], o["kept"], o["offsets"],
-                    o["perm_token"], o["slot_of"], o["x_perm"], ws)
+    ws2 = moe.new_workspace(cfg, dev)
+    moe.permute(cfg, inp["x"], layer.topk_idx, o["counts"], o["kept"], o["offsets"],
+                o["perm_token"], o["slot_of"], o["x_perm"], ws2)
 
     def part_ffn():
-        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws,
+        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws2,
                         b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
                         wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
                         y_shared=y_sh)
 
     def part_combine():
-        moe.combine(cfg, o["y_perm"], o["slot_of"], o["topk_w"], o["out"], y_shared=y_sh)
+        moe.combine(cfg, o["y_perm"], o["slot_of"], layer.topk_w, o["out"], y_shared=y_sh)
 
-    # eager warm-up (kernel attributes, tensor-map encoder), then one CUDA graph
-    # per part so the host never gates the device inside the timed region
-    for fn in (part_route, part_ffn, part_combine):
-        fn()
+    part_ffn()
+    part_combine()
     torch.cuda.synchronize(dev)
-    moe.check_status(ws)
-    graphs = []
-    for fn in (part_route, part_ffn, part_combine):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        graphs.append(g)
-    g_route, g_ffn, g_comb = graphs
+    moe.check_status(ws2)
+    g_ffn, g_comb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ffn):
+        part_ffn()
+    with torch.cuda.graph(g_comb):
+        part_combine()
 
-    def step(ev=None, evf=None):
-        if ev:
-            ev[0].record(stream)
-        g_route.replay()
-        if evf:
-            evf[0].record(stream)
-        g_ffn.replay()
-        if evf:
-            evf[1].record(stream)
-        g_comb.replay()
-        if ev:
-            ev[1].record(stream)
-
-    wev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    w_ms = []
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        step(wev)
-        torch.cuda.synchronize(dev)
-        w_ms.append(wev[0].elapsed_time(wev[1]))
-    moe.check_status(ws)
+    w_ms = _timed_graph_loop(g_fwd, flush, stream, max(3, args.warmup))
+    moe.check_status(layer.ws)
     if args.steps <= 0:
         t_step = max(min(w_ms), 1e-3)
         args.steps = int(min(20000, max(20, math.ceil(1500.0 / t_step))))
     args.warmup = max(3, args.warmup)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     time.sleep(0.5)
     if world > 1:
@@ -268,21 +266,20 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_wall0 = time.perf_counter()
     sampler.begin()
-    for i in range(args.steps):
-        flush.zero_()
-        step(ev[i], evf[i])
-    torch.cuda.synchronize(dev)
+    step_ms = _timed_graph_loop(g_fwd, flush, stream, args.steps)
     sampler.end()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    moe.check_status(ws)
-    dev_ms = sum(a.elapsed_time(b) for a, b in ev)
-    ffn_ms = sum(a.elapsed_time(b) for a, b in evf) / args.steps
-    # ev and evf share boundaries: route+permute = ev0..evf0, combine = evf1..ev1
-    rp_ms = sum(a[0].elapsed_time(b[0]) for a, b in zip(ev, evf)) / args.steps
-    cb_ms = sum(b[1].elapsed_time(a[1]) for a, b in zip(ev, evf)) / args.steps
+    moe.check_status(layer.ws)
+    dev_ms = sum(step_ms)
+
+    n_part = max(20, args.steps // 4)
+    _timed_graph_loop(g_ffn, flush, stream, 3)
+    ffn_ms = statistics.fmean(_timed_graph_loop(g_ffn, flush, stream, n_part))
+    cb_ms = statistics.fmean(_timed_graph_loop(g_comb, flush, stream, n_part))
+    moe.check_status(ws2)
 
     kept = o["kept"].cpu().tolist()
     byt, flops, n_a, active = algorithmic_ffn(cfg, kept, elem)
@@ -291,10 +288,10 @@ def run_ours(args, rank, world, local_rank):
     x_host = inp["x"].cpu().pin_memory()
     out_host = torch.empty((T, d), dtype=dt).pin_memory()
     aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
-    layer = moe.GraphedMoELayer(cfg, inp, device=dev)
+    glayer = moe.GraphedMoELayer(cfg, inp, device=dev)
 
     def e2e_step():
-        r = layer(x_host)
+        r = glayer(x_host)
         out_host.copy_(r["out"], non_blocking=True)
         aux_host.copy_(r["aux"], non_blocking=True)
 
@@ -311,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    moe.check_status(layer.ws)
+    moe.check_status(glayer.ws)
 
     # ---- max over ranks
     times = torch.tensor([dev_ms, e2e_ms, ffn_ms], dtype=torch.float64, device=dev)
@@ -319,10 +316,11 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     dev_ms, e2e_ms, ffn_ms = [float(v) for v in times.tolist()]
 
-    res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms, rp_ms=rp_ms, cb_ms=cb_ms,
+    res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms,
+               rp_ms=dev_ms / args.steps - ffn_ms - cb_ms, cb_ms=cb_ms,
                bytes=byt, flops=flops,
                n_a=n_a, active=active, clocks=clocks, wall_s=t_wall,
-               counts=o["counts"].cpu().tolist(), aux=float(o["aux"].cpu()[0]),
+               counts=layer.counts.cpu().tolist(), aux=float(layer.aux.cpu()[0]),
                h2d=x_host.numel() * x_host.element_size(),
                d2h=out_host.numel() * out_host.element_size() + 4)
     if rank == 0:
@@ -409,7 +407,7 @@ def emit_ours(args, res, world):
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"],
                 "api": "GraphedMoELayer (moe_forward captured in a CUDA graph), pinned host x in, out+aux back"},
-        "parts_ms": {"route+permute": round(res["rp_ms"], 4),
+        "parts_ms": {"route+permute (step - ffn - combine)": round(res["rp_ms"], 4),
                      "grouped_ffn": round(res["ffn_ms"], 4), "combine": round(res["cb_ms"], 4)},
         "gpu_launches": kernel_launches_per_step(cfg) * args.steps,
         "clocks": res["clocks"],

@@ -96,8 +96,12 @@ typedef struct {
 /* Bytes of workspace the entry points below need for `cfg` (host only). */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
-/* Clears the device status word at the head of `ws` (stream-ordered).  Call
- * once after allocating `ws`. */
+/* Clears the 1 MiB header of `ws` (stream-ordered): the device status word
+ * and the counters and accumulators the kernels keep there, which must start
+ * at zero and which every call leaves at zero again.  Call once after
+ * allocating `ws`; ws_bytes must be >= 1 MiB (every moe_workspace_size is).
+ * The header's layout does not depend on the configuration, so one
+ * workspace may serve configurations of different sizes in turn. */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream stream);
 
 /* Router + gating + load-balance statistics.
@@ -126,26 +130,33 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        void* ws, size_t ws_bytes, moe_stream stream);
 
 /* moe_permute without a workspace: the same dispatch (same kernels, same
- * outputs, bit for bit), with its one scratch array -- the stable rank of
- * each assignment inside its expert, T*k int32 -- held in a fixed array that
+ * outputs, bit for bit), with its scratch -- the in-chunk rank of each
+ * assignment and the per-chunk expert counts -- held in a fixed array that
  * the library declares at file scope in device memory.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory themselves, e.g. a plugin living inside a host program that
  * owns every device allocation through its own pool, or code on a latency
  * path where a cudaMalloc (which may synchronise the device) is forbidden.
- *   Limit: T*k <= MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS (1,048,576 entries,
- *   4 MiB).  Larger sizes return MOE_ERR_UNSUPPORTED with nothing enqueued.
- *   Memory: every GPU that loads the library holds the 4 MiB array until the
- *   process exits.  Nothing in it needs to start at zero: each call writes
- *   every entry it later reads.
+ *   Limits: T*k <= MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS and
+ *   32*ceil(ceil(T/32)/32)*E <= MOE_PERMUTE_NOALLOC_MAX_CHUNK_COUNTS (the
+ *   per-chunk counts of each expert, rows padded to 32 chunks).  Larger sizes
+ *   return MOE_ERR_UNSUPPORTED with nothing enqueued.
+ *   Memory: every GPU that loads the library holds the array (8 MiB plus a
+ *   2 KiB header) until the process exits.
  *   Set-up: the first call on a device (with that device current) looks up
- *   the array's device address once; make that first call before any stream
- *   capture.  No call allocates (no cudaMalloc, no cudaFree).
+ *   the array's device address and clears the header (a block counter and
+ *   per-expert totals, which must start at zero) on `stream`; every call
+ *   leaves them at zero again.  Make that first call before any stream
+ *   capture.  No call allocates (no
+ *   cudaMalloc, no cudaFree).
  *   Concurrency: all calls on one device share the one array, so calls whose
  *   kernels may overlap on the GPU (different streams without ordering) race
  *   and give wrong results; serialise them on one stream.
- *   Arguments, outputs and errors are those of moe_permute, without ws. */
+ *   Errors: as moe_permute, without ws.  An expert index outside [0, E) in
+ *   topk_idx drops that assignment (slot -1); unlike the workspace entry
+ *   points, no status word reports it. */
 #define MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS 1048576
+#define MOE_PERMUTE_NOALLOC_MAX_CHUNK_COUNTS 1048576
 moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                                int32_t* counts, int32_t* kept, int32_t* offsets,
                                int32_t* perm_token, int32_t* slot_of, void* x_perm,

@@ -1,15 +1,15 @@
 // Dispatch and combine: the local form of the all-to-all "dispatch -> compute
 // -> combine" of expert parallelism (第7章 §7.5), on one GPU.
 //
-//  k_rank     one block per expert: counts its assignments and gives each a
-//             stable rank in ascending t*k + j (the token order SimpleMoELayer's
-//             torch.where produces), plus kept = min(count, C).
-//  k_permute  exclusive scan of kept -> offsets; per token: slot of each of its
-//             k assignments (or -1 past the capacity), perm_token, and the row
-//             gather x -> x_perm (x read once, written k times, 16-byte vectors).
+//  k_permute  per token: the slot of each of its k assignments (or -1 past the
+//             capacity) from the in-chunk ranks and per-chunk counts the
+//             routing / ranking grid left (ascending t*k + j, the token order
+//             SimpleMoELayer's torch.where produces), perm_token, and the row
+//             gather x -> x_perm.
 //  k_combine  out[t] = sum_j w[t,j] * y[slot_of[t,j]] + sum_s y_shared[s,t],
 //             a gather in fixed order (no atomics); y is fp32, the sum is fp32
-//             and out is rounded once to its dtype.
+//             and out is rounded once to its dtype.  In a whole-layer pass one
+//             extra block reduces the routing statistics meanwhile.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -18,112 +18,108 @@
 
 namespace moe {
 
-__device__ __forceinline__ int block_excl_scan(int v, int& total) {
-  __shared__ int s_w[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = (blockDim.x + 31) >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += u;
-  }
-  if (lane == 31) s_w[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? s_w[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += u;
-    }
-    s_w[lane] = w;  // inclusive prefix of warp totals
-  }
-  __syncthreads();
-  total = s_w[nw - 1];
-  const int before = warp > 0 ? s_w[warp - 1] : 0;
-  __syncthreads();
-  return before + inc - v;
-}
-
-__global__ void __launch_bounds__(1024)
-k_rank(const int32_t* __restrict__ idx, int Tk, int C, int32_t* __restrict__ rank,
-       int32_t* __restrict__ counts, int32_t* __restrict__ kept) {
-  const int e = blockIdx.x;
-  const int nt = blockDim.x;
-  const int seg = (Tk + nt - 1) / nt;
-  const int beg = min(static_cast<int>(threadIdx.x) * seg, Tk);
-  const int end = min(beg + seg, Tk);
-  int c = 0;
-  for (int a = beg; a < end; ++a) c += (__ldg(idx + a) == e) ? 1 : 0;
-  int total;
-  int r = block_excl_scan(c, total);
-  for (int a = beg; a < end; ++a)
-    if (__ldg(idx + a) == e) rank[a] = r++;
-  if (threadIdx.x == 0) {
-    if (counts) counts[e] = total;
-    kept[e] = total < C ? total : C;
-  }
-}
-
-// offsets of the kept rows, computed by every block into shared memory
-__device__ __forceinline__ void scan_kept(const int32_t* kept, int E, int* s_off) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int carry = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      int v = e < E ? kept[e] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (e < E) s_off[e + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) s_off[0] = 0;
-  }
-  __syncthreads();
-}
-
+// Slot of every assignment and the row gather.  Block b takes tokens
+// [b*tpb, (b+1)*tpb) (tpb divides 32, so they lie in one chunk g).  Prologue:
+// the block lists the distinct experts of its assignments and, for each,
+// sums the counts of chunks 0..g-1 (hist row of that expert, 32 chunks = one
+// 128-byte line per (expert, step) pair, spread over all threads, integer
+// sums in shared memory).  Then one warp per token: the rank of assignment
+// (t, j) inside its expert is that prefix plus its in-chunk rank; it is kept
+// iff the rank is below kept[e], and lands in row offsets[e] + rank of
+// x_perm.  x is read once and written k times with 16-byte vectors.
 template <int KMAX>
 __global__ void __launch_bounds__(256)
-k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ rank,
-          const int32_t* __restrict__ kept, int T, int k, int E, int row_bytes,
-          const uint8_t* __restrict__ x, uint8_t* __restrict__ x_perm,
-          int32_t* __restrict__ offsets_out, int32_t* __restrict__ perm_token,
-          int32_t* __restrict__ slot_of) {
-  __shared__ int s_off[kMaxExperts + 1];
-  scan_kept(kept, E, s_off);
-  if (blockIdx.x == 0 && offsets_out)
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets_out[e] = s_off[e];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = gridDim.x * (blockDim.x >> 5);
-  const int nvec = row_bytes / 16;
-  for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += nw) {
-    int slot[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      slot[j] = -1;
-      if (j < k) {
-        const int64_t a = static_cast<int64_t>(t) * k + j;
-        const int e = __ldg(idx + a);
-        const int r = __ldg(rank + a);
-        slot[j] = (r < s_off[e + 1] - s_off[e]) ? s_off[e] + r : -1;
-        if (lane == j) {
-          slot_of[a] = slot[j];
-          if (slot[j] >= 0 && perm_token) perm_token[slot[j]] = t;
-        }
+k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
+          const int32_t* __restrict__ hist, const int32_t* __restrict__ kept,
+          const int32_t* __restrict__ offsets, int T, int k, int E, int ncs, int tpb,
+          int row_bytes, const uint8_t* __restrict__ x, uint8_t* __restrict__ x_perm,
+          int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_of) {
+  __shared__ int s_pre[kMaxExperts];
+  __shared__ int s_list[32 * kMaxK];
+  __shared__ unsigned int s_mark[kMaxExperts / 32];
+  __shared__ int s_n;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * tpb, t1 = min(t0 + tpb, T);
+  const int g = t0 / kChunk;
+  if (tid < kMaxExperts / 32) s_mark[tid] = 0u;
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  for (int a = t0 * k + tid; a < t1 * k; a += blockDim.x) {
+    const int e = __ldg(idx + a);
+    if (e >= 0 && e < E) {
+      const unsigned int bit = 1u << (e & 31);
+      if (!(atomicOr(&s_mark[e >> 5], bit) & bit)) {
+        s_pre[e] = 0;
+        s_list[atomicAdd(&s_n, 1)] = e;
       }
     }
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * row_bytes);
-    for (int c = lane; c < nvec; c += 32) {
-      const uint4 v = __ldg(src + c);
+  }
+  __syncthreads();
+  const int n = s_n;
+  const int steps = (g + 31) / 32;   // 32-chunk steps before chunk g
+  for (int p = tid; p < n * steps; p += blockDim.x) {
+    const int e = s_list[p / steps];
+    const int c0 = (p % steps) * 32;
+    const int4* src = reinterpret_cast<const int4*>(hist + static_cast<int64_t>(e) * ncs + c0);
+    int4 v[8];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (j < k && slot[j] >= 0)
-          reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(slot[j]) * row_bytes)[c] = v;
+    for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + 4 * i;
+      sum += (c < g ? v[i].x : 0) + (c + 1 < g ? v[i].y : 0) + (c + 2 < g ? v[i].z : 0) +
+             (c + 3 < g ? v[i].w : 0);
+    }
+    if (sum) atomicAdd(&s_pre[e], sum);
+  }
+  __syncthreads();
+  const int nvec = row_bytes / 16;
+  for (int t = t0 + warp; t < t1; t += blockDim.x >> 5) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * row_bytes);
+    // the first vectors of the row are in flight while the slots resolve
+    constexpr int PF = 4;
+    uint4 v[PF];
+#pragma unroll
+    for (int i = 0; i < PF; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nvec) v[i] = __ldg(src + c);
+    }
+    // lane j < k resolves slot j; the warp then shares the k slots
+    int my_slot = -1;
+    if (lane < k) {
+      const int64_t a = static_cast<int64_t>(t) * k + lane;
+      const int e = __ldg(idx + a);
+      if (e >= 0 && e < E) {
+        const int r = s_pre[e] + __ldg(crank + a);
+        my_slot = (r < __ldg(kept + e)) ? __ldg(offsets + e) + r : -1;
+      }
+      slot_of[a] = my_slot;
+      if (my_slot >= 0 && perm_token) perm_token[my_slot] = t;
+    }
+    int slot[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
+    for (int c0 = 0; c0 < nvec; c0 += 32 * PF) {
+      if (c0 > 0) {
+#pragma unroll
+        for (int i = 0; i < PF; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < nvec) v[i] = __ldg(src + c);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < PF; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < nvec) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j)
+            if (j < k && slot[j] >= 0)
+              reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(slot[j]) * row_bytes)[c] = v[i];
+        }
+      }
     }
   }
 }
@@ -161,9 +157,16 @@ template <typename TE, int KMAX>
 __global__ void __launch_bounds__(256)
 k_combine(const float* __restrict__ y, const int32_t* __restrict__ slot_of,
           const float* __restrict__ w, const float* __restrict__ y_shared, int n_shared, int T,
-          int k, int d, TE* __restrict__ out) {
+          int k, int d, TE* __restrict__ out, const StatsArgs st) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (st.p_part && blockIdx.x == gridDim.x - 1) {   // the extra block: routing statistics
+    stats_finalize(st, nullptr);
+    return;
+  }
+  const int grid = st.p_part ? gridDim.x - 1 : gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int nw = grid * (blockDim.x >> 5);
   const int nchunk = d / 8;
   for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += nw) {
     int slot[KMAX];
@@ -222,6 +225,8 @@ struct SimtArgs {
 
 __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
   constexpr int BM = 64, BN = 64, BK = 16;
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ GroupTable tb;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];

@@ -11,7 +11,21 @@
 //   warps 2..5 : epilogue - tcgen05.ld, bias / GELU, convert, store
 //                (GELU output in bf16: the next GEMM's A operand; others in fp32)
 // The accumulator is double-buffered in TMEM (2 x BN fp32 columns) so the
-// epilogue of one tile overlaps the main loop of the next.
+// epilogue of one segment overlaps the main loop of the next.
+//
+// Work split.  Round-robin: CTA c takes whole tiles c, c + grid, ... so the
+// CTAs running at the same time work on neighbouring tiles and share their
+// weight slabs through L2.  With stream-K (the expert FFN) that holds for all
+// whole waves but the last; the tiles left after them (one to two waves'
+// worth, where whole tiles would leave SMs idle while the weights still
+// stream) have their (tile, k-block) iterations flattened, and CTA c takes
+// the contiguous range [c*W/P, (c+1)*W/P).  A CTA whose range starts inside a
+// tile (only its first stream-K segment can) writes that segment's fp32
+// partial to its slot and raises one flag per epilogue warp; the CTA that
+// holds the tile's first k-block (the owner) adds the partials of the
+// following CTAs in ascending order before its epilogue, so the result is the
+// same on every run.  The following CTAs compute those pieces first, so the
+// owner's waits are short.
 //
 // Every wait is bounded: a wait that runs out records MOE_DEV_ERR_* in the
 // status word, raises the CTA abort flag, drains what this CTA has in flight
@@ -25,10 +39,16 @@
 namespace moe {
 
 enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_F32 = 2 };
-enum : int { DEV_ERR_WAIT_PRODUCER = 1, DEV_ERR_WAIT_MMA = 2, DEV_ERR_WAIT_EPILOGUE = 4 };
+enum : int {
+  DEV_ERR_WAIT_PRODUCER = 1,
+  DEV_ERR_WAIT_MMA = 2,
+  DEV_ERR_WAIT_EPILOGUE = 4,
+  DEV_ERR_WAIT_PARTIAL = 16
+};
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: any single wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s: draining after a give-up
+constexpr int kMaxGemmCtas = 160;                  // stream-K partial slots (grid <= this)
 
 struct TcArgs {
   GroupSpec gs;
@@ -39,6 +59,9 @@ struct TcArgs {
   const __nv_bfloat16* bias0;  // [E, N] or null
   const __nv_bfloat16* bias1;  // [n_shared, N] or null
   int* err;                    // device status word
+  int streamk;                 // 1: stream-K split of the (tile, k-block) iterations
+  float* partial;              // [kMaxGemmCtas][BN/16][128][16] fp32 (stream-K)
+  int* flags;                  // [kMaxGemmCtas][4] zero between launches (stream-K)
 };
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uint64_t limit) {
@@ -53,6 +76,61 @@ __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uin
 __device__ __forceinline__ float gelu_erf(float v) {
   return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
 }
+
+// The segments (tile, [kb0, kb1)) a CTA processes, in order; every warp role
+// walks the same sequence.
+// Stream-K part of the split: tiles [dp_tiles, total) whose W = rem * KB
+// iterations go to P = min(grid, W) CTAs, so every CTA below P has at least
+// one iteration and the CTAs from P on have none.
+struct SkSplit {
+  int dp_tiles;   // tiles done round-robin before the stream-K part
+  int64_t W;      // stream-K iterations
+  int64_t P;      // CTAs sharing them
+  __device__ void init(int total, int KB, int streamk) {
+    const int G = gridDim.x;
+    const int waves = total / G;
+    // whole waves stay round-robin (concurrent CTAs share weight slabs in L2);
+    // the last one to two waves' worth of tiles is split by iterations
+    dp_tiles = !streamk ? total : (waves >= 2 ? (waves - 1) * G : 0);
+    W = static_cast<int64_t>(total - dp_tiles) * KB;
+    P = W < G ? W : G;
+  }
+  __device__ int64_t start(int64_t cta) const { return W * cta / P; }
+};
+
+struct SegIter {
+  int t;             // next round-robin tile
+  int64_t it, end;   // stream-K iterations of this CTA
+  int dp_tiles, KB;
+  __device__ void init(const SkSplit& sp, int kb) {
+    KB = kb;
+    dp_tiles = sp.dp_tiles;
+    t = blockIdx.x;
+    if (blockIdx.x < sp.P) {
+      it = sp.start(blockIdx.x);
+      end = sp.start(blockIdx.x + 1);
+    } else {
+      it = end = 0;
+    }
+  }
+  __device__ bool next(int& tile, int& kb0, int& kb1) {
+    if (t < dp_tiles) {
+      tile = t;
+      kb0 = 0;
+      kb1 = KB;
+      t += gridDim.x;
+      return true;
+    }
+    if (it >= end) return false;
+    const int64_t lt = it / KB;
+    tile = dp_tiles + static_cast<int>(lt);
+    kb0 = static_cast<int>(it - lt * KB);
+    const int64_t rest = end - it;
+    kb1 = (rest < KB - kb0) ? kb0 + static_cast<int>(rest) : KB;
+    it += kb1 - kb0;
+    return true;
+  }
+};
 
 template <int BN, int STAGES>
 struct TcSmem {
@@ -83,6 +161,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           const TcArgs args) {
   using L = TcSmem<BN, STAGES>;
   constexpr int BM = L::BM, BK = L::BK;
+  constexpr int NCC = BN / 16;   // 16-column chunks of a tile
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert((BN & (BN - 1)) == 0, "TMEM columns must be a power of two");
 
@@ -124,6 +203,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     tmem_alloc(&c.tmem_base, L::TMEM_COLS);
     tmem_relinquish();
   }
+  // everything above overlaps the previous kernel's tail (programmatic launch)
+  griddep_wait();
+  griddep_launch_dependents();
   build_group_table<BM>(gs, n_tiles, c.tb);   // synchronises the block
   tc_fence_before();
   __syncthreads();
@@ -131,6 +213,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   const uint32_t tmem_base = c.tmem_base;
   const int total = c.tb.tile_start[G];
   volatile int* abort_flag = &c.abort_flag;
+  SkSplit split;
+  split.init(total, KB, args.streamk);
+  SegIter seg;
+  seg.init(split, KB);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -141,7 +227,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) armed[s] = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int t, kb0, kb1;
+      while (ok && seg.next(t, kb0, kb1)) {
         int g, m_blk, n_blk;
         decode_tile<BM>(c.tb, G, t, g, m_blk, n_blk);
         const bool routed = g < gs.E;
@@ -150,7 +237,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         const int bz = routed ? (gs.offsets ? g : 0) : g - gs.E;
         const int arow = c.tb.a_row0[g] + m_blk * BM;
         const int ncol = n_blk * BN;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&c.empty[stage], phase ^ 1u, abort_flag, args.err,
                                  DEV_ERR_WAIT_PRODUCER, kWaitLimitNs)) {
             ok = false;
@@ -182,7 +269,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int t, kb0, kb1;
+      while (ok && seg.next(t, kb0, kb1)) {
         if (!mbar_wait_bounded(&c.tempty[acc], acc_phase ^ 1u, abort_flag, args.err,
                                DEV_ERR_WAIT_MMA, kWaitLimitNs)) {
           ok = false;
@@ -190,7 +278,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&c.full[stage], phase, abort_flag, args.err, DEV_ERR_WAIT_MMA,
                                  kWaitLimitNs)) {
             ok = false;
@@ -202,7 +290,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             umma_bf16_f32(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32),
-                          sdesc_kmajor_sw128(b0 + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+                          sdesc_kmajor_sw128(b0 + kk * 32), idesc,
+                          (kb > kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit(&c.empty[stage]);   // frees this smem stage once read
           issued = true;
@@ -226,7 +315,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    int t, kb0, kb1;
+    while (seg.next(t, kb0, kb1)) {
       int g, m_blk, n_blk;
       decode_tile<BM>(c.tb, G, t, g, m_blk, n_blk);
       int ok = 1;
@@ -238,9 +328,66 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(acc * BN);
+      const int row = q * 32 + lane;   // row of the tile this thread holds
+
+      if (kb0 > 0) {
+        // --------------------------------------------- a later piece of a tile:
+        // fp32 partial to this CTA's slot, then this warp's flag
+        float* slot = args.partial + static_cast<int64_t>(blockIdx.x) * NCC * BM * 16;
+#pragma unroll 1
+        for (int cc = 0; cc < NCC; ++cc) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(trow + cc * 16, r);
+          tmem_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(slot + (static_cast<int64_t>(cc) * BM + row) * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&c.tempty[acc]);
+          st_release_gpu(args.flags + blockIdx.x * 4 + q, 1);
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
+
+      // --------------------------------------------- the tile's owner: if other
+      // CTAs hold its later k-blocks (CTAs blockIdx+1 .. last), wait for their
+      // partials (this warp's rows only)
+      int last = blockIdx.x;
+      if (kb1 < KB) {
+        const int64_t tile_end = static_cast<int64_t>(t - split.dp_tiles + 1) * KB;
+        while (last + 1 < split.P && split.start(last + 1) < tile_end) ++last;
+        int good = 1;
+        if (lane == 0) {
+          for (int p = blockIdx.x + 1; p <= last && good; ++p) {
+            const int* fl = args.flags + p * 4 + q;
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(fl) == 0) {
+              if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(args.err, DEV_ERR_WAIT_PARTIAL);
+                *abort_flag = 1;
+                good = 0;
+                break;
+              }
+            }
+            if (good) *const_cast<int*>(fl) = 0;   // consumed: zero for the next launch
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        __syncwarp();
+        if (!good) break;
+      }
 
       const bool routed = g < gs.E;
-      const int row_in_grp = m_blk * BM + q * 32 + lane;
+      const int row_in_grp = m_blk * BM + row;
       const bool valid = row_in_grp < c.tb.rows[g];
       const int64_t orow = static_cast<int64_t>(c.tb.out_row0[g]) + row_in_grp;
       const __nv_bfloat16* bias = nullptr;
@@ -248,10 +395,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         if (routed && args.bias0) bias = args.bias0 + static_cast<int64_t>(gs.offsets ? g : 0) * args.N;
         if (!routed && args.bias1) bias = args.bias1 + static_cast<int64_t>(g - gs.E) * args.N;
       }
-      const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                            static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 16; ++cc) {
+      for (int cc = 0; cc < NCC; ++cc) {
         uint32_t r[16];
         tmem_ld_32x32b_x16(trow + cc * 16, r);
         tmem_wait_ld();
@@ -260,6 +405,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+        for (int p = blockIdx.x + 1; p <= last; ++p) {   // later k-blocks, in order
+          const float4* src = reinterpret_cast<const float4*>(
+              args.partial + (static_cast<int64_t>(p) * NCC * BM + static_cast<int64_t>(cc) * BM + row) * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 u = __ldcg(src + i);
+            v[4 * i] += u.x;
+            v[4 * i + 1] += u.y;
+            v[4 * i + 2] += u.z;
+            v[4 * i + 3] += u.w;
+          }
+        }
         if (EPI != EPI_F32 && bias) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -280,14 +437,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           __nv_bfloat16* o =
               static_cast<__nv_bfloat16*>(routed ? args.out : args.out1) + orow * args.ldo + col;
           if (col + 16 <= args.N) {
-            uint32_t p[8];
+            uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-              p[i] = *reinterpret_cast<uint32_t*>(&h);
+              pk[i] = *reinterpret_cast<uint32_t*>(&h);
             }
-            *reinterpret_cast<uint4*>(o) = make_uint4(p[0], p[1], p[2], p[3]);
-            *reinterpret_cast<uint4*>(o + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+            *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(o + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           } else {
             for (int i = 0; i < 16 && col + i < args.N; ++i) o[i] = __float2bfloat16_rn(v[i]);
           }

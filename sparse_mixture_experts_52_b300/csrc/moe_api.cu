@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "moe.h"
 #include "dispatch.cuh"
@@ -21,11 +22,19 @@ using namespace moe;
 namespace {
 
 // ---------------------------------------------------------------- config
-constexpr int kTcRouterMinT = 256;     // bf16 routers with T below this use the FFMA kernel
 constexpr size_t kAlign = 256;
-// workspace header (64 bytes, zeroed by moe_workspace_init): the device status
-// word at byte 0 and the finalize kernel's self-resetting block counter here
-constexpr size_t kCounterOffset = 16;
+// workspace header (1 MiB at a fixed layout, zeroed by moe_workspace_init;
+// every kernel leaves it zeroed again except the status word): the device
+// status word at byte 0, the self-resetting block counters of the routing
+// grid and of the standalone ranking grid, the per-expert assignment and
+// arg-max totals, and the routing grid's per-block softmax partials
+constexpr size_t kHeaderBytes = 1 << 20;
+constexpr size_t kRouteCounterOffset = 16;
+constexpr size_t kRankCounterOffset = 20;
+constexpr size_t kTotalsOffset = 1024;    // int32 [E <= 256]
+constexpr size_t kArgmaxOffset = 2048;    // uint32 [E <= 256]
+constexpr size_t kFlagsOffset = 4096;     // int32 [kMaxGemmCtas][4] stream-K flags
+constexpr size_t kPartOffset = 65536;     // fp32 [E <= 256, blocks <= 512]
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -68,14 +77,16 @@ int capacity_of(const moe_config& c) {
   return std::max(cap, c.min_capacity);
 }
 
+// bf16 routers over more than 64 experts or more tokens than the small-batch
+// router takes run on the tensor cores
 bool use_tc_router(const moe_config& c) {
-  return c.dtype == MOE_BF16 && (c.E > 64 || c.T >= kTcRouterMinT);
+  return c.dtype == MOE_BF16 && (c.E > 64 || c.T > kSmallRouteMaxT);
 }
 
 struct Layout {
-  size_t status, logits, wgT, p_part, c_part, a_part, rank;
-  size_t idx, w, counts, kept, offsets, perm_token, slot_of, fin, f, P, aux;
-  size_t x_perm, H, Y, Ys, total;
+  size_t status, logits, wgT, crank, hist;
+  size_t idx, w, counts, kept, offsets, perm_token, slot_of, f, P, aux;
+  size_t x_perm, H, Y, Ys, sk_part, total;
   int nb, E_pad;
   bool tc_router;
 };
@@ -93,13 +104,16 @@ Layout make_layout(const moe_config& c) {
     off = align_up(off + std::max<size_t>(bytes, 1), kAlign);
     return at;
   };
-  L.status = take(64);
+  L.status = take(kHeaderBytes);
+  static_assert(kPartOffset + size_t(kMaxExperts) * (kRouteMaxBlocks > kSmallRouteMaxT
+                                                         ? kRouteMaxBlocks
+                                                         : kSmallRouteMaxT) * 4 <=
+                    kHeaderBytes,
+                "per-block partials must fit the header");
   L.logits = take(L.tc_router ? T * L.E_pad * 4 : 0);
   L.wgT = take(L.tc_router ? static_cast<size_t>(L.E_pad) * d * 2 : 0);
-  L.p_part = take(static_cast<size_t>(L.nb) * E * 4);
-  L.c_part = take(static_cast<size_t>(L.nb) * E * 4);
-  L.a_part = take(static_cast<size_t>(L.nb) * E * 4);
-  L.rank = take(T * k * 4);
+  L.crank = take(T * k * 4);
+  L.hist = take(static_cast<size_t>(chunk_stride(c.T)) * E * 4);
   L.idx = take(T * k * 4);
   L.w = take(T * k * 4);
   L.counts = take(E * 4);
@@ -107,7 +121,6 @@ Layout make_layout(const moe_config& c) {
   L.offsets = take((E + 1) * 4);
   L.perm_token = take(T * k * 4);
   L.slot_of = take(T * k * 4);
-  L.fin = take(E * 8);
   L.f = take(E * 4);
   L.P = take(E * 4);
   L.aux = take(4);
@@ -115,6 +128,8 @@ Layout make_layout(const moe_config& c) {
   L.H = take((T * k + S * T) * F * eb);
   L.Y = take(T * k * d * 4);
   L.Ys = take(S * T * d * 4);
+  // stream-K partial tiles of the tensor-core FFN: one 128 x 256 fp32 slot per CTA
+  L.sk_part = take(c.dtype == MOE_BF16 ? static_cast<size_t>(kMaxGemmCtas) * 128 * 256 * 4 : 0);
   L.total = off;
   return L;
 }
@@ -134,6 +149,30 @@ moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, const Layout
 
 inline moe_status launch_ok() {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Launches `kern` with programmatic stream serialisation: it may begin while
+// the previous kernel on the stream drains, and waits (griddep_wait) before
+// it touches memory that kernel reads or writes.  Every kernel launched here
+// starts with that wait.
+template <typename... KArgs, typename... Args>
+moe_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 int num_sms() {
@@ -214,12 +253,13 @@ moe_status launch_tc_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   }
   const int64_t n_tiles = (args.N + BN - 1) / BN;
   const int64_t ub = std::max<int64_t>(1, row_tiles_ub * n_tiles);
-  const int grid = static_cast<int>(std::min<int64_t>(ub, num_sms()));
-  k_gemm_tc<BN, STAGES, EPI><<<grid, 192, smem, st>>>(a0, a1, b0, b1, args);
-  return launch_ok();
+  // stream-K: one CTA per SM (at most one partial slot each) whatever the tile
+  // count; round-robin: no more CTAs than tiles
+  const int grid = args.streamk ? std::min(num_sms(), kMaxGemmCtas)
+                                : static_cast<int>(std::min<int64_t>(ub, num_sms()));
+  return launch_pdl(k_gemm_tc<BN, STAGES, EPI>, dim3(grid), dim3(192), smem, st, a0, a1, b0, b1,
+                    args);
 }
-
-int pick_bn_small(int N) { return N >= 64 ? 64 : 64; }
 
 // Row tiles (128 rows) of a grouped GEMM over n_rows expert-ordered rows in
 // E groups, estimated on the host: the per-expert counts stay on the device.
@@ -228,14 +268,23 @@ int64_t est_row_tiles(int64_t n_rows, int E) {
   return std::max<int64_t>(dense, std::min<int64_t>(E, n_rows));
 }
 
-// Tile width for a weight-streaming grouped GEMM: the persistent grid runs
-// ceil(tiles / SMs) rounds, each as long as one tile, whose cost grows with
-// BN (the B slab) plus a fixed share for A and the epilogue.  Picks the BN
-// with the smallest estimated makespan, preferring the wider tile on ties.
-int pick_bn_waves(int N, int64_t row_tiles, int sms) {
-  int best = 256;
+// Tile width and work split of an expert-FFN GEMM.  With many waves of tiles
+// (compute-bound layers) the split is stream-K over the last waves and the
+// widest tile wins.  With few waves (weight streaming) whole tiles go round
+// robin and the width is the one with the smallest estimated makespan: each
+// round costs one tile, whose cost grows with BN (its weight slab) plus a
+// fixed share for A and the epilogue.
+struct FfnSplit {
+  int bn, streamk;
+};
+FfnSplit pick_ffn_split(int N, int64_t row_tiles, int sms) {
+  const int wide = N >= 256 ? 256 : (N >= 128 ? 128 : 64);
+  const int64_t tiles_wide = row_tiles * ((N + wide - 1) / wide);
+  if (tiles_wide >= 8 * static_cast<int64_t>(sms)) return FfnSplit{wide, 1};
+  int best = wide;
   int64_t best_cost = INT64_MAX;
-  for (int bn : {256, 128}) {
+  for (int bn : {256, 128, 64}) {
+    if (bn > wide) continue;
     const int64_t tiles = row_tiles * ((N + bn - 1) / bn);
     const int64_t rounds = (tiles + sms - 1) / sms;
     const int64_t cost = rounds * (bn + 64);
@@ -244,7 +293,7 @@ int pick_bn_waves(int N, int64_t row_tiles, int sms) {
       best = bn;
     }
   }
-  return N < 128 ? pick_bn_small(N) : best;
+  return FfnSplit{best, 0};
 }
 
 int pick_bn(int N, bool allow_small) {
@@ -290,8 +339,100 @@ struct RouteOut {
   float* f;
   float* P;
   float* aux;
+  int32_t* counts;
+  int32_t* kept;
+  int32_t* offsets;
+  int defer_stats;
 };
 
+int kmax_of(int k) { return k <= 2 ? 2 : (k <= 4 ? 4 : (k <= 8 ? 8 : 16)); }
+
+// Ranking state of a grid: chunk ranks and prefixes in `crank` / `hist`.
+DispatchArgs dispatch_args(const moe_config& c, int32_t* crank, int32_t* hist, int32_t* totals,
+                           int32_t* counts, int32_t* kept, int32_t* offsets, unsigned int* done,
+                           int* err) {
+  DispatchArgs dp{};
+  dp.T = c.T;
+  dp.k = c.k;
+  dp.E = c.E;
+  dp.C = capacity_of(c);
+  dp.cpb = route_cpb(c.T);
+  dp.crank = crank;
+  dp.hist = hist;
+  dp.totals = totals;
+  dp.counts = counts;
+  dp.kept = kept;
+  dp.offsets = offsets;
+  dp.done = done;
+  dp.err = err;
+  return dp;
+}
+
+template <int NPL>
+moe_status launch_gate(int km, int nb, cudaStream_t st, const RouteArgs& ra) {
+  switch (km) {
+    case 2: return launch_pdl(k_gate<NPL, 2>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
+    case 4: return launch_pdl(k_gate<NPL, 4>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
+    case 8: return launch_pdl(k_gate<NPL, 8>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
+    default: return launch_pdl(k_gate<NPL, 16>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
+  }
+}
+
+template <typename TE, int EP>
+moe_status launch_route_warp(int km, int nb, cudaStream_t st, const RouteArgs& ra, const TE* x,
+                             const TE* w_g) {
+  switch (km) {
+    case 2: return launch_pdl(k_route_warp<TE, EP, 2>, dim3(nb), dim3(kRouteThreads), 0, st, ra, x, w_g);
+    case 4: return launch_pdl(k_route_warp<TE, EP, 4>, dim3(nb), dim3(kRouteThreads), 0, st, ra, x, w_g);
+    case 8: return launch_pdl(k_route_warp<TE, EP, 8>, dim3(nb), dim3(kRouteThreads), 0, st, ra, x, w_g);
+    default: return launch_pdl(k_route_warp<TE, EP, 16>, dim3(nb), dim3(kRouteThreads), 0, st, ra, x, w_g);
+  }
+}
+
+template <typename TE>
+moe_status launch_route_warp_e(const moe_config& c, int nb, cudaStream_t st, const RouteArgs& ra,
+                               const void* x, const void* w_g) {
+  const int km = kmax_of(c.k);
+  const auto* xt = static_cast<const TE*>(x);
+  const auto* wt = static_cast<const TE*>(w_g);
+  if (c.E <= 8) return launch_route_warp<TE, 8>(km, nb, st, ra, xt, wt);
+  if (c.E <= 16) return launch_route_warp<TE, 16>(km, nb, st, ra, xt, wt);
+  if (c.E <= 32) return launch_route_warp<TE, 32>(km, nb, st, ra, xt, wt);
+  return launch_route_warp<TE, 64>(km, nb, st, ra, xt, wt);
+}
+
+template <typename TE, int EP>
+moe_status launch_route_small(int km, int T, cudaStream_t st, const RouteArgs& ra, const TE* x,
+                              const TE* w_g) {
+  switch (km) {
+    case 2: return launch_pdl(k_route_small<TE, EP, 2>, dim3(T), dim3(kRouteThreads), 0, st, ra, x, w_g);
+    case 4: return launch_pdl(k_route_small<TE, EP, 4>, dim3(T), dim3(kRouteThreads), 0, st, ra, x, w_g);
+    case 8: return launch_pdl(k_route_small<TE, EP, 8>, dim3(T), dim3(kRouteThreads), 0, st, ra, x, w_g);
+    default: return launch_pdl(k_route_small<TE, EP, 16>, dim3(T), dim3(kRouteThreads), 0, st, ra, x, w_g);
+  }
+}
+
+template <typename TE>
+moe_status launch_route_small_e(const moe_config& c, cudaStream_t st, const RouteArgs& ra,
+                                const void* x, const void* w_g) {
+  const int km = kmax_of(c.k);
+  const auto* xt = static_cast<const TE*>(x);
+  const auto* wt = static_cast<const TE*>(w_g);
+  if (c.E <= 8) return launch_route_small<TE, 8>(km, c.T, st, ra, xt, wt);
+  if (c.E <= 16) return launch_route_small<TE, 16>(km, c.T, st, ra, xt, wt);
+  if (c.E <= 32) return launch_route_small<TE, 32>(km, c.T, st, ra, xt, wt);
+  return launch_route_small<TE, 64>(km, c.T, st, ra, xt, wt);
+}
+
+// Blocks of the routing grid do_route launches (one per token for the
+// small-batch router).
+int route_grid(const moe_config& c, const Layout& L) {
+  if (!L.tc_router && c.T <= kSmallRouteMaxT) return c.T;
+  return L.nb;
+}
+
+// Router, gating, statistics and the dispatch ranking in one routing grid
+// (plus the tensor-core router GEMM ahead of it for wide or long batches).
 moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* x,
                     const void* w_g, const float* lb, const float* sb, const RouteOut& o,
                     cudaStream_t st) {
@@ -307,18 +448,29 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
   ra.logits_out = o.logits;
   ra.idx = o.idx;
   ra.w = o.w;
-  ra.p_part = at<float>(ws, L.p_part);
-  ra.c_part = at<int32_t>(ws, L.c_part);
-  ra.a_part = at<int32_t>(ws, L.a_part);
+  ra.p_part = at<float>(ws, L.status + kPartOffset);
+  ra.a_tot = at<unsigned int>(ws, L.status + kArgmaxOffset);
+  ra.aux_f = c.aux_f;
+  ra.alpha = c.aux_alpha;
+  ra.f = o.f;
+  ra.P = o.P;
+  ra.aux = o.aux;
+  ra.defer_stats = o.defer_stats;
+  ra.dp = dispatch_args(c, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist),
+                        at<int32_t>(ws, L.status + kTotalsOffset), o.counts, o.kept, o.offsets,
+                        at<unsigned int>(ws, L.status + kRouteCounterOffset),
+                        at<int>(ws, L.status));
   const int nb = L.nb;
+  const int km = kmax_of(c.k);
   moe_status s = MOE_OK;
   if (L.tc_router) {
     __nv_bfloat16* wgT = at<__nv_bfloat16>(ws, L.wgT);
     float* logits_ws = at<float>(ws, L.logits);
     dim3 tgrid((c.d_model + 31) / 32, (L.E_pad + 31) / 32);
-    k_transpose_wg<<<tgrid, dim3(32, 8), 0, st>>>(static_cast<const __nv_bfloat16*>(w_g),
-                                                   c.d_model, c.E, L.E_pad, wgT);
-    if ((s = launch_ok()) != MOE_OK) return s;
+    if ((s = launch_pdl(k_transpose_wg, tgrid, dim3(32, 8), 0, st,
+                        static_cast<const __nv_bfloat16*>(w_g), c.d_model, c.E, L.E_pad, wgT)) !=
+        MOE_OK)
+      return s;
     CUtensorMap ma, mb;
     if (!map_a(&ma, x, c.d_model, c.T) || !map_b(&mb, wgT, c.d_model, L.E_pad, 1, L.E_pad))
       return MOE_ERR_CUDA;
@@ -334,68 +486,83 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
     if (s != MOE_OK) return s;
     ra.logits_in = logits_ws;
     ra.ld_in = L.E_pad;
-    if (c.E <= 32) k_gate<1><<<nb, kRouteWarps * 32, 0, st>>>(ra);
-    else if (c.E <= 64) k_gate<2><<<nb, kRouteWarps * 32, 0, st>>>(ra);
-    else if (c.E <= 128) k_gate<4><<<nb, kRouteWarps * 32, 0, st>>>(ra);
-    else k_gate<8><<<nb, kRouteWarps * 32, 0, st>>>(ra);
-  } else if (c.dtype == MOE_BF16) {
-    const auto* xb = static_cast<const __nv_bfloat16*>(x);
-    const auto* wb = static_cast<const __nv_bfloat16*>(w_g);
-    if (c.E <= 8) k_route_warp<__nv_bfloat16, 8><<<nb, kRouteWarps * 32, 0, st>>>(ra, xb, wb);
-    else if (c.E <= 16) k_route_warp<__nv_bfloat16, 16><<<nb, kRouteWarps * 32, 0, st>>>(ra, xb, wb);
-    else if (c.E <= 32) k_route_warp<__nv_bfloat16, 32><<<nb, kRouteWarps * 32, 0, st>>>(ra, xb, wb);
-    else k_route_warp<__nv_bfloat16, 64><<<nb, kRouteWarps * 32, 0, st>>>(ra, xb, wb);
-  } else {
-    const auto* xf = static_cast<const float*>(x);
-    const auto* wf = static_cast<const float*>(w_g);
-    if (c.E <= 8) k_route_warp<float, 8><<<nb, kRouteWarps * 32, 0, st>>>(ra, xf, wf);
-    else if (c.E <= 16) k_route_warp<float, 16><<<nb, kRouteWarps * 32, 0, st>>>(ra, xf, wf);
-    else if (c.E <= 32) k_route_warp<float, 32><<<nb, kRouteWarps * 32, 0, st>>>(ra, xf, wf);
-    else k_route_warp<float, 64><<<nb, kRouteWarps * 32, 0, st>>>(ra, xf, wf);
+    if (c.E <= 32) return launch_gate<1>(km, nb, st, ra);
+    if (c.E <= 64) return launch_gate<2>(km, nb, st, ra);
+    if (c.E <= 128) return launch_gate<4>(km, nb, st, ra);
+    return launch_gate<8>(km, nb, st, ra);
   }
-  if ((s = launch_ok()) != MOE_OK) return s;
-  k_route_finalize<<<c.E, 256, 0, st>>>(nb, c.T, c.E, c.aux_f, c.aux_alpha, ra.p_part,
-                                         ra.c_part, ra.a_part, o.f, o.P, o.aux,
-                                         at<double>(ws, L.fin),
-                                         at<unsigned int>(ws, L.status + kCounterOffset));
-  return launch_ok();
+  if (c.T <= kSmallRouteMaxT) {
+    if (c.dtype == MOE_BF16) return launch_route_small_e<__nv_bfloat16>(c, st, ra, x, w_g);
+    return launch_route_small_e<float>(c, st, ra, x, w_g);
+  }
+  // fp32 batches beyond the small-batch router (bf16 ones take the tensor cores)
+  return launch_route_warp_e<float>(c, nb, st, ra, x, w_g);
 }
 
-int kmax_of(int k) { return k <= 2 ? 2 : (k <= 4 ? 4 : (k <= 8 ? 8 : 16)); }
-
-moe_status do_permute(const moe_config& c, const Layout& L, void* ws, const void* x,
-                      const int32_t* idx, int32_t* counts, int32_t* kept, int32_t* offsets,
-                      int32_t* perm_token, int32_t* slot_of, void* x_perm, cudaStream_t st) {
-  int32_t* rank = at<int32_t>(ws, L.rank);
-  const int Tk = c.T * c.k;
-  k_rank<<<c.E, 1024, 0, st>>>(idx, Tk, capacity_of(c), rank, counts, kept);
-  moe_status s;
-  if ((s = launch_ok()) != MOE_OK) return s;
+// Slot resolution and row gather from the ranks a routing or ranking grid
+// left.  Tokens per block: the largest of 32, 16, 8, 4 that still gives at
+// least two blocks per SM.
+moe_status launch_permute(const moe_config& c, const int32_t* idx, const int32_t* crank,
+                          const int32_t* hist, const int32_t* kept, const int32_t* offsets,
+                          int32_t* perm_token, int32_t* slot_of, const void* x, void* x_perm,
+                          cudaStream_t st) {
   const int row_bytes = c.d_model * static_cast<int>(elem_bytes(c));
-  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
+  int tpb = 32;
+  while (tpb > 4 && (c.T + tpb - 1) / tpb < 2 * num_sms()) tpb >>= 1;
+  const int grid = std::max(1, (c.T + tpb - 1) / tpb);
+  const int ncs = chunk_stride(c.T);
   const auto* xb = static_cast<const uint8_t*>(x);
   auto* xp = static_cast<uint8_t*>(x_perm);
+#define MOE_PERMUTE(KM)                                                                     \
+  launch_pdl(k_permute<KM>, dim3(grid), dim3(256), 0, st, idx, crank, hist, kept, offsets, \
+             c.T, c.k, c.E, ncs, tpb, row_bytes, xb, xp, perm_token, slot_of)
   switch (kmax_of(c.k)) {
-    case 2: k_permute<2><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-    case 4: k_permute<4><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-    case 8: k_permute<8><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-    default: k_permute<16><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
+    case 2: return MOE_PERMUTE(2);
+    case 4: return MOE_PERMUTE(4);
+    case 8: return MOE_PERMUTE(8);
+    default: return MOE_PERMUTE(16);
   }
-  return launch_ok();
+#undef MOE_PERMUTE
+}
+
+// Ranking of caller-supplied indices, then the permute.
+moe_status permute_from_idx(const moe_config& c, const DispatchArgs& dp, const void* x,
+                            const int32_t* idx, int32_t* perm_token, int32_t* slot_of,
+                            void* x_perm, cudaStream_t st) {
+  const int nb = route_blocks(c.T);
+  moe_status s;
+  switch (kmax_of(c.k)) {
+    case 2: s = launch_pdl(k_dispatch_rank<2>, dim3(nb), dim3(kRouteThreads), 0, st, dp, idx); break;
+    case 4: s = launch_pdl(k_dispatch_rank<4>, dim3(nb), dim3(kRouteThreads), 0, st, dp, idx); break;
+    case 8: s = launch_pdl(k_dispatch_rank<8>, dim3(nb), dim3(kRouteThreads), 0, st, dp, idx); break;
+    default: s = launch_pdl(k_dispatch_rank<16>, dim3(nb), dim3(kRouteThreads), 0, st, dp, idx); break;
+  }
+  if (s != MOE_OK) return s;
+  return launch_permute(c, idx, dp.crank, dp.hist, dp.kept, dp.offsets, perm_token, slot_of, x,
+                        x_perm, st);
 }
 
 // ---------------------------------------------------------------- fixed scratch
-// Rank array of moe_permute_noalloc: a file-scope device array, so that entry
+// Scratch of moe_permute_noalloc: a file-scope device array, so that entry
 // point needs no caller workspace and allocates nothing.  Host code must not
-// pass `g_noalloc_rank` itself to a kernel (in host code the name is only a
+// pass `g_noalloc_scratch` itself to a kernel (in host code the name is only a
 // host-side stand-in): the device address comes from cudaGetSymbolAddress,
-// looked up once per device with that device current.
-constexpr int64_t kNoallocRankEntries = MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS;
-static __device__ __align__(256) int32_t g_noalloc_rank[kNoallocRankEntries];
+// looked up once per device with that device current.  Layout in int32
+// words: [0, 512) header (status word at 0, the ranking grid's block counter
+// at 4 and the per-expert totals at [256, 512): all must start at zero), then
+// the in-chunk ranks (T*k entries), then the per-chunk counts (E rows of
+// ceil(T/32) rounded up to 32 entries).
+constexpr int64_t kNoallocAssignments = MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS;
+constexpr int64_t kNoallocChunkCounts = MOE_PERMUTE_NOALLOC_MAX_CHUNK_COUNTS;
+constexpr int64_t kNoallocHeader = 512;
+constexpr int64_t kNoallocTotals = 256;
+static __device__ __align__(256) int32_t
+    g_noalloc_scratch[kNoallocHeader + kNoallocAssignments + kNoallocChunkCounts];
 
-// Device address of g_noalloc_rank on the current device, or null when the
-// lookup fails.  The first call on each device does the lookup.
-int32_t* noalloc_rank_address() {
+// Device address of g_noalloc_scratch on the current device, or null when the
+// set-up fails.  The first call on each device looks the address up and clears
+// the header on `st` (stream ordered before the first use).
+int32_t* noalloc_scratch(cudaStream_t st) {
   constexpr int kMaxDevices = 64;
   static int32_t* addr[kMaxDevices] = {};
   static std::mutex mu;
@@ -404,32 +571,11 @@ int32_t* noalloc_rank_address() {
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_rank) != cudaSuccess || !p) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    if (cudaMemsetAsync(p, 0, kNoallocHeader * sizeof(int32_t), st) != cudaSuccess) return nullptr;
     addr[dev] = static_cast<int32_t*>(p);
   }
   return addr[dev];
-}
-
-// The dispatch of do_permute with the rank scratch passed in directly.
-moe_status permute_with_rank(const moe_config& c, int32_t* rank, const void* x,
-                             const int32_t* idx, int32_t* counts, int32_t* kept,
-                             int32_t* offsets, int32_t* perm_token, int32_t* slot_of,
-                             void* x_perm, cudaStream_t st) {
-  const int Tk = c.T * c.k;
-  k_rank<<<c.E, 1024, 0, st>>>(idx, Tk, capacity_of(c), rank, counts, kept);
-  moe_status s;
-  if ((s = launch_ok()) != MOE_OK) return s;
-  const int row_bytes = c.d_model * static_cast<int>(elem_bytes(c));
-  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
-  const auto* xb = static_cast<const uint8_t*>(x);
-  auto* xp = static_cast<uint8_t*>(x_perm);
-  switch (kmax_of(c.k)) {
-    case 2: k_permute<2><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-    case 4: k_permute<4><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-    case 8: k_permute<8><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-    default: k_permute<16><<<grid, 256, 0, st>>>(idx, rank, kept, c.T, c.k, c.E, row_bytes, xb, xp, offsets, perm_token, slot_of); break;
-  }
-  return launch_ok();
 }
 
 struct FfnIn {
@@ -455,7 +601,8 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     // up-projection + GELU:  H = GELU(x_perm W1^T + b1)
     if (!map_a(&ma0, in.x_perm, d, std::max<int64_t>(Tk, 1))) return MOE_ERR_CUDA;
     const int64_t rt = est_row_tiles(Tk, c.E) + S * ((T + 127) / 128);
-    const int bn_up = pick_bn_waves(F, rt, num_sms());
+    const FfnSplit sp_up = pick_ffn_split(F, rt, num_sms());
+    const int bn_up = sp_up.bn;
     if (!map_b(&mb0, in.w1, d, F, c.E, bn_up)) return MOE_ERR_CUDA;
     if (S > 0) {
       if (!map_a(&ma1, in.x, d, T) || !map_b(&mb1, in.ws1, d, F, S, bn_up)) return MOE_ERR_CUDA;
@@ -463,6 +610,7 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
       ma1 = ma0;
       mb1 = mb0;
     }
+    static_assert(kFlagsOffset + kMaxGemmCtas * 4 * sizeof(int) <= kPartOffset, "header layout");
     TcArgs up{};
     up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0, 0};
     up.N = F;
@@ -473,12 +621,16 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     up.bias0 = static_cast<const __nv_bfloat16*>(b1);
     up.bias1 = static_cast<const __nv_bfloat16*>(wsb1);
     up.err = at<int>(ws, L.status);
+    up.streamk = sp_up.streamk;
+    up.partial = at<float>(ws, L.sk_part);
+    up.flags = at<int>(ws, L.status + kFlagsOffset);
     if ((s = launch_tc(EPI_GELU_BF16, ma0, ma1, mb0, mb1, up, bn_up, row_tiles_ub, st)) != MOE_OK)
       return s;
     // down-projection:  y = H W2^T + b2
     CUtensorMap ha, hb0, hb1;
     if (!map_a(&ha, H, F, Tk + S * T)) return MOE_ERR_CUDA;
-    const int bn_dn = pick_bn_waves(d, rt, num_sms());
+    const FfnSplit sp_dn = pick_ffn_split(d, rt, num_sms());
+    const int bn_dn = sp_dn.bn;
     if (!map_b(&hb0, in.w2, F, d, c.E, bn_dn)) return MOE_ERR_CUDA;
     if (S > 0) {
       if (!map_b(&hb1, in.ws2, F, d, S, bn_dn)) return MOE_ERR_CUDA;
@@ -495,6 +647,9 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     dn.bias0 = static_cast<const __nv_bfloat16*>(b2);
     dn.bias1 = static_cast<const __nv_bfloat16*>(wsb2);
     dn.err = at<int>(ws, L.status);
+    dn.streamk = sp_dn.streamk;
+    dn.partial = at<float>(ws, L.sk_part);
+    dn.flags = at<int>(ws, L.status + kFlagsOffset);
     return launch_tc(EPI_BIAS_F32, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
   }
   // fp32: CUDA-core grouped GEMMs
@@ -515,8 +670,8 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   up.ldo = F;
   up.gelu = 1;
   int grid = static_cast<int>(std::min<int64_t>(tiles_ub * ((F + 63) / 64), num_sms() * 4));
-  k_gemm_simt_f32<<<std::max(grid, 1), 256, 0, st>>>(up);
-  if ((s = launch_ok()) != MOE_OK) return s;
+  if ((s = launch_pdl(k_gemm_simt_f32, dim3(std::max(grid, 1)), dim3(256), 0, st, up)) != MOE_OK)
+    return s;
   SimtArgs dn{};
   dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0, c.T};
   dn.N = d;
@@ -533,32 +688,31 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   dn.ldo = d;
   dn.gelu = 0;
   grid = static_cast<int>(std::min<int64_t>(tiles_ub * ((d + 63) / 64), num_sms() * 4));
-  k_gemm_simt_f32<<<std::max(grid, 1), 256, 0, st>>>(dn);
-  return launch_ok();
+  return launch_pdl(k_gemm_simt_f32, dim3(std::max(grid, 1)), dim3(256), 0, st, dn);
 }
 
 moe_status do_combine(const moe_config& c, const void* y_perm, const int32_t* slot_of,
-                      const float* w, const void* y_shared, void* out, cudaStream_t st) {
-  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
+                      const float* w, const void* y_shared, void* out, cudaStream_t st,
+                      const StatsArgs& stats = StatsArgs{}) {
+  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8)) + (stats.p_part ? 1 : 0);
   const int S = y_shared ? c.n_shared : 0;
-#define MOE_COMBINE(TE, KM)                                                                  \
-  k_combine<TE, KM><<<grid, 256, 0, st>>>(static_cast<const float*>(y_perm), slot_of, w,   \
-                                          static_cast<const float*>(y_shared), S, c.T, c.k, \
-                                          c.d_model, static_cast<TE*>(out))
+#define MOE_COMBINE(TE, KM)                                                                 \
+  return launch_pdl(k_combine<TE, KM>, dim3(grid), dim3(256), 0, st,                        \
+                    static_cast<const float*>(y_perm), slot_of, w,                          \
+                    static_cast<const float*>(y_shared), S, c.T, c.k, c.d_model,             \
+                    static_cast<TE*>(out), stats)
   const int km = kmax_of(c.k);
   if (c.dtype == MOE_BF16) {
     if (km == 2) MOE_COMBINE(__nv_bfloat16, 2);
-    else if (km == 4) MOE_COMBINE(__nv_bfloat16, 4);
-    else if (km == 8) MOE_COMBINE(__nv_bfloat16, 8);
-    else MOE_COMBINE(__nv_bfloat16, 16);
-  } else {
-    if (km == 2) MOE_COMBINE(float, 2);
-    else if (km == 4) MOE_COMBINE(float, 4);
-    else if (km == 8) MOE_COMBINE(float, 8);
-    else MOE_COMBINE(float, 16);
+    if (km == 4) MOE_COMBINE(__nv_bfloat16, 4);
+    if (km == 8) MOE_COMBINE(__nv_bfloat16, 8);
+    MOE_COMBINE(__nv_bfloat16, 16);
   }
+  if (km == 2) MOE_COMBINE(float, 2);
+  if (km == 4) MOE_COMBINE(float, 4);
+  if (km == 8) MOE_COMBINE(float, 8);
+  MOE_COMBINE(float, 16);
 #undef MOE_COMBINE
-  return launch_ok();
 }
 
 moe_status zero_stats(const moe_config& c, int32_t* counts, float* f, float* P, float* aux,
@@ -587,9 +741,9 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
 }
 
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream stream) {
-  if (!ws || ws_bytes < 64 || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)
+  if (!ws || ws_bytes < kHeaderBytes || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)
     return MOE_ERR_WORKSPACE;
-  return cudaMemsetAsync(ws, 0, 64, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return cudaMemsetAsync(ws, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
@@ -608,7 +762,9 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
   if (c.T == 0) return zero_stats(c, nullptr, f, P, aux, nullptr, nullptr, st);
   if (!x || !w_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   return do_route(c, L, ws, x, w_g, logit_bias, select_bias,
-                  RouteOut{logits, topk_idx, topk_w, f, P, aux}, st);
+                  RouteOut{logits, topk_idx, topk_w, f, P, aux, at<int32_t>(ws, L.counts),
+                           at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets), 0},
+                  st);
 }
 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -624,8 +780,12 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   auto st = static_cast<cudaStream_t>(stream);
   if (c.T == 0) return zero_stats(c, counts, nullptr, nullptr, nullptr, offsets, kept, st);
   if (!x || !topk_idx || !perm_token || !slot_of || !x_perm) return MOE_ERR_INVALID_ARG;
-  return do_permute(c, L, ws, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm,
-                    st);
+  const DispatchArgs dp = dispatch_args(c, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist),
+                                        at<int32_t>(ws, L.status + kTotalsOffset), counts, kept,
+                                        offsets,
+                                        at<unsigned int>(ws, L.status + kRankCounterOffset),
+                                        at<int>(ws, L.status));
+  return permute_from_idx(c, dp, x, topk_idx, perm_token, slot_of, x_perm, st);
 }
 
 moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -635,15 +795,20 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
-  if (static_cast<int64_t>(c.T) * c.k > kNoallocRankEntries) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(c.T) * c.k > kNoallocAssignments ||
+      static_cast<int64_t>(chunk_stride(c.T)) * c.E > kNoallocChunkCounts)
+    return MOE_ERR_UNSUPPORTED;
   if (!counts || !kept || !offsets) return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);
   if (c.T == 0) return zero_stats(c, counts, nullptr, nullptr, nullptr, offsets, kept, st);
   if (!x || !topk_idx || !perm_token || !slot_of || !x_perm) return MOE_ERR_INVALID_ARG;
-  int32_t* rank = noalloc_rank_address();
-  if (!rank) return MOE_ERR_CUDA;
-  return permute_with_rank(c, rank, x, topk_idx, counts, kept, offsets, perm_token, slot_of,
-                           x_perm, st);
+  int32_t* scratch = noalloc_scratch(st);
+  if (!scratch) return MOE_ERR_CUDA;
+  const DispatchArgs dp =
+      dispatch_args(c, scratch + kNoallocHeader, scratch + kNoallocHeader + kNoallocAssignments,
+                    scratch + kNoallocTotals, counts, kept, offsets,
+                    reinterpret_cast<unsigned int*>(scratch + 4), scratch);
+  return permute_from_idx(c, dp, x, topk_idx, perm_token, slot_of, x_perm, st);
 }
 
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -702,21 +867,36 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   if (c.n_shared > 0 && (!ws1 || !ws2)) return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && c.has_bias && (!wsb1 || !wsb2)) return MOE_ERR_INVALID_ARG;
 
-  if ((s = do_route(c, L, ws, x, w_g, logit_bias, select_bias,
-                    RouteOut{nullptr, idx, w, fo, Po, ao}, st)) != MOE_OK)
-    return s;
   int32_t* kept = at<int32_t>(ws, L.kept);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* slot_of = at<int32_t>(ws, L.slot_of);
   void* x_perm = at<uint8_t>(ws, L.x_perm);
-  if ((s = do_permute(c, L, ws, x, idx, cnt, kept, offsets, at<int32_t>(ws, L.perm_token),
-                      slot_of, x_perm, st)) != MOE_OK)
+  // the routing grid also ranks the assignments: the permute follows directly
+  if ((s = do_route(c, L, ws, x, w_g, logit_bias, select_bias,
+                    RouteOut{nullptr, idx, w, fo, Po, ao, cnt, kept, offsets, 1}, st)) != MOE_OK)
+    return s;
+  if ((s = launch_permute(c, idx, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist), kept,
+                          offsets, at<int32_t>(ws, L.perm_token), slot_of, x, x_perm, st)) !=
+      MOE_OK)
     return s;
   void* Y = at<uint8_t>(ws, L.Y);
   void* Ys = at<uint8_t>(ws, L.Ys);
   FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
   if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
-  return do_combine(c, Y, slot_of, w, c.n_shared > 0 ? Ys : nullptr, out, st);
+  // the combine kernel's extra block reduces the routing statistics
+  StatsArgs sa{};
+  sa.p_part = at<float>(ws, L.status + kPartOffset);
+  sa.nb = route_grid(c, L);
+  sa.a_tot = at<unsigned int>(ws, L.status + kArgmaxOffset);
+  sa.counts = cnt;
+  sa.T = c.T;
+  sa.E = c.E;
+  sa.aux_f = c.aux_f;
+  sa.alpha = c.aux_alpha;
+  sa.f = fo;
+  sa.P = Po;
+  sa.aux = ao;
+  return do_combine(c, Y, slot_of, w, c.n_shared > 0 ? Ys : nullptr, out, st, sa);
 }
 
 moe_status moe_check_status(void* ws, moe_stream stream) {
@@ -727,7 +907,7 @@ moe_status moe_check_status(void* ws, moe_stream stream) {
   if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (v != 0) {
     if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
-    return MOE_ERR_TIMEOUT;
+    return (v & DEV_ERR_BAD_EXPERT_INDEX) ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
   }
   return MOE_OK;
 }

@@ -1,4 +1,4 @@
-// Router and gating kernels.
+// Router, gating, load-balance statistics and the dispatch bookkeeping.
 //
 // Gating follows the three forms of the pages: softmax over E -> top-k ->
 // renormalise (SparseMoEGate / MoELayer), top-k on the logits -> softmax over
@@ -6,26 +6,64 @@
 // per-expert bias with weights from the unbiased softmax (DeepSeek-V3).  One
 // warp owns one token; lane l holds experts l, l+32, ... in registers, the
 // top-k is k rounds of a warp arg-max with the lower expert index winning equal
-// scores.  Load-balance partial sums (sum of softmax, top-k counts, arg-max
-// counts) are kept per block in a fixed order and reduced by k_route_finalize,
-// so f, P and aux are bitwise reproducible.
+// scores.
+//
+// A routing grid gives each block a contiguous range of 32-token chunks.
+// After gating its tokens, the block ranks every assignment (t, j) inside its
+// chunk among the chunk's assignments to the same expert, in ascending t*k+j
+// (a token's k experts are distinct, so this is the number of earlier tokens
+// of the chunk routed to that expert), stores the chunk's count per expert,
+// and adds those counts to per-expert totals with integer atomics (whose sum
+// does not depend on their order).  The last block to finish (a
+// self-resetting counter in the workspace) turns the totals into counts, kept
+// = min(count, C) and offsets, and sums the per-block softmax partials into
+// P, f and aux in a fixed order.  The permute kernel later adds, for each
+// token, the counts of the earlier chunks to the in-chunk rank: the stable
+// rank of the assignment inside its expert.  Every result is bitwise
+// reproducible.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
 #include "groups.cuh"
+#include "ptx_sm100.cuh"
 
 namespace moe {
 
 enum : int { ROUTE_SOFTMAX_TOPK = 0, ROUTE_TOPK_SOFTMAX = 1, ROUTE_BIASED_SOFTMAX = 2 };
 enum : int { AUXF_TOPK_COUNT = 0, AUXF_ARGMAX = 1 };
+enum : int { DEV_ERR_BAD_EXPERT_INDEX = 8 };   // status bit: an expert index outside [0, E)
 constexpr int kMaxK = 16;
 constexpr int kRouteWarps = 8;          // warps per routing block
+constexpr int kRouteThreads = kRouteWarps * 32;
 constexpr int kRouteMaxBlocks = 296;    // partial-sum rows (fixed: layout must not depend on the GPU)
+constexpr int kChunk = 32;              // tokens per ranking chunk (one warp's lanes)
 
-__host__ __device__ inline int route_blocks(int T) {
-  const int nb = (T + kRouteWarps - 1) / kRouteWarps;
-  return nb < 1 ? 1 : (nb > kRouteMaxBlocks ? kRouteMaxBlocks : nb);
+__host__ __device__ inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+// row stride of the per-chunk counts: a multiple of 32 chunks (128 bytes)
+__host__ __device__ inline int chunk_stride(int T) { return (num_chunks(T) + 31) / 32 * 32; }
+// chunks per routing block, and the number of blocks
+__host__ __device__ inline int route_cpb(int T) {
+  const int nc = num_chunks(T) < 1 ? 1 : num_chunks(T);
+  return (nc + kRouteMaxBlocks - 1) / kRouteMaxBlocks;
 }
+__host__ __device__ inline int route_blocks(int T) {
+  const int nc = num_chunks(T) < 1 ? 1 : num_chunks(T);
+  const int cpb = route_cpb(T);
+  return (nc + cpb - 1) / cpb;
+}
+
+struct DispatchArgs {
+  int T, k, E, C;          // C = INT_MAX when there is no capacity limit
+  int cpb;                 // chunks per block
+  int32_t* crank;          // [T*k] in-chunk rank of each assignment
+  int32_t* hist;           // [E, chunk_stride(T)] per-chunk counts
+  int32_t* totals;         // [E] assignments per expert (zero between calls)
+  int32_t* counts;         // [E]
+  int32_t* kept;           // [E]
+  int32_t* offsets;        // [E+1]
+  unsigned int* done;      // self-resetting block counter (starts at 0)
+  int* err;                // device status word
+};
 
 struct RouteArgs {
   int T, d, E, k, route, renorm;
@@ -36,10 +74,46 @@ struct RouteArgs {
   float* logits_out;          // [T, E] or null
   int32_t* idx;               // [T, k]
   float* w;                   // [T, k]
-  float* p_part;              // [E, nb] (expert-major: one row per expert)
-  int32_t* c_part;            // [E, nb] top-k counts
-  int32_t* a_part;            // [E, nb] arg-max counts
+  float* p_part;              // [E, nb] per-block sums of the softmax (expert-major; zero between calls)
+  unsigned int* a_tot;        // [E] arg-max counts (zero between calls)
+  int aux_f;
+  float alpha;
+  float* f;                   // [E]
+  float* P;                   // [E]
+  float* aux;                 // [1]
+  DispatchArgs dp;
+  int defer_stats;            // 1: the combine kernel reduces the statistics instead
 };
+
+// The statistics reduction: P, f and aux from the routing grid's per-block
+// softmax partials (p_part, nb blocks), arg-max totals and counts.
+struct StatsArgs {
+  float* p_part;              // [E, nb]; cleared after reading
+  int nb;
+  unsigned int* a_tot;        // [E]; cleared after reading
+  const int32_t* counts;      // [E] (read when s_cnt is not given)
+  int T, E, aux_f;
+  float alpha;
+  float* f;
+  float* P;
+  float* aux;
+};
+
+__host__ __device__ inline StatsArgs stats_args(const RouteArgs& a, int nb) {
+  StatsArgs st;
+  st.p_part = a.p_part;
+  st.nb = nb;
+  st.a_tot = a.a_tot;
+  st.counts = a.dp.counts;
+  st.T = a.T;
+  st.E = a.E;
+  st.aux_f = a.aux_f;
+  st.alpha = a.alpha;
+  st.f = a.f;
+  st.P = a.P;
+  st.aux = a.aux;
+  return st;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -68,13 +142,11 @@ __device__ __forceinline__ void warp_argmax(float& v, int& e) {
 template <int NPL>
 struct LaneStats {
   float p[NPL];
-  int cnt[NPL];
   int amax[NPL];
   __device__ void zero() {
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       p[i] = 0.f;
-      cnt[i] = 0;
       amax[i] = 0;
     }
   }
@@ -161,10 +233,7 @@ __device__ __forceinline__ void gate_token(const float (&l)[NPL], const float (&
       float mine = 0.f;
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
-        if (be == lane + 32 * i) {
-          taken |= 1u << i;
-          st.cnt[i] += 1;
-        }
+        if (be == lane + 32 * i) taken |= 1u << i;
         if (i == (be >> 5)) mine = (route == ROUTE_TOPK_SOFTMAX) ? lv[i] : p[i];
       }
       sel_e[j] = be;
@@ -203,32 +272,251 @@ __device__ __forceinline__ void gate_token(const float (&l)[NPL], const float (&
   for (int i = 0; i < NPL; ++i) st.p[i] += p[i];
 }
 
-// Block epilogue of the statistics: warps' partials summed in warp order.
+// Block epilogue of the statistics: warps' softmax partials summed in warp
+// order into column blockIdx.x of the expert-major [E, gridDim.x] partials;
+// arg-max counts added to the per-expert totals.
 template <int NPL>
 __device__ __forceinline__ void flush_stats(const LaneStats<NPL>& st, int E, float* p_part,
-                                            int32_t* c_part, int32_t* a_part) {
+                                            unsigned int* a_tot) {
   __shared__ float s_p[kRouteWarps][32 * NPL];
-  __shared__ int s_c[kRouteWarps][32 * NPL];
   __shared__ int s_a[kRouteWarps][32 * NPL];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     s_p[warp][lane + 32 * i] = st.p[i];
-    s_c[warp][lane + 32 * i] = st.cnt[i];
     s_a[warp][lane + 32 * i] = st.amax[i];
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float ps = 0.f;
-    int cs = 0, as = 0;
+    int as = 0;
     for (int w = 0; w < kRouteWarps; ++w) {
       ps += s_p[w][e];
-      cs += s_c[w][e];
       as += s_a[w][e];
     }
-    p_part[static_cast<int64_t>(e) * gridDim.x + blockIdx.x] = ps;
-    c_part[static_cast<int64_t>(e) * gridDim.x + blockIdx.x] = cs;
-    a_part[static_cast<int64_t>(e) * gridDim.x + blockIdx.x] = as;
+    // a reduction into a slot that is zero and that only this block touches:
+    // the value lands at L2 (0 + ps == ps, so the result is exact)
+    if (ps != 0.f) atomicAdd(p_part + static_cast<int64_t>(e) * gridDim.x + blockIdx.x, ps);
+    if (as) atomicAdd(a_tot + e, static_cast<unsigned int>(as));
+  }
+}
+
+// ---------------------------------------------------------------- ranking
+// Ranks the assignments of chunk `g` (tokens 32g .. 32g+31, lane = token),
+// writes crank and the chunk's entries of hist, and adds its counts to the
+// totals.  `idx` is read from L2
+// (ld.cg): this grid may have just written it.  s_hist is this warp's
+// zeroed [E] counter row; it is zero again on return.
+template <int KMAX>
+__device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t* idx, int g,
+                                           int* s_hist) {
+  const int lane = threadIdx.x & 31;
+  const int t = g * kChunk + lane;
+  const bool valid_t = t < a.T;
+  int e[KMAX], r[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    e[j] = -1;
+    r[j] = 0;
+    if (j < a.k && valid_t) {
+      const int v = __ldcg(idx + static_cast<int64_t>(t) * a.k + j);
+      if (v >= 0 && v < a.E) {
+        e[j] = v;
+      } else {
+        atomicOr(a.err, DEV_ERR_BAD_EXPERT_INDEX);
+      }
+    }
+  }
+  // r[j] = number of tokens before this lane's in the chunk that chose e[j]
+  for (int src = 0; src < kChunk - 1; ++src) {
+#pragma unroll
+    for (int jj = 0; jj < KMAX; ++jj) {
+      if (jj < a.k) {
+        const int o = __shfl_sync(0xffffffffu, e[jj], src);
+        if (src < lane && o >= 0) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) r[j] += (e[j] == o) ? 1 : 0;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < a.k && valid_t) {
+      a.crank[static_cast<int64_t>(t) * a.k + j] = r[j];
+      if (e[j] >= 0) atomicAdd(s_hist + e[j], 1);
+    }
+  }
+  __syncwarp();
+  const int ncs = chunk_stride(a.T);
+  for (int x = lane; x < a.E; x += 32) {
+    const int c = s_hist[x];
+    a.hist[static_cast<int64_t>(x) * ncs + g] = c;
+    if (c) atomicAdd(a.totals + x, c);
+    s_hist[x] = 0;
+  }
+  __syncwarp();
+}
+
+// Ranks chunks [g0, g1) (warp w takes chunks g0+w, g0+w+8, ...).
+template <int KMAX>
+__device__ __forceinline__ void rank_chunks(const DispatchArgs& a, const int32_t* idx, int g0,
+                                            int g1) {
+  __shared__ int s_hist[kRouteWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int x = lane; x < a.E; x += 32) s_hist[warp][x] = 0;
+  __syncwarp();
+  for (int g = g0 + warp; g < g1; g += kRouteWarps) rank_chunk<KMAX>(a, idx, g, s_hist[warp]);
+}
+
+// Ranks every chunk of this block's range.
+template <int KMAX>
+__device__ __forceinline__ void rank_block_chunks(const DispatchArgs& a, const int32_t* idx) {
+  const int g0 = blockIdx.x * a.cpb;
+  rank_chunks<KMAX>(a, idx, g0, min(g0 + a.cpb, num_chunks(a.T)));
+}
+
+// True in the one block that arrives last; every thread of the block must call
+// it.  The barrier orders all of this block's writes before thread 0's
+// acquire-release increment of the counter (release is cumulative over what
+// the barrier made visible to thread 0); the last block's increment acquires
+// every other block's writes, and its closing barrier passes them on to the
+// block's threads.
+__device__ __forceinline__ bool arrive_last_block(unsigned int* done) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(done)
+                 : "memory");
+    s_last = (prev == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  return s_last != 0;
+}
+
+// Last block of a routing or ranking grid: counts (from the totals, which it
+// clears for the next call), kept and offsets.  Leaves the counts in s_cnt
+// (shared, >= E entries).
+__device__ void dispatch_finalize(const DispatchArgs& a, int* s_cnt) {
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    s_cnt[e] = __ldcg(a.totals + e);
+    a.totals[e] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int run = 0;
+    for (int base = 0; base < a.E; base += 32) {
+      const int x = base + lane;
+      const int c = x < a.E ? s_cnt[x] : 0;
+      const int kp = c < a.C ? c : a.C;
+      int w = kp;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += u;
+      }
+      if (x < a.E) {
+        a.counts[x] = c;
+        a.kept[x] = kp;
+        a.offsets[x] = run + w - kp;
+      }
+      run += __shfl_sync(0xffffffffu, w, 31);
+    }
+    if (lane == 0) a.offsets[a.E] = run;
+  }
+  __syncthreads();
+}
+
+// P, f and aux (the routing grid's last block, or an extra block of the
+// combine kernel), fp32 throughout (the FP64 pipe
+// of this GPU is 64x slower) and in a fixed order.  Warp w reduces the rows
+// of partials of experts w, w+8, ...: lane l sums blocks l, l+32, ... in
+// ascending order, a fixed shuffle tree combines the lanes.  The loads of up
+// to 16 (expert, 32-block step) pairs per lane are in flight together, and
+// consecutive lanes read consecutive blocks (one 128-byte line per warp load).
+// The arg-max totals are read up front (and cleared for the next call).
+__device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
+  constexpr int kBatch = 16;
+  __shared__ float s_fp[kMaxExperts];
+  __shared__ int s_am[kMaxExperts];
+  const int E = a.E, nb = a.nb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {   // all arg-max totals at once
+    s_am[e] = static_cast<int>(__ldcg(a.a_tot + e));
+    a.a_tot[e] = 0u;
+  }
+  __syncthreads();
+  const int steps = (nb + 31) / 32;
+  const int per_warp = (E + kRouteWarps - 1) / kRouteWarps;
+  const int pairs = per_warp * steps;   // expert-major: steps of one expert are consecutive
+  float ps = 0.f;
+  int cur = -1;
+  auto flush = [&](int e) {
+    float p = ps;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+    if (lane == 0) {
+      const float Pe = p / static_cast<float>(a.T);
+      const int cnt = (a.aux_f == AUXF_ARGMAX) ? s_am[e] : (s_cnt ? s_cnt[e] : __ldg(a.counts + e));
+      const float fe = static_cast<float>(cnt) / static_cast<float>(a.T);
+      a.P[e] = Pe;
+      a.f[e] = fe;
+      s_fp[e] = fe * Pe;
+    }
+  };
+  for (int p0 = 0; p0 < pairs; p0 += kBatch) {
+    float pv[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int p = p0 + i;
+      const int e = warp + kRouteWarps * (p / steps);
+      const int b = (p % steps) * 32 + lane;
+      const bool ok = p < pairs && e < E && b < nb;
+      float* src = a.p_part + static_cast<int64_t>(ok ? e : 0) * nb + (ok ? b : 0);
+      pv[i] = ok ? __ldcg(src) : 0.f;
+      if (ok) *src = 0.f;   // zero for the next call
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int p = p0 + i;
+      const int e = warp + kRouteWarps * (p / steps);
+      if (p < pairs && e < E) {          // warp-uniform
+        if (e != cur) {
+          if (cur >= 0) flush(cur);
+          cur = e;
+          ps = 0.f;
+        }
+        ps += pv[i];
+      }
+    }
+  }
+  if (cur >= 0) flush(cur);
+  __syncthreads();
+  if (warp == 0) {   // aux = alpha * E * sum_e f_e P_e: lane-strided, then a fixed tree
+    float sum = 0.f;
+    for (int x = lane; x < E; x += 32) sum += s_fp[x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) *a.aux = a.alpha * static_cast<float>(E) * sum;
+  }
+}
+
+// Common tail of the routing kernels: statistics partials, chunk ranking, and
+// the last block's finalize.
+template <int NPL, int KMAX>
+__device__ __forceinline__ void route_block_tail(const RouteArgs& a, const LaneStats<NPL>& st) {
+  flush_stats<NPL>(st, a.E, a.p_part, a.a_tot);
+  __syncthreads();   // this block's idx writes are visible to all its warps
+  rank_block_chunks<KMAX>(a.dp, a.idx);
+  if (arrive_last_block(a.dp.done)) {
+    __shared__ int s_cnt[kMaxExperts];
+    dispatch_finalize(a.dp, s_cnt);
+    if (!a.defer_stats) stats_finalize(stats_args(a, gridDim.x), s_cnt);
+    if (threadIdx.x == 0) *a.dp.done = 0u;   // ready for the next grid on this workspace
   }
 }
 
@@ -243,16 +531,26 @@ __device__ __forceinline__ void load_biases(const RouteArgs& a, int lane, float 
   }
 }
 
+template <typename TE>
+__device__ __forceinline__ float to_f32(TE v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
 // Gate from precomputed logits (tensor-core router), E <= 32 * NPL.
-template <int NPL>
-__global__ void __launch_bounds__(kRouteWarps * 32) k_gate(const RouteArgs a) {
+template <int NPL, int KMAX>
+__global__ void __launch_bounds__(kRouteThreads) k_gate(const RouteArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float lb[NPL], sb[NPL];
   load_biases<NPL>(a, lane, lb, sb);
   LaneStats<NPL> st;
   st.zero();
-  const int nw = gridDim.x * kRouteWarps;
-  for (int t = blockIdx.x * kRouteWarps + warp; t < a.T; t += nw) {
+  const int t0 = blockIdx.x * a.dp.cpb * kChunk;
+  const int t1 = min(t0 + a.dp.cpb * kChunk, a.T);
+  for (int t = t0 + warp; t < t1; t += kRouteWarps) {
     float l[NPL];
     const float* row = a.logits_in + static_cast<int64_t>(t) * a.ld_in;
 #pragma unroll
@@ -264,31 +562,27 @@ __global__ void __launch_bounds__(kRouteWarps * 32) k_gate(const RouteArgs a) {
     gate_token<NPL>(l, sb, a.E, a.k, a.route, a.renorm, lane,
                     a.idx + static_cast<int64_t>(t) * a.k, a.w + static_cast<int64_t>(t) * a.k, st);
   }
-  flush_stats<NPL>(st, a.E, a.p_part, a.c_part, a.a_part);
+  route_block_tail<NPL, KMAX>(a, st);
 }
-
-template <typename TE>
-__device__ __forceinline__ float to_f32(TE v);
-template <>
-__device__ __forceinline__ float to_f32<float>(float v) { return v; }
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // Fused router + gating on the CUDA cores for E <= EP <= 64: lane l sums the
 // products of d-indices l, l+32, ... for all experts (fp32 FMA), a butterfly
 // all-reduce completes the E logits, then the token is gated in registers.
-template <typename TE, int EP>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+template <typename TE, int EP, int KMAX>
+__global__ void __launch_bounds__(kRouteThreads)
 k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__ w_g) {
   constexpr int NPL = (EP + 31) / 32;
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float lb[NPL], sb[NPL];
   load_biases<NPL>(a, lane, lb, sb);
   LaneStats<NPL> st;
   st.zero();
-  const int nw = gridDim.x * kRouteWarps;
   const int E = a.E, d = a.d;
-  for (int t = blockIdx.x * kRouteWarps + warp; t < a.T; t += nw) {
+  const int t0 = blockIdx.x * a.dp.cpb * kChunk;
+  const int t1 = min(t0 + a.dp.cpb * kChunk, a.T);
+  for (int t = t0 + warp; t < t1; t += kRouteWarps) {
     float acc[EP];
 #pragma unroll
     for (int e = 0; e < EP; ++e) acc[e] = 0.f;
@@ -317,68 +611,139 @@ k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__
     gate_token<NPL>(l, sb, E, a.k, a.route, a.renorm, lane,
                     a.idx + static_cast<int64_t>(t) * a.k, a.w + static_cast<int64_t>(t) * a.k, st);
   }
-  flush_stats<NPL>(st, E, a.p_part, a.c_part, a.a_part);
+  route_block_tail<NPL, KMAX>(a, st);
 }
 
-// f_i, P_i and aux from the per-block partials.  Block e reduces expert e's
-// row (thread t sums partial rows t, t+256, ... in float64; warps then combine
-// in a fixed tree), writes f[e] and P[e], and the last block to finish (a
-// counter in the workspace header, reset by that block) sums f_e * P_e in
-// expert order for aux.  Every sum has a fixed order: bitwise reproducible.
-__global__ void __launch_bounds__(256)
-k_route_finalize(int nb, int T, int E, int aux_f, float alpha, const float* p_part,
-                 const int32_t* c_part, const int32_t* a_part, float* f, float* P, float* aux,
-                 double* fp_scratch, unsigned int* done_counter) {
-  __shared__ double s_p[8];
-  __shared__ int s_c[8], s_a[8];
-  __shared__ int s_last;
-  const int e = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(e) * nb;
-  double ps = 0.0;
-  int cs = 0, as = 0;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    ps += static_cast<double>(p_part[row + b]);
-    cs += c_part[row + b];
-    as += a_part[row + b];
-  }
+// Router + gating for short batches (T <= kSmallRouteMaxT), E <= EP <= 64:
+// one block per token.  When E is a multiple of VE (the experts in 16 bytes),
+// thread (g, s) of the block takes expert group g (VE consecutive experts,
+// one 16-byte load per row of W_g) and the d-indices s, s+S, ...; otherwise
+// thread i takes the 16-byte vectors i, i+256, ... of x with scalar loads of
+// the matching W_g rows.  fp32 FMA, a block reduction in a fixed order
+// completes the E logits, warp 0 gates the token.  The last block ranks every
+// chunk of the batch and finalises.
+constexpr int kSmallRouteMaxT = 512;
+
+template <typename TE, int EP, int KMAX>
+__global__ void __launch_bounds__(kRouteThreads)
+k_route_small(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__ w_g) {
+  constexpr int NPL = (EP + 31) / 32;
+  constexpr int VE = 16 / static_cast<int>(sizeof(TE));   // elements per 16 bytes
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float s_red[kRouteWarps][EP];
+  __shared__ float s_logit[EP];
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, d = a.d;
+  const TE* xr = x + static_cast<int64_t>(t) * d;
+  if (E % VE == 0) {
+    const int G = E / VE;
+    int Gp = 1;
+    while (Gp < G) Gp <<= 1;
+    const int S = kRouteThreads / Gp;        // threads per expert group
+    const int g = tid / S, sl = tid % S;
+    float acc[VE];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    cs += __shfl_xor_sync(0xffffffffu, cs, o);
-    as += __shfl_xor_sync(0xffffffffu, as, o);
-  }
-  if (lane == 0) {
-    s_p[warp] = ps;
-    s_c[warp] = cs;
-    s_a[warp] = as;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    ps = 0.0;
-    cs = 0;
-    as = 0;
-    for (int w = 0; w < (blockDim.x >> 5); ++w) {
-      ps += s_p[w];
-      cs += s_c[w];
-      as += s_a[w];
+    for (int v = 0; v < VE; ++v) acc[v] = 0.f;
+    if (g < G) {
+#pragma unroll 4
+      for (int i = sl; i < d; i += S) {
+        const float xv = to_f32<TE>(__ldg(xr + i));
+        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_g + static_cast<int64_t>(i) * E + g * VE));
+        const TE* wp = reinterpret_cast<const TE*>(&wv);
+#pragma unroll
+        for (int v = 0; v < VE; ++v) acc[v] = fmaf(xv, to_f32<TE>(wp[v]), acc[v]);
+      }
     }
-    const float Pe = static_cast<float>(ps / static_cast<double>(T));
-    const float fe = static_cast<float>(aux_f == AUXF_ARGMAX ? as : cs) / static_cast<float>(T);
-    P[e] = Pe;
-    f[e] = fe;
-    fp_scratch[e] = static_cast<double>(fe) * static_cast<double>(Pe);
-    __threadfence();
-    s_last = (atomicAdd(done_counter, 1u) == static_cast<unsigned int>(E - 1)) ? 1 : 0;
+    const int W = S < 32 ? S : 32;           // lanes of one group inside a warp
+    for (int o = W >> 1; o > 0; o >>= 1) {
+#pragma unroll
+      for (int v = 0; v < VE; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], o);
+    }
+    if (lane % W == 0) {
+#pragma unroll
+      for (int v = 0; v < VE; ++v) s_red[warp][(lane / W) * VE + v] = acc[v];
+    }
+    __syncthreads();
+    if (tid < E) {
+      const int ge = tid / VE, v = tid % VE;
+      float sum = 0.f;
+      if (S >= 32) {
+        for (int w = ge * S / 32; w < (ge + 1) * S / 32; ++w) sum += s_red[w][v];
+      } else {
+        sum = s_red[(ge * S) / 32][(((ge * S) % 32) / S) * VE + v];
+      }
+      s_logit[tid] = sum;
+    }
+  } else {
+    float acc[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+    for (int i0 = tid * VE; i0 < d; i0 += blockDim.x * VE) {
+      const uint4 xv4 = __ldg(reinterpret_cast<const uint4*>(xr + i0));
+      const TE* xs = reinterpret_cast<const TE*>(&xv4);
+#pragma unroll
+      for (int u = 0; u < VE; ++u) {
+        const float xv = to_f32<TE>(xs[u]);
+        const TE* wr = w_g + static_cast<int64_t>(i0 + u) * E;
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+          if (e < E) acc[e] = fmaf(xv, to_f32<TE>(__ldg(wr + e)), acc[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      const float v = warp_sum(acc[e]);
+      if (lane == 0) s_red[warp][e] = v;
+    }
+    __syncthreads();
+    if (tid < E) {
+      float sum = 0.f;
+      for (int w = 0; w < kRouteWarps; ++w) sum += s_red[w][tid];
+      s_logit[tid] = sum;
+    }
   }
   __syncthreads();
-  if (s_last && threadIdx.x == 0) {
-    __threadfence();
-    const volatile double* fp = fp_scratch;
-    double sum = 0.0;
-    for (int i = 0; i < E; ++i) sum += fp[i];
-    *aux = static_cast<float>(static_cast<double>(alpha) * E * sum);
-    *done_counter = 0u;   // ready for the next call on this workspace
+  LaneStats<NPL> st;
+  st.zero();
+  if (warp == 0) {
+    float lb[NPL], sb[NPL];
+    load_biases<NPL>(a, lane, lb, sb);
+    float l[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      l[i] = (e < E ? s_logit[e] : 0.f) + lb[i];
+      if (a.logits_out && e < E) a.logits_out[static_cast<int64_t>(t) * E + e] = l[i];
+    }
+    gate_token<NPL>(l, sb, E, a.k, a.route, a.renorm, lane,
+                    a.idx + static_cast<int64_t>(t) * a.k, a.w + static_cast<int64_t>(t) * a.k, st);
+  }
+  flush_stats<NPL>(st, E, a.p_part, a.a_tot);
+  if (arrive_last_block(a.dp.done)) {
+    __shared__ int s_cnt[kMaxExperts];
+    rank_chunks<KMAX>(a.dp, a.idx, 0, num_chunks(a.T));
+    __syncthreads();
+    dispatch_finalize(a.dp, s_cnt);
+    if (!a.defer_stats) stats_finalize(stats_args(a, gridDim.x), s_cnt);
+    if (threadIdx.x == 0) *a.dp.done = 0u;
+  }
+}
+
+// Ranking of caller-supplied expert indices (the standalone dispatch entry
+// points): the same chunk ranks, prefixes, counts, kept and offsets as the
+// routing kernels produce.
+template <int KMAX>
+__global__ void __launch_bounds__(kRouteThreads) k_dispatch_rank(const DispatchArgs a,
+                                                                 const int32_t* idx) {
+  griddep_wait();
+  griddep_launch_dependents();
+  rank_block_chunks<KMAX>(a, idx);
+  if (arrive_last_block(a.done)) {
+    __shared__ int s_cnt[kMaxExperts];
+    dispatch_finalize(a, s_cnt);
+    if (threadIdx.x == 0) *a.done = 0u;
   }
 }
 
@@ -386,6 +751,8 @@ k_route_finalize(int nb, int T, int E, int aux_f, float alpha, const float* p_pa
 // the tensor-core router.
 __global__ void k_transpose_wg(const __nv_bfloat16* __restrict__ w_g, int d, int E, int E_pad,
                                __nv_bfloat16* __restrict__ wgT) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ __nv_bfloat16 tile[32][33];
   const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += blockDim.y) {

@@ -187,8 +187,10 @@ def permute(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm
           _stream(stream))
 
 
-# T*k limit of moe_permute_noalloc (MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS in moe.h)
+# limits of moe_permute_noalloc (MOE_PERMUTE_NOALLOC_MAX_* in moe.h): T*k and
+# ceil(T/32)*E
 PERMUTE_NOALLOC_MAX_ASSIGNMENTS = 1 << 20
+PERMUTE_NOALLOC_MAX_CHUNK_COUNTS = 1 << 20
 
 
 def permute_noalloc(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm,
@@ -196,10 +198,11 @@ def permute_noalloc(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of
     """moe_permute_noalloc: the dispatch of ``permute`` without a workspace.
 
     For callers that cannot allocate device memory themselves: its scratch is a
-    fixed 4 MiB array inside the library.  The first call on a device must come
+    fixed 8 MiB array inside the library.  The first call on a device must come
     before any stream capture; calls that may overlap on the GPU race, because
     they share that array.  Raises MoEError (MOE_ERR_UNSUPPORTED) when
-    T*k > PERMUTE_NOALLOC_MAX_ASSIGNMENTS.
+    T*k > PERMUTE_NOALLOC_MAX_ASSIGNMENTS or ceil(T/32)*E >
+    PERMUTE_NOALLOC_MAX_CHUNK_COUNTS.
     """
     T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
     dt = TORCH_DTYPES[cfg["dtype"]]

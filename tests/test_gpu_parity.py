@@ -97,6 +97,8 @@ def check_steps(cfg, inp, st, rep_ref):
 SMALL = {
     "fp32_top2_bias": dict(name="tiny_fp32_top2", T=300, d_model=64, d_ff=96, E=8, k=2,
                            nonzero_bias=True),
+    "fp32_warp_router_e24": dict(name="tiny_fp32_top2", T=700, d_model=96, d_ff=64, E=24, k=3,
+                                 route="topk_softmax"),
     "switch_cap_small": dict(name="switch_top1_cap", T=1000, d_model=128, d_ff=384, E=16, k=1),
     "switch_cap_renorm": dict(name="switch_top1_cap", T=600, d_model=64, d_ff=128, E=8, k=1,
                               renorm=1, aux_f="topk_count"),
@@ -246,3 +248,38 @@ def test_invalid_argument_enqueues_nothing():
         moe.forward(bad, inp["x"], inp["w_g"], inp["w1"], inp["w2"], layer.out, layer.ws)
     assert ei.value.status in (1,)
     moe.check_status(layer.ws)
+
+
+def test_out_of_range_expert_index_is_dropped_and_reported():
+    """moe_permute takes caller-supplied indices: one outside [0, E) drops that
+    assignment (slot -1), the others are dispatched as usual, and the status
+    word reports MOE_ERR_INVALID_ARG."""
+    cfg = synth.workload("switch_top1_cap", T=96, d_model=64, d_ff=64, E=8, k=2,
+                         capacity_factor=0.0, renorm=1, aux_f="topk_count")
+    T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
+    inp = synth.make_inputs(cfg, device=DEV)
+    g = torch.Generator().manual_seed(3)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    idx[5, 1] = E + 3
+    idx[40, 0] = -1
+    idx = idx.to(DEV)
+    ws = moe.new_workspace(cfg, DEV)
+    z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
+    o = dict(counts=z((E,), torch.int32), kept=z((E,), torch.int32),
+             offsets=z((E + 1,), torch.int32), perm_token=z((T * k,), torch.int32),
+             slot_of=z((T * k,), torch.int32), x_perm=z((T * k, d), torch.bfloat16))
+    moe.permute(cfg, inp["x"], idx, o["counts"], o["kept"], o["offsets"], o["perm_token"],
+                o["slot_of"], o["x_perm"], ws)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.check_status(ws)
+    assert ei.value.status == 1
+    moe.check_status(ws)          # the status word was cleared by the read
+    slot = o["slot_of"].cpu().view(T, k)
+    assert slot[5, 1] == -1 and slot[40, 0] == -1
+    good = idx.cpu().clone()
+    good[5, 1] = -1
+    good[40, 0] = -1
+    want = torch.bincount(good[good >= 0].long(), minlength=E)
+    assert torch.equal(o["counts"].cpu(), want.to(torch.int32))
+    assert int(o["offsets"][-1]) == T * k - 2
+    assert int((slot >= 0).sum()) == T * k - 2

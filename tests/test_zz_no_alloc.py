@@ -98,3 +98,11 @@ def test_noalloc_permute_rejects_sizes_beyond_its_array():
     # at the limit the size check passes and the null counts pointer is what fails
     s = moe.lib().moe_permute_noalloc(ctypes.byref(c), 1, 1, None, 1, 1, 1, 1, 1, None)
     assert s == 1, moe.status_string(s)
+    # the per-chunk expert counts (ceil(T/32) * E entries) have a limit of their own
+    chunks = moe.PERMUTE_NOALLOC_MAX_CHUNK_COUNTS // 256
+    for T, want in ((32 * chunks, 1), (32 * chunks + 1, 2)):
+        cfg = synth.workload("deepseek_v3_top8", T=T, d_model=64, d_ff=64, E=256, k=1,
+                             n_shared=0)
+        c = moe.make_config(cfg)
+        s = moe.lib().moe_permute_noalloc(ctypes.byref(c), 1, 1, None, 1, 1, 1, 1, 1, None)
+        assert s == want, (T, moe.status_string(s))
