@@ -175,10 +175,13 @@ def algorithmic_ffn(cfg, kept, elem):
 def kernel_launches_per_step(cfg) -> int:
     """Kernels one moe_forward enqueues (see moe_api.cu): routing grid (plus the
     W_g transpose and tensor-core router GEMM ahead of it for bf16 layers with
-    E > 64 or T > 512), permute, up-projection, down-projection, combine."""
+    E > 64 or T > 512), permute, up-projection, down-projection, and the
+    combine unless a bf16 top-1 layer without shared experts folds it into
+    the down-projection."""
     tc_router = cfg["dtype"] == "bf16" and (cfg["E"] > 64 or cfg["T"] > 512)
     route = 3 if tc_router else 1
-    return route + 1 + 2 + 1
+    fused = cfg["dtype"] == "bf16" and cfg["k"] == 1 and cfg.get("n_shared", 0) == 0
+    return route + 1 + 2 + (0 if fused else 1)
 
 
 def _timed_graph_loop(graph, flush, stream, steps, before=None):
@@ -227,8 +230,8 @@ def run_ours(args, rank, world, local_rank):
     o = dict(counts=z((E,), torch.int32), kept=z((E,), torch.int32),
              offsets=z((E + 1,), torch.int32), perm_token=z((T * k,), torch.int32),
              slot_of=z((T * k,), torch.int32), x_perm=z((T * k, d), dt),
-             y_perm=z((T * k, d), torch.float32), out=z((T, d), dt))
-    y_sh = z((S, T, d), torch.float32) if S else None
+             y_perm=z((T * k, d), dt), out=z((T, d), dt))
+    y_sh = z((S, T, d), dt) if S else None
     ws2 = moe.new_workspace(cfg, dev)
     moe.permute(cfg, inp["x"], layer.topk_idx, o["counts"], o["kept"], o["offsets"],
                 o["perm_token"], o["slot_of"], o["x_perm"], ws2)

@@ -166,11 +166,11 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
  *   x_perm [T*k, d], offsets [E+1] (device; read on the device only).
  *   w1 [E,F,d], b1 [E,F] or NULL, w2 [E,d,F], b2 [E,d] or NULL.
  *   Shared experts (cfg.n_shared > 0): x [T,d], ws1 [S,F,d], wsb1 [S,F] or
- *   NULL, ws2 [S,d,F], wsb2 [S,d] or NULL, output y_shared [S,T,d] fp32.
- *   Output y_perm [T*k, d] fp32: row r = FFN_e(x_perm[r]) for the expert e
- *   whose range holds r; rows >= offsets[E] unspecified.  The hidden
- *   activation GELU(x W1^T + b1) is rounded to dtype (the second GEMM's
- *   operand type) in `ws`; the expert outputs stay fp32 for the combine. */
+ *   NULL, ws2 [S,d,F], wsb2 [S,d] or NULL, output y_shared [S,T,d] dtype.
+ *   Output y_perm [T*k, d] dtype: row r = FFN_e(x_perm[r]) for the expert e
+ *   whose range holds r; rows >= offsets[E] unspecified.  Both GEMMs
+ *   accumulate in fp32; the hidden activation GELU(x W1^T + b1) (in `ws`) and
+ *   the expert outputs are rounded once to dtype. */
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                            const void* w1, const void* b1, const void* w2, const void* b2,
                            const void* x, const void* ws1, const void* wsb1,
@@ -181,13 +181,17 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int3
 /* Gate-weighted un-permute: out[t] = sum_{j: slot_of[t*k+j] >= 0}
  * topk_w[t,j] * y_perm[slot_of[t*k+j]] + sum_s y_shared[s,t], accumulated in
  * fp32 in ascending j then s, stored once in dtype.  y_perm [T*k, d] and
- * y_shared [S,T,d] are fp32; y_shared may be NULL when n_shared = 0. */
+ * y_shared [S,T,d] are in dtype; y_shared may be NULL when n_shared = 0. */
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_of,
                        const float* topk_w, const void* y_shared, void* out,
                        moe_stream stream);
 
 /* The whole layer: route -> permute -> grouped FFN -> combine, all stream
- * ordered with no host synchronisation.  Intermediates live in `ws`.
+ * ordered with no host synchronisation.  Intermediates live in `ws`.  For a
+ * bf16 top-1 layer without shared experts the combine is folded into the
+ * down-projection (out[t] = w_t * FFN(x_t) rounded once to bf16, 0 for a
+ * dropped token), which skips the rounding of the expert output that the
+ * step-by-step entry points do.
  *   Outputs: out [T,d] dtype; topk_idx [T,k]; topk_w [T,k]; counts [E];
  *   f [E]; P [E]; aux [1].  Any of topk_idx .. aux may be NULL except
  *   out. */

@@ -7,9 +7,8 @@
 //             SimpleMoELayer's torch.where produces), perm_token, and the row
 //             gather x -> x_perm.
 //  k_combine  out[t] = sum_j w[t,j] * y[slot_of[t,j]] + sum_s y_shared[s,t],
-//             a gather in fixed order (no atomics); y is fp32, the sum is fp32
-//             and out is rounded once to its dtype.  In a whole-layer pass one
-//             extra block reduces the routing statistics meanwhile.
+//             a gather in fixed order (no atomics); y is in the layer dtype,
+//             the sum is fp32 and out is rounded once to its dtype.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -26,20 +25,29 @@ namespace moe {
 // sums in shared memory).  Then one warp per token: the rank of assignment
 // (t, j) inside its expert is that prefix plus its in-chunk rank; it is kept
 // iff the rank is below kept[e], and lands in row offsets[e] + rank of
-// x_perm.  x is read once and written k times with 16-byte vectors.
+// x_perm.  x is read once and written k times with 16-byte vectors.  In a
+// whole-layer pass of a top-1 layer without shared experts (whose combine is
+// fused into the down-projection), tokens with no kept assignment get their
+// zero output row here (zero_out), and one extra block reduces the routing
+// statistics meanwhile.
 template <int KMAX>
 __global__ void __launch_bounds__(256)
 k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
           const int32_t* __restrict__ hist, const int32_t* __restrict__ kept,
           const int32_t* __restrict__ offsets, int T, int k, int E, int ncs, int tpb,
           int row_bytes, const uint8_t* __restrict__ x, uint8_t* __restrict__ x_perm,
-          int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_of) {
+          int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_of,
+          uint8_t* __restrict__ zero_out, const StatsArgs st) {
   __shared__ int s_pre[kMaxExperts];
   __shared__ int s_list[32 * kMaxK];
   __shared__ unsigned int s_mark[kMaxExperts / 32];
   __shared__ int s_n;
   griddep_wait();
   griddep_launch_dependents();
+  if (st.p_part && blockIdx.x == gridDim.x - 1) {   // the extra block: routing statistics
+    stats_finalize(st, nullptr);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * tpb, t1 = min(t0 + tpb, T);
   const int g = t0 / kChunk;
@@ -102,6 +110,15 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
     int slot[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
+    if (zero_out) {   // a token with every assignment dropped gets a zero output row
+      bool any = false;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) any |= (j < k && slot[j] >= 0);
+      if (!any) {
+        uint4* o = reinterpret_cast<uint4*>(zero_out + static_cast<int64_t>(t) * row_bytes);
+        for (int c = lane; c < nvec; c += 32) o[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     for (int c0 = 0; c0 < nvec; c0 += 32 * PF) {
       if (c0 > 0) {
 #pragma unroll
@@ -155,18 +172,13 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
 
 template <typename TE, int KMAX>
 __global__ void __launch_bounds__(256)
-k_combine(const float* __restrict__ y, const int32_t* __restrict__ slot_of,
-          const float* __restrict__ w, const float* __restrict__ y_shared, int n_shared, int T,
-          int k, int d, TE* __restrict__ out, const StatsArgs st) {
+k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
+          const float* __restrict__ w, const TE* __restrict__ y_shared, int n_shared, int T,
+          int k, int d, TE* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
-  if (st.p_part && blockIdx.x == gridDim.x - 1) {   // the extra block: routing statistics
-    stats_finalize(st, nullptr);
-    return;
-  }
-  const int grid = st.p_part ? gridDim.x - 1 : gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = grid * (blockDim.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
   const int nchunk = d / 8;
   for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += nw) {
     int slot[KMAX];

@@ -38,7 +38,10 @@
 
 namespace moe {
 
-enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_F32 = 2 };
+// Epilogues: fp32 logits (router); GELU(acc + b1) in bf16 (up-projection);
+// acc + b2 in bf16 (down-projection); and the down-projection fused with the
+// top-1 combine: out[token of the row] = w[token] * (acc + b2) in bf16.
+enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_BF16 = 2, EPI_SCATTER_BF16 = 3 };
 enum : int {
   DEV_ERR_WAIT_PRODUCER = 1,
   DEV_ERR_WAIT_MMA = 2,
@@ -62,6 +65,8 @@ struct TcArgs {
   int streamk;                 // 1: stream-K split of the (tile, k-block) iterations
   float* partial;              // [kMaxGemmCtas][BN/16][128][16] fp32 (stream-K)
   int* flags;                  // [kMaxGemmCtas][4] zero between launches (stream-K)
+  const int32_t* scatter_token;  // EPI_SCATTER_BF16: token of each output row
+  const float* scatter_w;        // EPI_SCATTER_BF16: gate weight of each token (k = 1)
 };
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uint64_t limit) {
@@ -389,7 +394,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       const bool routed = g < gs.E;
       const int row_in_grp = m_blk * BM + row;
       const bool valid = row_in_grp < c.tb.rows[g];
-      const int64_t orow = static_cast<int64_t>(c.tb.out_row0[g]) + row_in_grp;
+      int64_t orow = static_cast<int64_t>(c.tb.out_row0[g]) + row_in_grp;
+      float gate_w = 1.f;
+      if (EPI == EPI_SCATTER_BF16 && valid) {   // the output row is the token's own row
+        const int tok = __ldg(args.scatter_token + orow);
+        gate_w = __ldg(args.scatter_w + tok);
+        orow = tok;
+      }
       const __nv_bfloat16* bias = nullptr;
       if (EPI != EPI_F32) {
         if (routed && args.bias0) bias = args.bias0 + static_cast<int64_t>(gs.offsets ? g : 0) * args.N;
@@ -422,7 +433,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           for (int i = 0; i < 16; ++i)
             if (col + i < args.N) v[i] += __bfloat162float(bias[col + i]);
         }
-        if (EPI == EPI_F32 || EPI == EPI_BIAS_F32) {
+        if (EPI == EPI_F32) {
           float* o = static_cast<float*>(routed ? args.out : args.out1) + orow * args.ldo + col;
           if (col + 16 <= args.N) {
 #pragma unroll
@@ -432,8 +443,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
             for (int i = 0; i < 16 && col + i < args.N; ++i) o[i] = v[i];
           }
         } else {
+          if (EPI == EPI_GELU_BF16) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+            for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
+          } else if (EPI == EPI_SCATTER_BF16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= gate_w;
+          }
           __nv_bfloat16* o =
               static_cast<__nv_bfloat16*>(routed ? args.out : args.out1) + orow * args.ldo + col;
           if (col + 16 <= args.N) {

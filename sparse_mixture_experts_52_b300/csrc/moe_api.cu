@@ -126,8 +126,8 @@ Layout make_layout(const moe_config& c) {
   L.aux = take(4);
   L.x_perm = take(T * k * d * eb);
   L.H = take((T * k + S * T) * F * eb);
-  L.Y = take(T * k * d * 4);
-  L.Ys = take(S * T * d * 4);
+  L.Y = take(T * k * d * eb);
+  L.Ys = take(S * T * d * eb);
   // stream-K partial tiles of the tensor-core FFN: one 128 x 256 fp32 slot per CTA
   L.sk_part = take(c.dtype == MOE_BF16 ? static_cast<size_t>(kMaxGemmCtas) * 128 * 256 * 4 : 0);
   L.total = off;
@@ -315,11 +315,17 @@ moe_status launch_tc(int epi, const CUtensorMap& a0, const CUtensorMap& a1,
       case 128: return launch_tc_inst<128, 6, EPI_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
       case 256: return launch_tc_inst<256, 4, EPI_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
     }
-  } else if (epi == EPI_BIAS_F32) {
+  } else if (epi == EPI_BIAS_BF16) {
     switch (BN) {
-      case 64: return launch_tc_inst<64, 8, EPI_BIAS_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 128: return launch_tc_inst<128, 6, EPI_BIAS_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 256: return launch_tc_inst<256, 4, EPI_BIAS_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 64: return launch_tc_inst<64, 8, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 128: return launch_tc_inst<128, 6, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 256: return launch_tc_inst<256, 4, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
+    }
+  } else if (epi == EPI_SCATTER_BF16) {
+    switch (BN) {
+      case 64: return launch_tc_inst<64, 8, EPI_SCATTER_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 128: return launch_tc_inst<128, 6, EPI_SCATTER_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
+      case 256: return launch_tc_inst<256, 4, EPI_SCATTER_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
     }
   } else if (epi == EPI_GELU_BF16) {
     switch (BN) {
@@ -505,17 +511,20 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
 moe_status launch_permute(const moe_config& c, const int32_t* idx, const int32_t* crank,
                           const int32_t* hist, const int32_t* kept, const int32_t* offsets,
                           int32_t* perm_token, int32_t* slot_of, const void* x, void* x_perm,
-                          cudaStream_t st) {
+                          cudaStream_t st, void* zero_out = nullptr,
+                          const StatsArgs& stats = StatsArgs{}) {
   const int row_bytes = c.d_model * static_cast<int>(elem_bytes(c));
   int tpb = 32;
   while (tpb > 4 && (c.T + tpb - 1) / tpb < 2 * num_sms()) tpb >>= 1;
-  const int grid = std::max(1, (c.T + tpb - 1) / tpb);
+  // plus one block for the routing statistics in a whole-layer pass
+  const int grid = std::max(1, (c.T + tpb - 1) / tpb) + (stats.p_part ? 1 : 0);
   const int ncs = chunk_stride(c.T);
   const auto* xb = static_cast<const uint8_t*>(x);
   auto* xp = static_cast<uint8_t*>(x_perm);
 #define MOE_PERMUTE(KM)                                                                     \
   launch_pdl(k_permute<KM>, dim3(grid), dim3(256), 0, st, idx, crank, hist, kept, offsets, \
-             c.T, c.k, c.E, ncs, tpb, row_bytes, xb, xp, perm_token, slot_of)
+             c.T, c.k, c.E, ncs, tpb, row_bytes, xb, xp, perm_token, slot_of,             \
+             static_cast<uint8_t*>(zero_out), stats)
   switch (kmax_of(c.k)) {
     case 2: return MOE_PERMUTE(2);
     case 4: return MOE_PERMUTE(4);
@@ -583,8 +592,16 @@ struct FfnIn {
   const int32_t* offsets;
 };
 
+// The top-1 combine fused into the down-projection (bf16, k = 1, no shared
+// experts): each output row goes straight to out[token] scaled by the gate.
+struct FfnScatter {
+  void* out;                  // [T, d]
+  const int32_t* perm_token;  // token of each expert-ordered row
+  const float* w;             // [T] gate weights
+};
+
 moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& in, void* y_perm,
-                  void* y_shared, cudaStream_t st) {
+                  void* y_shared, cudaStream_t st, const FfnScatter* scatter = nullptr) {
   const int64_t T = c.T, Tk = static_cast<int64_t>(c.T) * c.k, S = c.n_shared;
   const int d = c.d_model, F = c.d_ff;
   void* H = at<uint8_t>(ws, L.H);
@@ -650,7 +667,13 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     dn.streamk = sp_dn.streamk;
     dn.partial = at<float>(ws, L.sk_part);
     dn.flags = at<int>(ws, L.status + kFlagsOffset);
-    return launch_tc(EPI_BIAS_F32, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
+    if (scatter) {
+      dn.out = scatter->out;
+      dn.scatter_token = scatter->perm_token;
+      dn.scatter_w = scatter->w;
+      return launch_tc(EPI_SCATTER_BF16, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
+    }
+    return launch_tc(EPI_BIAS_BF16, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
   }
   // fp32: CUDA-core grouped GEMMs
   const int64_t tiles_ub = (Tk + S * T + 63) / 64 + c.E + S;
@@ -692,15 +715,14 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
 }
 
 moe_status do_combine(const moe_config& c, const void* y_perm, const int32_t* slot_of,
-                      const float* w, const void* y_shared, void* out, cudaStream_t st,
-                      const StatsArgs& stats = StatsArgs{}) {
-  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8)) + (stats.p_part ? 1 : 0);
+                      const float* w, const void* y_shared, void* out, cudaStream_t st) {
+  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
   const int S = y_shared ? c.n_shared : 0;
 #define MOE_COMBINE(TE, KM)                                                                 \
   return launch_pdl(k_combine<TE, KM>, dim3(grid), dim3(256), 0, st,                        \
-                    static_cast<const float*>(y_perm), slot_of, w,                          \
-                    static_cast<const float*>(y_shared), S, c.T, c.k, c.d_model,             \
-                    static_cast<TE*>(out), stats)
+                    static_cast<const TE*>(y_perm), slot_of, w,                             \
+                    static_cast<const TE*>(y_shared), S, c.T, c.k, c.d_model,                \
+                    static_cast<TE*>(out))
   const int km = kmax_of(c.k);
   if (c.dtype == MOE_BF16) {
     if (km == 2) MOE_COMBINE(__nv_bfloat16, 2);
@@ -870,20 +892,13 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   int32_t* kept = at<int32_t>(ws, L.kept);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* slot_of = at<int32_t>(ws, L.slot_of);
+  int32_t* perm_token = at<int32_t>(ws, L.perm_token);
   void* x_perm = at<uint8_t>(ws, L.x_perm);
   // the routing grid also ranks the assignments: the permute follows directly
   if ((s = do_route(c, L, ws, x, w_g, logit_bias, select_bias,
                     RouteOut{nullptr, idx, w, fo, Po, ao, cnt, kept, offsets, 1}, st)) != MOE_OK)
     return s;
-  if ((s = launch_permute(c, idx, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist), kept,
-                          offsets, at<int32_t>(ws, L.perm_token), slot_of, x, x_perm, st)) !=
-      MOE_OK)
-    return s;
-  void* Y = at<uint8_t>(ws, L.Y);
-  void* Ys = at<uint8_t>(ws, L.Ys);
-  FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
-  if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
-  // the combine kernel's extra block reduces the routing statistics
+  // the permute kernel's extra block reduces the routing statistics
   StatsArgs sa{};
   sa.p_part = at<float>(ws, L.status + kPartOffset);
   sa.nb = route_grid(c, L);
@@ -896,7 +911,22 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   sa.f = fo;
   sa.P = Po;
   sa.aux = ao;
-  return do_combine(c, Y, slot_of, w, c.n_shared > 0 ? Ys : nullptr, out, st, sa);
+  // top-1 bf16 layers without shared experts: the combine is fused into the
+  // down-projection (and the permute writes the zero rows of dropped tokens)
+  const bool fused_combine = c.dtype == MOE_BF16 && c.k == 1 && c.n_shared == 0;
+  if ((s = launch_permute(c, idx, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist), kept,
+                          offsets, perm_token, slot_of, x, x_perm, st,
+                          fused_combine ? out : nullptr, sa)) != MOE_OK)
+    return s;
+  void* Y = at<uint8_t>(ws, L.Y);
+  void* Ys = at<uint8_t>(ws, L.Ys);
+  FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
+  if (fused_combine) {
+    const FfnScatter sc{out, perm_token, w};
+    return do_ffn(c, L, ws, in, Y, Ys, st, &sc);
+  }
+  if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
+  return do_combine(c, Y, slot_of, w, c.n_shared > 0 ? Ys : nullptr, out, st);
 }
 
 moe_status moe_check_status(void* ws, moe_stream stream) {

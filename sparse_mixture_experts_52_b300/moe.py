@@ -230,12 +230,12 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
     _want(w2, "w2", (E, d, F), dt)
     _want(b1, "b1", (E, F), dt, allow_none=not cfg.get("has_bias", 0))
     _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
-    _want(y_perm, "y_perm", (T * k, d), torch.float32)
+    _want(y_perm, "y_perm", (T * k, d), dt)
     if S:
         _want(x, "x", (T, d), dt)
         _want(ws1, "ws1", (S, F, d), dt)
         _want(ws2, "ws2", (S, d, F), dt)
-        _want(y_shared, "y_shared", (S, T, d), torch.float32)
+        _want(y_shared, "y_shared", (S, T, d), dt)
     _call("moe_grouped_ffn", ctypes.byref(make_config(cfg)), _p(x_perm), _p(offsets), _p(w1),
           _p(b1), _p(w2), _p(b2), _p(x), _p(ws1), _p(wsb1), _p(ws2), _p(wsb2), _p(y_perm),
           _p(y_shared), _p(ws), ws.numel(), _stream(stream))
@@ -244,12 +244,12 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
 def combine(cfg, y_perm, slot_of, topk_w, out, y_shared=None, stream=None):
     T, d, k, S = cfg["T"], cfg["d_model"], cfg["k"], cfg.get("n_shared", 0)
     dt = TORCH_DTYPES[cfg["dtype"]]
-    _want(y_perm, "y_perm", (T * k, d), torch.float32)
+    _want(y_perm, "y_perm", (T * k, d), dt)
     _want(slot_of, "slot_of", (T * k,), torch.int32)
     _want(topk_w, "topk_w", (T, k), torch.float32)
     _want(out, "out", (T, d), dt)
     if S:
-        _want(y_shared, "y_shared", (S, T, d), torch.float32)
+        _want(y_shared, "y_shared", (S, T, d), dt)
     _call("moe_combine", ctypes.byref(make_config(cfg)), _p(y_perm), _p(slot_of), _p(topk_w),
           _p(y_shared), _p(out), _stream(stream))
 
