@@ -477,8 +477,11 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
                         static_cast<const __nv_bfloat16*>(w_g), c.d_model, c.E, L.E_pad, wgT)) !=
         MOE_OK)
       return s;
+    // expert columns in tiles of at most 64: a wide router (E = 256) then
+    // spreads over four times as many CTAs as row tiles
+    const int bn_r = std::min(L.E_pad, 64);
     CUtensorMap ma, mb;
-    if (!map_a(&ma, x, c.d_model, c.T) || !map_b(&mb, wgT, c.d_model, L.E_pad, 1, L.E_pad))
+    if (!map_a(&ma, x, c.d_model, c.T) || !map_b(&mb, wgT, c.d_model, L.E_pad, 1, bn_r))
       return MOE_ERR_CUDA;
     TcArgs ta{};
     ta.gs = GroupSpec{nullptr, 1, c.T, 0, 0, 0, 0, 0, 0};
@@ -488,7 +491,7 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
     ta.out1 = logits_ws;
     ta.ldo = L.E_pad;
     ta.err = at<int>(ws, L.status);
-    s = launch_tc(EPI_F32, ma, ma, mb, mb, ta, L.E_pad, (c.T + 127) / 128 + 1, st);
+    s = launch_tc(EPI_F32, ma, ma, mb, mb, ta, bn_r, (c.T + 127) / 128 + 1, st);
     if (s != MOE_OK) return s;
     ra.logits_in = logits_ws;
     ra.ld_in = L.E_pad;
