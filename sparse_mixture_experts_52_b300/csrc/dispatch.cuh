@@ -192,26 +192,47 @@ k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
         wt[j] = __ldg(w + static_cast<int64_t>(t) * k + j);
       }
     }
-    for (int c = lane; c < nchunk; c += 32) {
-      float acc[8];
+    // two 8-element chunks per lane per pass: the loads of both (for every
+    // slot) are in flight together
+    constexpr int U = 2;
+    for (int c0 = 0; c0 < nchunk; c0 += 32 * U) {
+      float acc[U][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         if (j < k && slot[j] >= 0) {
-          float v[8];
-          load8(y + static_cast<int64_t>(slot[j]) * d + c * 8, v);
+          float v[U][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt[j], v[i], acc[i]);
+          for (int u = 0; u < U; ++u) {
+            const int c = c0 + lane + 32 * u;
+            if (c < nchunk) load8(y + static_cast<int64_t>(slot[j]) * d + c * 8, v[u]);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wt[j], v[u][i], acc[u][i]);
         }
       }
       for (int s = 0; s < n_shared; ++s) {
-        float v[8];
-        load8(y_shared + (static_cast<int64_t>(s) * T + t) * d + c * 8, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += v[i];
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (c < nchunk) {
+            float v[8];
+            load8(y_shared + (static_cast<int64_t>(s) * T + t) * d + c * 8, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[u][i] += v[i];
+          }
+        }
       }
-      store8(out + static_cast<int64_t>(t) * d + c * 8, acc);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + lane + 32 * u;
+        if (c < nchunk) store8(out + static_cast<int64_t>(t) * d + c * 8, acc[u]);
+      }
     }
   }
 }
@@ -237,11 +258,12 @@ struct SimtArgs {
 
 __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
   constexpr int BM = 64, BN = 64, BK = 16;
+  constexpr int LA = BK * BM / 256, LB = BK * BN / 256;   // elements per thread per k-step
   griddep_wait();
   griddep_launch_dependents();
   __shared__ GroupTable tb;
-  __shared__ float As[BK][BM + 4];
-  __shared__ float Bs[BK][BN + 4];
+  __shared__ float As[2][BK][BM + 4];
+  __shared__ float Bs[2][BK][BN + 4];
   const GroupSpec& gs = a.gs;
   const int G = gs.E + gs.n_shared;
   const int n_tiles = (a.N + BN - 1) / BN;
@@ -259,35 +281,62 @@ __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
     if (bias) bias += static_cast<int64_t>(gi) * a.N;
     const int rows = tb.rows[g];
     const int m0 = m_blk * BM, n0 = n_blk * BN;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < a.K; k0 += BK) {
-      for (int i = tid; i < BK * BM; i += 256) {
+    const int64_t arow0 = tb.a_row0[g];
+    // global -> registers for k-step k0 (the next step's loads are in flight
+    // while the current step computes from shared memory)
+    float ra[LA], rb[LB];
+    auto fetch = [&](int k0) {
+#pragma unroll
+      for (int q = 0; q < LA; ++q) {
+        const int i = tid + 256 * q;
         const int r = i / BK, kk = i % BK;
         const int gr = m0 + r, gk = k0 + kk;
-        As[kk][r] = (gr < rows && gk < a.K)
-                        ? A[(static_cast<int64_t>(tb.a_row0[g]) + gr) * a.lda + gk]
-                        : 0.f;
+        ra[q] = (gr < rows && gk < a.K) ? __ldg(A + (arow0 + gr) * a.lda + gk) : 0.f;
       }
-      for (int i = tid; i < BK * BN; i += 256) {
+#pragma unroll
+      for (int q = 0; q < LB; ++q) {
+        const int i = tid + 256 * q;
         const int n = i / BK, kk = i % BK;
         const int gn = n0 + n, gk = k0 + kk;
-        Bs[kk][n] = (gn < a.N && gk < a.K) ? B[static_cast<int64_t>(gn) * a.K + gk] : 0.f;
+        rb[q] = (gn < a.N && gk < a.K) ? __ldg(B + static_cast<int64_t>(gn) * a.K + gk) : 0.f;
       }
-      __syncthreads();
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+      for (int q = 0; q < LA; ++q) {
+        const int i = tid + 256 * q;
+        As[buf][i % BK][i / BK] = ra[q];
+      }
+#pragma unroll
+      for (int q = 0; q < LB; ++q) {
+        const int i = tid + 256 * q;
+        Bs[buf][i % BK][i / BK] = rb[q];
+      }
+    };
+    float acc[4][4] = {};
+    fetch(0);
+    stash(0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < a.K; k0 += BK) {
+      const bool more = k0 + BK < a.K;
+      if (more) fetch(k0 + BK);
 #pragma unroll
       for (int kk = 0; kk < BK; ++kk) {
         float av[4], bv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          av[i] = As[kk][ty * 4 + i];
-          bv[i] = Bs[kk][tx * 4 + i];
+          av[i] = As[buf][kk][ty * 4 + i];
+          bv[i] = Bs[buf][kk][tx * 4 + i];
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
       }
+      if (more) stash(buf ^ 1);
       __syncthreads();
+      buf ^= 1;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
