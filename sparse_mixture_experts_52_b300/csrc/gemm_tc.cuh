@@ -345,7 +345,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         for (int cc = 0; cc < NCC; ++cc) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(trow + cc * 16, r);
-          tmem_wait_ld();
+          tmem_wait_ld(r);
           float4* dst = reinterpret_cast<float4*>(slot + (static_cast<int64_t>(cc) * BM + row) * 16);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -410,7 +410,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       for (int cc = 0; cc < NCC; ++cc) {
         uint32_t r[16];
         tmem_ld_32x32b_x16(trow + cc * 16, r);
-        tmem_wait_ld();
+        tmem_wait_ld(r);
         const int col = n_blk * BN + cc * 16;
         if (!valid || col >= args.N) continue;
         float v[16];
