@@ -16,6 +16,7 @@
 #include "gemm_tc.cuh"
 #include "groups.cuh"
 #include "route.cuh"
+#include "route_tc.cuh"
 
 using namespace moe;
 
@@ -287,7 +288,7 @@ FfnSplit pick_ffn_split(int N, int64_t row_tiles, int sms) {
     if (bn > wide) continue;
     const int64_t tiles = row_tiles * ((N + bn - 1) / bn);
     const int64_t rounds = (tiles + sms - 1) / sms;
-    const int64_t cost = rounds * (bn + 64);
+    const int64_t cost = rounds * (bn + 16);
     if (cost < best_cost) {
       best_cost = cost;
       best = bn;
@@ -430,11 +431,53 @@ moe_status launch_route_small_e(const moe_config& c, cudaStream_t st, const Rout
   return launch_route_small<TE, 64>(km, c.T, st, ra, xt, wt);
 }
 
+// The tensor-core router with the gating in its epilogue: bf16, E <= 16, and
+// per-CTA softmax partials (one column per 128 tokens) that fit the header.
+// Its epilogue gates one token per thread, serially over the experts; past 16
+// experts that is slower on B300 than the separate gate kernel, which spreads
+// a token's experts over a warp (measured: 36 vs 27 us of routing at T = 4096,
+// E = 64).
+bool use_fused_tc_router(const moe_config& c) {
+  const int64_t ctas = (static_cast<int64_t>(c.T) + 127) / 128;
+  return use_tc_router(c) && c.E <= 16 &&
+         ctas * c.E <= static_cast<int64_t>(kMaxExperts) * kRouteMaxRows;
+}
+
 // Blocks of the routing grid do_route launches (one per token for the
-// small-batch router).
+// small-batch router, one per 128 tokens for the fused tensor-core router).
 int route_grid(const moe_config& c, const Layout& L) {
   if (!L.tc_router && c.T <= kSmallRouteMaxT) return c.T;
+  if (use_fused_tc_router(c)) return (c.T + 127) / 128;
   return L.nb;
+}
+
+template <int EPAD, int KMAX>
+moe_status launch_route_tc_inst(const CUtensorMap& mx, const CUtensorMap& mw, int grid,
+                                const RouteArgs& ra, cudaStream_t st) {
+  constexpr int STAGES = 8;
+  constexpr size_t smem = RouteTcSmem<EPAD, STAGES>::bytes();
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(k_route_tc<EPAD, KMAX, STAGES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  return launch_pdl(k_route_tc<EPAD, KMAX, STAGES>, dim3(grid), dim3(192), smem, st, mx, mw, ra);
+}
+
+template <int EPAD>
+moe_status launch_route_tc_k(int km, const CUtensorMap& mx, const CUtensorMap& mw, int grid,
+                             const RouteArgs& ra, cudaStream_t st) {
+  switch (km) {
+    case 2: return launch_route_tc_inst<EPAD, 2>(mx, mw, grid, ra, st);
+    case 4: return launch_route_tc_inst<EPAD, 4>(mx, mw, grid, ra, st);
+    case 8: return launch_route_tc_inst<EPAD, 8>(mx, mw, grid, ra, st);
+    default: return launch_route_tc_inst<EPAD, 16>(mx, mw, grid, ra, st);
+  }
 }
 
 // Router, gating, statistics and the dispatch ranking in one routing grid
@@ -477,6 +520,16 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
                         static_cast<const __nv_bfloat16*>(w_g), c.d_model, c.E, L.E_pad, wgT)) !=
         MOE_OK)
       return s;
+    if (use_fused_tc_router(c)) {
+      // one CTA per 128 tokens, the gating in the GEMM epilogue
+      CUtensorMap mx, mw;
+      if (!map_a(&mx, x, c.d_model, c.T) || !map_b(&mw, wgT, c.d_model, L.E_pad, 1, L.E_pad))
+        return MOE_ERR_CUDA;
+      const int grid = (c.T + 127) / 128;
+      if (L.E_pad == 16) return launch_route_tc_k<16>(km, mx, mw, grid, ra, st);
+      if (L.E_pad == 32) return launch_route_tc_k<32>(km, mx, mw, grid, ra, st);
+      return launch_route_tc_k<64>(km, mx, mw, grid, ra, st);
+    }
     // expert columns in tiles of at most 64: a wide router (E = 256) then
     // spreads over four times as many CTAs as row tiles
     const int bn_r = std::min(L.E_pad, 64);

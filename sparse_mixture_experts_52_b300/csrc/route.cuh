@@ -37,6 +37,7 @@ constexpr int kRouteWarps = 8;          // warps per routing block
 constexpr int kRouteThreads = kRouteWarps * 32;
 constexpr int kRouteMaxBlocks = 296;    // partial-sum rows (fixed: layout must not depend on the GPU)
 constexpr int kChunk = 32;              // tokens per ranking chunk (one warp's lanes)
+constexpr int kRouteMaxRows = 512;      // routing-grid blocks whose softmax partials the header holds
 
 __host__ __device__ inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
 // row stride of the per-chunk counts: a multiple of 32 chunks (128 bytes)
@@ -302,31 +303,20 @@ __device__ __forceinline__ void flush_stats(const LaneStats<NPL>& st, int E, flo
 }
 
 // ---------------------------------------------------------------- ranking
-// Ranks the assignments of chunk `g` (tokens 32g .. 32g+31, lane = token),
-// writes crank and the chunk's entries of hist, and adds its counts to the
-// totals.  `idx` is read from L2
-// (ld.cg): this grid may have just written it.  s_hist is this warp's
-// zeroed [E] counter row; it is zero again on return.
+// Ranks the assignments of chunk `g` (tokens 32g .. 32g+31, lane = token)
+// given each lane's experts e[j] (-1 for none: a token past T or an index
+// outside [0, E)); writes crank and the chunk's entries of hist, and adds its
+// counts to the totals.  s_hist is this warp's zeroed [E] counter row; it is
+// zero again on return.
 template <int KMAX>
-__device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t* idx, int g,
-                                           int* s_hist) {
+__device__ __forceinline__ void rank_chunk_experts(const DispatchArgs& a, const int (&e)[KMAX],
+                                                   int g, int* s_hist) {
   const int lane = threadIdx.x & 31;
   const int t = g * kChunk + lane;
   const bool valid_t = t < a.T;
-  int e[KMAX], r[KMAX];
+  int r[KMAX];
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    e[j] = -1;
-    r[j] = 0;
-    if (j < a.k && valid_t) {
-      const int v = __ldcg(idx + static_cast<int64_t>(t) * a.k + j);
-      if (v >= 0 && v < a.E) {
-        e[j] = v;
-      } else {
-        atomicOr(a.err, DEV_ERR_BAD_EXPERT_INDEX);
-      }
-    }
-  }
+  for (int j = 0; j < KMAX; ++j) r[j] = 0;
   // r[j] = number of tokens before this lane's in the chunk that chose e[j]
   for (int src = 0; src < kChunk - 1; ++src) {
 #pragma unroll
@@ -356,6 +346,30 @@ __device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t*
     s_hist[x] = 0;
   }
   __syncwarp();
+}
+
+// The same, reading the experts of the chunk's tokens from `idx` (from L2,
+// ld.cg: this grid may have just written it).  An index outside [0, E) sets
+// the status bit and counts as no expert.
+template <int KMAX>
+__device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t* idx, int g,
+                                           int* s_hist) {
+  const int lane = threadIdx.x & 31;
+  const int t = g * kChunk + lane;
+  int e[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    e[j] = -1;
+    if (j < a.k && t < a.T) {
+      const int v = __ldcg(idx + static_cast<int64_t>(t) * a.k + j);
+      if (v >= 0 && v < a.E) {
+        e[j] = v;
+      } else {
+        atomicOr(a.err, DEV_ERR_BAD_EXPERT_INDEX);
+      }
+    }
+  }
+  rank_chunk_experts<KMAX>(a, e, g, s_hist);
 }
 
 // Ranks chunks [g0, g1) (warp w takes chunks g0+w, g0+w+8, ...).
@@ -434,7 +448,7 @@ __device__ void dispatch_finalize(const DispatchArgs& a, int* s_cnt) {
 // P, f and aux (the routing grid's last block, or an extra block of the
 // combine kernel), fp32 throughout (the FP64 pipe
 // of this GPU is 64x slower) and in a fixed order.  Warp w reduces the rows
-// of partials of experts w, w+8, ...: lane l sums blocks l, l+32, ... in
+// of partials of experts w, w + nwarps, ...: lane l sums blocks l, l+32, ... in
 // ascending order, a fixed shuffle tree combines the lanes.  The loads of up
 // to 16 (expert, 32-block step) pairs per lane are in flight together, and
 // consecutive lanes read consecutive blocks (one 128-byte line per warp load).
@@ -445,13 +459,14 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
   __shared__ int s_am[kMaxExperts];
   const int E = a.E, nb = a.nb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {   // all arg-max totals at once
     s_am[e] = static_cast<int>(__ldcg(a.a_tot + e));
     a.a_tot[e] = 0u;
   }
   __syncthreads();
   const int steps = (nb + 31) / 32;
-  const int per_warp = (E + kRouteWarps - 1) / kRouteWarps;
+  const int per_warp = (E + nwarps - 1) / nwarps;
   const int pairs = per_warp * steps;   // expert-major: steps of one expert are consecutive
   float ps = 0.f;
   int cur = -1;
@@ -473,7 +488,7 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int p = p0 + i;
-      const int e = warp + kRouteWarps * (p / steps);
+      const int e = warp + nwarps * (p / steps);
       const int b = (p % steps) * 32 + lane;
       const bool ok = p < pairs && e < E && b < nb;
       float* src = a.p_part + static_cast<int64_t>(ok ? e : 0) * nb + (ok ? b : 0);
@@ -483,7 +498,7 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int p = p0 + i;
-      const int e = warp + kRouteWarps * (p / steps);
+      const int e = warp + nwarps * (p / steps);
       if (p < pairs && e < E) {          // warp-uniform
         if (e != cur) {
           if (cur >= 0) flush(cur);

@@ -185,10 +185,13 @@ def test_determinism_bitwise():
         assert np.array_equal(a[k], b[k]), k
 
 
-def test_exact_ties_lowest_index_and_capacity_in_token_order():
+@pytest.mark.parametrize("T", [512, 1024])
+def test_exact_ties_lowest_index_and_capacity_in_token_order(T):
     """W_g = 0: every logit is exactly 0 on both sides, so every token ties;
-    the lowest indices win and the capacity keeps the first tokens."""
-    cfg = synth.workload("switch_top1_cap", T=512, d_model=64, d_ff=64, E=8, k=2,
+    the lowest indices win and the capacity keeps the first tokens (T = 512
+    takes the block-per-token router, T = 1024 the tensor-core router with the
+    gating in its epilogue)."""
+    cfg = synth.workload("switch_top1_cap", T=T, d_model=64, d_ff=64, E=8, k=2,
                          capacity_factor=1.0, renorm=1, aux_f="topk_count")
     inp = synth.make_inputs(cfg, device=DEV)
     inp["w_g"].zero_()
@@ -196,11 +199,11 @@ def test_exact_ties_lowest_index_and_capacity_in_token_order():
     assert np.all(fw["topk_idx"] == np.array([0, 1]))
     assert np.all(fw["topk_w"] == 0.5)
     rep = compare.check_layer(cfg, inp, fw)
-    C = int(np.floor(1.0 * 512 / 8))
-    assert list(fw["counts"][:2]) == [512, 512]
+    C = int(np.floor(1.0 * T / 8))
+    assert list(fw["counts"][:2]) == [T, T]
     st = run_steps(cfg, inp)
     assert list(st["kept"]) == [C, C] + [0] * 6
-    sl = st["slot_of"].reshape(512, 2)
+    sl = st["slot_of"].reshape(T, 2)
     assert np.all(sl[:C] >= 0) and np.all(sl[C:] == -1)
     assert abs(float(fw["aux"][0]) - 2 * 0.01) < 1e-7     # aux = k * alpha (uniform P)
     print(rep.summary())
