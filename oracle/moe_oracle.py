@@ -23,7 +23,7 @@ Sources (page title, then section / listing / formula):
   alpha * E * sum(f * P)).
 * [SKILLS] "AI-Research-SKILLs MoE 训练实战…全指南": §3.1 ``MoELayer`` (softmax
   -> top-k -> renormalise), §4.3 ``load_balancing_loss`` (bincount of the
-  chosen indices) and the DeepSeek-V3 bias remark, §7.1 ``DeepSeekMoE``
+  chosen indices), ``router_z_loss`` and the DeepSeek-V3 bias remark, §7.1 ``DeepSeekMoE``
   (shared experts always computed and added with weight one), §8.2 the
   capacity formula ``int((tokens / num_experts) * capacity_factor)``.
 * [CH7]    "第7章 Mixture of Experts": §7.1 MoE(x) = sum_i G(x)_i * E_i(x);
@@ -285,6 +285,19 @@ def load_balance(cfg: OracleConfig, logits: np.ndarray, p: np.ndarray,
     return f, P, aux
 
 
+def router_z_loss(logits: np.ndarray) -> float:
+    """Router z-loss ([SKILLS] §4.3 ``router_z_loss``): the mean over tokens of
+    the squared log-sum-exp of the router logits, in float64 from the float32
+    logits (max-subtracted, so the value is the textbook
+    log(sum_e exp(l_e))^2 averaged over tokens)."""
+    l = np.asarray(logits, np.float64)
+    if l.shape[0] == 0:
+        return 0.0
+    m = l.max(axis=-1, keepdims=True)
+    lse = m[:, 0] + np.log(np.exp(l - m).sum(axis=-1))
+    return float(np.mean(lse * lse))
+
+
 # --------------------------------------------------------------------------
 # The whole layer.
 # --------------------------------------------------------------------------
@@ -331,6 +344,7 @@ def moe_forward(cfg: OracleConfig, x: np.ndarray, w_g: np.ndarray,
     C = capacity(cfg)
     disp = dispatch(g.idx, cfg.E, C)
     f, P, aux = load_balance(cfg, logits, g.p, disp.counts)
+    z = router_z_loss(logits)
 
     rows = np.arange(T) if rows is None else np.asarray(rows, np.int64)
     out = np.zeros((len(rows), cfg.d_model), np.float64)
@@ -354,4 +368,4 @@ def moe_forward(cfg: OracleConfig, x: np.ndarray, w_g: np.ndarray,
         out += expert_ffn(x64_rows, w1, b1, w2, b2)
 
     return ForwardResult(logits=logits, gate=g, disp=disp, C=C, f=f, P=P,
-                         aux=aux, rows=rows, out=out)
+                         aux=aux, rows=rows, out=out, extra={"z_loss": z})

@@ -446,6 +446,43 @@ def test_dropped_tokens_output_zero():
     check_dropped_tokens_output_zero()
 
 
+def check_router_z_loss():
+    """z-loss pins: uniform logits give log(E)^2 exactly; a hand-computed
+    two-token case; adding c to every logit of a token moves its log-sum-exp
+    by exactly c; the full-layer result carries the same value."""
+    for E in (1, 2, 8, 64):
+        z = om.router_z_loss(np.zeros((5, E), np.float32))
+        assert abs(z - math.log(E) ** 2) < 1e-12, (E, z)
+    # token 0: logits 0 and log 3 -> lse = log(1 + 3) = log 4 (log 3 as float32);
+    # token 1: two equal logits 1 -> lse = 1 + log 2
+    l = np.array([[0.0, math.log(3.0)], [1.0, 1.0]], np.float32)
+    lse0 = math.log(1.0 + math.exp(float(l[0, 1])))
+    assert abs(lse0 - math.log(4.0)) < 1e-6
+    want = (lse0 ** 2 + (1.0 + math.log(2.0)) ** 2) / 2.0
+    assert abs(om.router_z_loss(l) - want) < 1e-12, (om.router_z_loss(l), want)
+    rng = np.random.default_rng(5)
+    a = rng.standard_normal((7, 6)).astype(np.float32)
+    c = 2.5
+    la = om.router_z_loss(a)
+    lse = np.log(np.exp(a.astype(np.float64)).sum(-1))
+    assert abs(la - np.mean(lse ** 2)) < 1e-12
+    shifted = om.router_z_loss((a + np.float32(c)).astype(np.float32))
+    want_shift = np.mean((np.log(np.exp((a + np.float32(c)).astype(np.float64)).sum(-1))) ** 2)
+    assert abs(shifted - want_shift) < 1e-9
+    assert abs(shifted - np.mean((lse + c) ** 2)) < 1e-5
+    cfg = om.OracleConfig(T=7, d_model=4, d_ff=4, E=6, k=2)
+    x = rng.standard_normal((7, 4))
+    w_g = rng.standard_normal((4, 6)) * 0.5
+    ex = {e: (rng.standard_normal((4, 4)), None, rng.standard_normal((4, 4)), None)
+          for e in range(6)}
+    r = om.moe_forward(cfg, x, w_g, lambda e: ex[e])
+    assert abs(r.extra["z_loss"] - om.router_z_loss(r.logits)) == 0.0
+
+
+def test_router_z_loss():
+    check_router_z_loss()
+
+
 # ---------------------------------------------------------------- planted mistakes
 ALL_CHECKS = [check_golden_pages_values, check_selection_bruteforce, check_hand_gate_examples,
               check_softmax_topk_equals_topk_softmax, check_weights_sum_to_one,
@@ -453,7 +490,7 @@ ALL_CHECKS = [check_golden_pages_values, check_selection_bruteforce, check_hand_
               check_dense_reductions, check_aux_uniform_router, check_aux_hand_example,
               check_aux_nonnegative_and_argmax, check_capacity_hand_example,
               check_dispatch_invariants, check_forward_bruteforce,
-              check_dropped_tokens_output_zero]
+              check_dropped_tokens_output_zero, check_router_z_loss]
 
 
 def _some_pin_fails():
@@ -500,11 +537,24 @@ def _capacity_ceil(cfg):
 _orig_load_balance = om.load_balance
 
 
+def _z_without_square(logits):
+    l = np.asarray(logits, np.float64)
+    m = l.max(axis=-1, keepdims=True)
+    return float(np.mean(m[:, 0] + np.log(np.exp(l - m).sum(axis=-1))))
+
+
+def _z_without_max(logits):
+    l = np.asarray(logits, np.float64)
+    return float(np.mean(np.log(np.exp(l - l.max(axis=-1, keepdims=True)).sum(-1)) ** 2))
+
+
 @pytest.mark.parametrize("name,patch", [
     ("tanh GELU", ("gelu", _tanh_gelu)),
     ("untransposed W2", ("expert_ffn", _ffn_transposed)),
     ("highest index wins ties", ("select_topk", _select_highest_index_on_ties)),
     ("ceil capacity", ("capacity", _capacity_ceil)),
+    ("z-loss not squared", ("router_z_loss", _z_without_square)),
+    ("z-loss without the max term", ("router_z_loss", _z_without_max)),
     ("aux without the E factor", ("load_balance",
                                   lambda c, l, p, n: (lambda r: (r[0], r[1], r[2] / c.E))(
                                       _orig_load_balance(c, l, p, n)))),
