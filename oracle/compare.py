@@ -35,6 +35,10 @@ TOL_F32_REL_L2 = 1e-4
 TOL_P_REL = 1e-5
 TOL_AUX_REL = 1e-5
 TOL_W_ABS = 1e-5
+# router z-loss: each token's log-sum-exp is 1-Lipschitz in the logits, which
+# agree to about 1e-6 relative (fp32 dot products); squaring doubles that and
+# the fp32 mean over T tokens in blocked order adds a few 1e-7 more.
+TOL_Z_REL = 1e-4
 
 
 def oracle_config(cfg: dict) -> om.OracleConfig:
@@ -47,7 +51,7 @@ def oracle_config(cfg: dict) -> om.OracleConfig:
         min_capacity=int(cfg.get("min_capacity", 0)), route=cfg["route"],
         renorm=bool(cfg.get("renorm", 1)),
         aux_alpha=float(np.float32(cfg.get("aux_alpha", 0.01))),
-        aux_f=cfg.get("aux_f", om.AUX_TOPK_COUNT))
+        aux_f=cfg.get("aux_f", om.AUX_TOPK_COUNT), act=cfg.get("act", om.ACT_GELU))
 
 
 def np64(t) -> Optional[np.ndarray]:
@@ -117,7 +121,7 @@ def _near_tie_and_override(ref: om.ForwardResult, gpu_idx: np.ndarray):
 
 
 def compare_routing(cfg: dict, ref: om.ForwardResult, gpu: dict, rep: Report) -> None:
-    """idx / w / counts / f / P / aux (the dict holds numpy arrays)."""
+    """idx / w / counts / f / P / aux / z_loss (the dict holds numpy arrays)."""
     idx = np.asarray(gpu["topk_idx"]).astype(np.int64)
     T = idx.shape[0]
     ok = np.ones(T, bool)
@@ -153,6 +157,10 @@ def compare_routing(cfg: dict, ref: om.ForwardResult, gpu: dict, rep: Report) ->
             slack = cfg["aux_alpha"] * cfg["E"] * len(rep.near_tie) / T
         assert abs(a - ref.aux) <= TOL_AUX_REL * abs(ref.aux) + slack + 1e-12, \
             f"aux {a} vs {ref.aux}"
+    if gpu.get("z_loss") is not None and "z_loss" in ref.extra:
+        z = float(np.asarray(gpu["z_loss"]).reshape(-1)[0])
+        zr = float(ref.extra["z_loss"])
+        assert abs(z - zr) <= TOL_Z_REL * abs(zr) + 1e-12, f"z_loss {z} vs {zr}"
 
 
 def compare_dispatch(ref: om.ForwardResult, gpu: dict) -> None:

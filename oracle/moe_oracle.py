@@ -26,6 +26,8 @@ Sources (page title, then section / listing / formula):
   chosen indices), ``router_z_loss`` and the DeepSeek-V3 bias remark, §7.1 ``DeepSeekMoE``
   (shared experts always computed and added with weight one), §8.2 the
   capacity formula ``int((tokens / num_experts) * capacity_factor)``.
+  §6.1 ``MixtralMoEBlock`` (experts Linear -> SiLU -> Linear without bias,
+  and the text naming SwiGLU as Mixtral's FFN activation).
 * [CH7]    "第7章 Mixture of Experts": §7.1 MoE(x) = sum_i G(x)_i * E_i(x);
   §7.2 ``top_k_gating`` (top-k on logits, softmax over the k); §7.3 shared +
   fine-grained experts; §7.4 the balance loss N * sum f_i p_i and capacity
@@ -43,13 +45,16 @@ from dataclasses import dataclass, field
 from typing import Callable, Optional, Sequence
 
 import numpy as np
-from scipy.special import erf
+from scipy.special import erf, expit
 
 ROUTE_SOFTMAX_TOPK = "softmax_topk"      # [BAIDU] SparseMoEGate, [SKILLS] §3.1
 ROUTE_TOPK_SOFTMAX = "topk_softmax"      # [BEE] steps 2-3, [CH7] §7.2 top_k_gating
 ROUTE_BIASED_SOFTMAX = "biased_softmax"  # [SKILLS] §4.3 / §7.1 DeepSeek-V3 bias
 AUX_TOPK_COUNT = "topk_count"            # [BAIDU] one-hot of the top-k, summed
 AUX_ARGMAX = "argmax"                    # [BEE] load_balance_loss, argmax routing
+ACT_GELU = "gelu"                        # [BAIDU] §五, [SKILLS] §3.1 nn.GELU()
+ACT_SILU = "silu"                        # [SKILLS] §6.1 MixtralMoEBlock nn.SiLU()
+ACT_SWIGLU = "swiglu"                    # [SKILLS] §6.1 "SwiGLU" (R18)
 
 
 @dataclass
@@ -70,6 +75,7 @@ class OracleConfig:
     renorm: bool = True
     aux_alpha: float = 0.01
     aux_f: str = AUX_TOPK_COUNT
+    act: str = ACT_GELU
 
 
 # --------------------------------------------------------------------------
@@ -244,14 +250,32 @@ def gelu(v: np.ndarray) -> np.ndarray:
     return 0.5 * v * (1.0 + erf(v / math.sqrt(2.0)))
 
 
+def silu(v: np.ndarray) -> np.ndarray:
+    """nn.SiLU(): v * sigmoid(v), the sigmoid being the logistic function."""
+    v = np.asarray(v, np.float64)
+    return v * expit(v)
+
+
 def expert_ffn(xe: np.ndarray, w1: np.ndarray, b1: Optional[np.ndarray],
-               w2: np.ndarray, b2: Optional[np.ndarray]) -> np.ndarray:
-    """y = GELU(x W1^T + b1) W2^T + b2 with nn.Linear weights W1 [d_ff, d],
-    W2 [d, d_ff], in float64."""
+               w2: np.ndarray, b2: Optional[np.ndarray], act: str = ACT_GELU) -> np.ndarray:
+    """y = act(x W1^T + b1) W2^T + b2 with nn.Linear weights W1 [d_ff, d],
+    W2 [d, d_ff], in float64; act is GELU or SiLU.
+
+    SwiGLU (R18): W1 is [2 d_ff, d], the gate projection's rows first and the
+    up projection's after them (b1 likewise [2 d_ff]); with h = x W1^T + b1
+    split into those two halves, y = (SiLU(h_gate) * h_up) W2^T + b2."""
     h = np.asarray(xe, np.float64) @ np.asarray(w1, np.float64).T
     if b1 is not None:
         h = h + np.asarray(b1, np.float64)
-    h = gelu(h)
+    if act == ACT_GELU:
+        h = gelu(h)
+    elif act == ACT_SILU:
+        h = silu(h)
+    elif act == ACT_SWIGLU:
+        F = h.shape[1] // 2
+        h = silu(h[:, :F]) * h[:, F:]
+    else:
+        raise ValueError(f"unknown activation {act!r}")
     y = h @ np.asarray(w2, np.float64).T
     if b2 is not None:
         y = y + np.asarray(b2, np.float64)
@@ -359,13 +383,13 @@ def moe_forward(cfg: OracleConfig, x: np.ndarray, w_g: np.ndarray,
         if ii.size == 0:
             continue
         w1, b1, w2, b2 = experts(e)
-        y = expert_ffn(x64_rows[ii], w1, b1, w2, b2)
+        y = expert_ffn(x64_rows[ii], w1, b1, w2, b2, act=cfg.act)
         wt = g.w[rows[ii], jj][:, None]
         np.add.at(out, ii, wt * y)          # index_add_ of the weighted outputs
 
     for s in range(cfg.n_shared):
         w1, b1, w2, b2 = shared(s)
-        out += expert_ffn(x64_rows, w1, b1, w2, b2)
+        out += expert_ffn(x64_rows, w1, b1, w2, b2, act=cfg.act)
 
     return ForwardResult(logits=logits, gate=g, disp=disp, C=C, f=f, P=P,
                          aux=aux, rows=rows, out=out, extra={"z_loss": z})

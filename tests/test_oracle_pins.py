@@ -227,6 +227,74 @@ def test_gelu_closed_form():
     check_gelu_closed_form()
 
 
+def check_silu_closed_form():
+    """SiLU(v) = v * sigmoid(v): sigmoid(log 3) = 3/4 exactly, so SiLU(log 3)
+    = 0.75 log 3; SiLU(0) = 0; SiLU(v) - SiLU(-v) = v for every v (sigmoid(v)
+    + sigmoid(-v) = 1); SiLU(40) = 40 to double precision, SiLU(-40) ~ -40 e^-40."""
+    v = om.silu(np.array([LN3, 0.0, 40.0, -40.0]))
+    assert abs(v[0] - 0.75 * LN3) < 1e-15
+    assert v[1] == 0.0
+    assert abs(v[2] - 40.0) < 1e-12
+    assert abs(v[3] + 40.0 * math.exp(-40.0)) < 1e-25
+    r = np.random.default_rng(11).standard_normal(50) * 4
+    np.testing.assert_allclose(om.silu(r) - om.silu(-r), r, rtol=0, atol=1e-14)
+
+
+def test_silu_closed_form():
+    check_silu_closed_form()
+
+
+def check_glu_experts(seed=12):
+    """Hand values of the SiLU and SwiGLU experts, and the special case of
+    SwiGLU that reduces to the SiLU expert.
+    d = d_ff = 1, x = 1: a SiLU expert with W1 = log 3, W2 = 1 gives 0.75 log 3;
+    a SwiGLU expert with gate row log 3, up row 2 gives SiLU(log 3) * 2
+    = 1.5 log 3 (the halves the other way round would give 2 sigmoid(2) log 3).
+    With the up rows zero and the up bias one, SwiGLU equals the SiLU expert of
+    the gate rows."""
+    one = np.ones((1, 1))
+    y = om.expert_ffn(one, np.array([[LN3]]), None, one, None, act=om.ACT_SILU)
+    assert abs(y[0, 0] - 0.75 * LN3) < 1e-15
+    y = om.expert_ffn(one, np.array([[LN3], [2.0]]), None, one, None, act=om.ACT_SWIGLU)
+    assert abs(y[0, 0] - 1.5 * LN3) < 1e-15, y
+    rng = np.random.default_rng(seed)
+    T, d, F = 9, 5, 7
+    x = rng.standard_normal((T, d))
+    wg_rows, bg = rng.standard_normal((F, d)), rng.standard_normal(F)
+    w2, b2 = rng.standard_normal((d, F)), rng.standard_normal(d)
+    w1 = np.concatenate([wg_rows, np.zeros((F, d))])
+    b1 = np.concatenate([bg, np.ones(F)])
+    np.testing.assert_allclose(om.expert_ffn(x, w1, b1, w2, b2, act=om.ACT_SWIGLU),
+                               om.expert_ffn(x, wg_rows, bg, w2, b2, act=om.ACT_SILU),
+                               rtol=1e-14, atol=1e-14)
+    # through torch's own SiLU for the plain SiLU expert
+    t = lambda a: torch.as_tensor(a, dtype=torch.float64)
+    want = torch.nn.functional.linear(
+        torch.nn.functional.silu(torch.nn.functional.linear(t(x), t(wg_rows), t(bg))),
+        t(w2), t(b2)).numpy()
+    np.testing.assert_allclose(om.expert_ffn(x, wg_rows, bg, w2, b2, act=om.ACT_SILU), want,
+                               rtol=1e-13, atol=1e-13)
+    # the layer applies the configured activation to routed and shared experts
+    E = 3
+    w1s = [rng.standard_normal((2 * F, d)) for _ in range(E)]
+    ex = {e: (w1s[e], None, w2, None) for e in range(E)}
+    cfg = om.OracleConfig(T=T, d_model=d, d_ff=F, E=E, k=1, n_shared=1, act=om.ACT_SWIGLU)
+    r = om.moe_forward(cfg, x, rng.standard_normal((d, E)), lambda e: ex[e],
+                       shared=lambda s: ex[0])
+    for t_ in range(T):
+        e = int(r.gate.idx[t_, 0])
+        h1 = x[t_] @ w1s[e].T
+        h0 = x[t_] @ w1s[0].T
+        routed = (h1[:F] / (1 + np.exp(-h1[:F])) * h1[F:]) @ w2.T
+        shared = (h0[:F] / (1 + np.exp(-h0[:F])) * h0[F:]) @ w2.T
+        np.testing.assert_allclose(r.out[t_], r.gate.w[t_, 0] * routed + shared,
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_glu_experts():
+    check_glu_experts()
+
+
 def check_dense_reductions(seed=4):
     rng = np.random.default_rng(seed)
     T, d, F = 10, 6, 10
@@ -490,7 +558,8 @@ ALL_CHECKS = [check_golden_pages_values, check_selection_bruteforce, check_hand_
               check_dense_reductions, check_aux_uniform_router, check_aux_hand_example,
               check_aux_nonnegative_and_argmax, check_capacity_hand_example,
               check_dispatch_invariants, check_forward_bruteforce,
-              check_dropped_tokens_output_zero, check_router_z_loss]
+              check_dropped_tokens_output_zero, check_router_z_loss, check_silu_closed_form,
+              check_glu_experts]
 
 
 def _some_pin_fails():
@@ -512,7 +581,7 @@ def _tanh_gelu(v):
     return 0.5 * v * (1 + np.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
 
 
-def _ffn_transposed(xe, w1, b1, w2, b2):
+def _ffn_transposed(xe, w1, b1, w2, b2, act=om.ACT_GELU):
     # plausible slip: second layer multiplied without the transpose of W2 when
     # d == d_ff would go unnoticed; with d != d_ff this must raise or differ
     h = om.gelu(np.asarray(xe) @ np.asarray(w1).T + (0 if b1 is None else b1))
@@ -535,6 +604,20 @@ def _capacity_ceil(cfg):
 
 
 _orig_load_balance = om.load_balance
+_orig_expert_ffn = om.expert_ffn
+
+
+def _silu_as_sigmoid(v):
+    return 1.0 / (1.0 + np.exp(-np.asarray(v, np.float64)))
+
+
+def _swiglu_halves_swapped(xe, w1, b1, w2, b2, act=om.ACT_GELU):
+    if act == om.ACT_SWIGLU:
+        F = np.asarray(w1).shape[0] // 2
+        w1 = np.concatenate([np.asarray(w1)[F:], np.asarray(w1)[:F]])
+        if b1 is not None:
+            b1 = np.concatenate([np.asarray(b1)[F:], np.asarray(b1)[:F]])
+    return _orig_expert_ffn(xe, w1, b1, w2, b2, act=act)
 
 
 def _z_without_square(logits):
@@ -554,6 +637,8 @@ def _z_without_max(logits):
     ("highest index wins ties", ("select_topk", _select_highest_index_on_ties)),
     ("ceil capacity", ("capacity", _capacity_ceil)),
     ("z-loss not squared", ("router_z_loss", _z_without_square)),
+    ("SiLU as the plain sigmoid", ("silu", _silu_as_sigmoid)),
+    ("SwiGLU gate and up halves swapped", ("expert_ffn", _swiglu_halves_swapped)),
     ("z-loss without the max term", ("router_z_loss", _z_without_max)),
     ("aux without the E factor", ("load_balance",
                                   lambda c, l, p, n: (lambda r: (r[0], r[1], r[2] / c.E))(
