@@ -13,6 +13,7 @@
  *   y      = sum_kept w[t,j] * FFN_{idx[t,j]}(x_t) + sum_s FFN_s(x_t)
  *   FFN(v) = GELU_erf(v W1^T + b1) W2^T + b2
  *   f_i, P_i, aux = alpha * E * sum_i f_i P_i          (Switch load balance)
+ *   z      = mean_t logsumexp_e(logits[t, e])^2        (router z-loss)
  *
  * Sources: "混合专家大模型MoE架构选型与部署实践教程" §五 (SparseMoEGate,
  * SimpleMoELayer); "[BEE-30064] 混合專家架構與服務", 專家路由工作原理 (routing
@@ -109,12 +110,14 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream stream);
  *   logits); select_bias [E] fp32 or NULL (MOE_ROUTE_BIASED_SOFTMAX only).
  *   Outputs: logits [T,E] fp32 or NULL; topk_idx [T,k] int32 (descending
  *   selection score, lower expert index first on equal scores); topk_w [T,k]
- *   fp32; f [E], P [E] fp32; aux [1] fp32.  f and P count all T tokens
- *   before any capacity drop. */
+ *   fp32; f [E], P [E] fp32; aux [1] fp32; z_loss [1] fp32 or NULL (the
+ *   router z-loss of "AI-Research-SKILLs MoE 训练实战…全指南" §4.3: the mean over
+ *   tokens of the squared log-sum-exp of the logits, logit_bias included).  f,
+ *   P and z_loss count all T tokens before any capacity drop. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
                      const float* logit_bias, const float* select_bias,
                      float* logits, int32_t* topk_idx, float* topk_w,
-                     float* f, float* P, float* aux,
+                     float* f, float* P, float* aux, float* z_loss,
                      void* ws, size_t ws_bytes, moe_stream stream);
 
 /* Dispatch: histogram, exclusive scan, capacity cut and row gather.
@@ -193,14 +196,14 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
  * dropped token), which skips the rounding of the expert output that the
  * step-by-step entry points do.
  *   Outputs: out [T,d] dtype; topk_idx [T,k]; topk_w [T,k]; counts [E];
- *   f [E]; P [E]; aux [1].  Any of topk_idx .. aux may be NULL except
- *   out. */
+ *   f [E]; P [E]; aux [1]; z_loss [1] (as in moe_route).  Any of topk_idx ..
+ *   z_loss may be NULL; out may not. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
                        const float* logit_bias, const float* select_bias,
                        const void* w1, const void* b1, const void* w2, const void* b2,
                        const void* ws1, const void* wsb1, const void* ws2, const void* wsb2,
                        void* out, int32_t* topk_idx, float* topk_w, int32_t* counts,
-                       float* f, float* P, float* aux,
+                       float* f, float* P, float* aux, float* z_loss,
                        void* ws, size_t ws_bytes, moe_stream stream);
 
 /* Synchronises `stream`, reads and clears the device status word of `ws`.

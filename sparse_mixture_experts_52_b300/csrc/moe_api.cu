@@ -35,7 +35,7 @@ constexpr size_t kRankCounterOffset = 20;
 constexpr size_t kTotalsOffset = 1024;    // int32 [E <= 256]
 constexpr size_t kArgmaxOffset = 2048;    // uint32 [E <= 256]
 constexpr size_t kFlagsOffset = 4096;     // int32 [kMaxGemmCtas][4] stream-K flags
-constexpr size_t kPartOffset = 65536;     // fp32 [E <= 256, blocks <= 512]
+constexpr size_t kPartOffset = 65536;     // fp32 [E + 1 <= 257, blocks <= 512]
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -106,7 +106,7 @@ Layout make_layout(const moe_config& c) {
     return at;
   };
   L.status = take(kHeaderBytes);
-  static_assert(kPartOffset + size_t(kMaxExperts) * (kRouteMaxBlocks > kSmallRouteMaxT
+  static_assert(kPartOffset + size_t(kMaxExperts + 1) * (kRouteMaxBlocks > kSmallRouteMaxT
                                                          ? kRouteMaxBlocks
                                                          : kSmallRouteMaxT) * 4 <=
                     kHeaderBytes,
@@ -350,6 +350,7 @@ struct RouteOut {
   int32_t* kept;
   int32_t* offsets;
   int defer_stats;
+  float* z;
 };
 
 int kmax_of(int k) { return k <= 2 ? 2 : (k <= 4 ? 4 : (k <= 8 ? 8 : 16)); }
@@ -440,7 +441,7 @@ moe_status launch_route_small_e(const moe_config& c, cudaStream_t st, const Rout
 bool use_fused_tc_router(const moe_config& c) {
   const int64_t ctas = (static_cast<int64_t>(c.T) + 127) / 128;
   return use_tc_router(c) && c.E <= 16 &&
-         ctas * c.E <= static_cast<int64_t>(kMaxExperts) * kRouteMaxRows;
+         ctas * (c.E + 1) <= static_cast<int64_t>(kMaxExperts + 1) * kRouteMaxRows;
 }
 
 // Blocks of the routing grid do_route launches (one per token for the
@@ -505,6 +506,7 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
   ra.P = o.P;
   ra.aux = o.aux;
   ra.defer_stats = o.defer_stats;
+  ra.z = o.z;
   ra.dp = dispatch_args(c, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist),
                         at<int32_t>(ws, L.status + kTotalsOffset), o.counts, o.kept, o.offsets,
                         at<unsigned int>(ws, L.status + kRouteCounterOffset),
@@ -828,8 +830,8 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream stream) {
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
                      const float* logit_bias, const float* select_bias, float* logits,
-                     int32_t* topk_idx, float* topk_w, float* f, float* P, float* aux, void* ws,
-                     size_t ws_bytes, moe_stream stream) {
+                     int32_t* topk_idx, float* topk_w, float* f, float* P, float* aux,
+                     float* z_loss, void* ws, size_t ws_bytes, moe_stream stream) {
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
@@ -837,11 +839,14 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
   if ((s = check_ws(c, ws, ws_bytes, L)) != MOE_OK) return s;
   if (!f || !P || !aux) return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);
-  if (c.T == 0) return zero_stats(c, nullptr, f, P, aux, nullptr, nullptr, st);
+  if (c.T == 0) {
+    if (z_loss && cudaMemsetAsync(z_loss, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return zero_stats(c, nullptr, f, P, aux, nullptr, nullptr, st);
+  }
   if (!x || !w_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   return do_route(c, L, ws, x, w_g, logit_bias, select_bias,
                   RouteOut{logits, topk_idx, topk_w, f, P, aux, at<int32_t>(ws, L.counts),
-                           at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets), 0},
+                           at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets), 0, z_loss},
                   st);
 }
 
@@ -925,7 +930,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
                        const void* b1, const void* w2, const void* b2, const void* ws1,
                        const void* wsb1, const void* ws2, const void* wsb2, void* out,
                        int32_t* topk_idx, float* topk_w, int32_t* counts, float* f, float* P,
-                       float* aux, void* ws, size_t ws_bytes, moe_stream stream) {
+                       float* aux, float* z_loss, void* ws, size_t ws_bytes, moe_stream stream) {
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
@@ -939,7 +944,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   float* fo = f ? f : at<float>(ws, L.f);
   float* Po = P ? P : at<float>(ws, L.P);
   float* ao = aux ? aux : at<float>(ws, L.aux);
-  if (c.T == 0) return zero_stats(c, counts, f, P, aux, nullptr, nullptr, st);
+  if (c.T == 0) {
+    if (z_loss && cudaMemsetAsync(z_loss, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return zero_stats(c, counts, f, P, aux, nullptr, nullptr, st);
+  }
   if (!x || !w_g || !w1 || !w2) return MOE_ERR_INVALID_ARG;
   if (c.has_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && (!ws1 || !ws2)) return MOE_ERR_INVALID_ARG;
@@ -952,7 +960,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   void* x_perm = at<uint8_t>(ws, L.x_perm);
   // the routing grid also ranks the assignments: the permute follows directly
   if ((s = do_route(c, L, ws, x, w_g, logit_bias, select_bias,
-                    RouteOut{nullptr, idx, w, fo, Po, ao, cnt, kept, offsets, 1}, st)) != MOE_OK)
+                    RouteOut{nullptr, idx, w, fo, Po, ao, cnt, kept, offsets, 1, z_loss}, st)) !=
+      MOE_OK)
     return s;
   // the permute kernel's extra block reduces the routing statistics
   StatsArgs sa{};
@@ -967,6 +976,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   sa.f = fo;
   sa.P = Po;
   sa.aux = ao;
+  sa.z = z_loss;
   // top-1 bf16 layers without shared experts: the combine is fused into the
   // down-projection (and the permute writes the zero rows of dropped tokens)
   const bool fused_combine = c.dtype == MOE_BF16 && c.k == 1 && c.n_shared == 0;

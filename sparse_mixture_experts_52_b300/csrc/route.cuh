@@ -75,13 +75,15 @@ struct RouteArgs {
   float* logits_out;          // [T, E] or null
   int32_t* idx;               // [T, k]
   float* w;                   // [T, k]
-  float* p_part;              // [E, nb] per-block sums of the softmax (expert-major; zero between calls)
+  float* p_part;              // [E + 1, nb] per-block sums of the softmax (expert-major), row E:
+                              // sums of logsumexp^2 (router z-loss); zero between calls
   unsigned int* a_tot;        // [E] arg-max counts (zero between calls)
   int aux_f;
   float alpha;
   float* f;                   // [E]
   float* P;                   // [E]
   float* aux;                 // [1]
+  float* z;                   // [1] router z-loss, or null
   DispatchArgs dp;
   int defer_stats;            // 1: the combine kernel reduces the statistics instead
 };
@@ -89,7 +91,7 @@ struct RouteArgs {
 // The statistics reduction: P, f and aux from the routing grid's per-block
 // softmax partials (p_part, nb blocks), arg-max totals and counts.
 struct StatsArgs {
-  float* p_part;              // [E, nb]; cleared after reading
+  float* p_part;              // [E + 1, nb]; cleared after reading
   int nb;
   unsigned int* a_tot;        // [E]; cleared after reading
   const int32_t* counts;      // [E] (read when s_cnt is not given)
@@ -98,6 +100,7 @@ struct StatsArgs {
   float* f;
   float* P;
   float* aux;
+  float* z;                   // router z-loss, or null
 };
 
 __host__ __device__ inline StatsArgs stats_args(const RouteArgs& a, int nb) {
@@ -113,6 +116,7 @@ __host__ __device__ inline StatsArgs stats_args(const RouteArgs& a, int nb) {
   st.f = a.f;
   st.P = a.P;
   st.aux = a.aux;
+  st.z = a.z;
   return st;
 }
 
@@ -144,12 +148,14 @@ template <int NPL>
 struct LaneStats {
   float p[NPL];
   int amax[NPL];
+  float z;   // lane 0: sum over the warp's tokens of logsumexp(logits)^2
   __device__ void zero() {
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       p[i] = 0.f;
       amax[i] = 0;
     }
+    z = 0.f;
   }
 };
 
@@ -183,6 +189,10 @@ __device__ __forceinline__ void gate_token(const float (&l)[NPL], const float (&
   s = warp_sum(s);
 #pragma unroll
   for (int i = 0; i < NPL; ++i) p[i] = p[i] / s;
+  if (lane == 0) {   // router z-loss term: logsumexp of the logits, squared
+    const float lse = m + logf(s);
+    st.z += lse * lse;
+  }
 
   // arg-max of the logits (Switch f_i)
   {
@@ -281,13 +291,20 @@ __device__ __forceinline__ void flush_stats(const LaneStats<NPL>& st, int E, flo
                                             unsigned int* a_tot) {
   __shared__ float s_p[kRouteWarps][32 * NPL];
   __shared__ int s_a[kRouteWarps][32 * NPL];
+  __shared__ float s_z[kRouteWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     s_p[warp][lane + 32 * i] = st.p[i];
     s_a[warp][lane + 32 * i] = st.amax[i];
   }
+  if (lane == 0) s_z[warp] = st.z;
   __syncthreads();
+  if (threadIdx.x == 0) {   // z-loss row of the partials, warps in order
+    float zs = 0.f;
+    for (int w = 0; w < kRouteWarps; ++w) zs += s_z[w];
+    if (zs != 0.f) atomicAdd(p_part + static_cast<int64_t>(E) * gridDim.x + blockIdx.x, zs);
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float ps = 0.f;
     int as = 0;
@@ -466,7 +483,8 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
   }
   __syncthreads();
   const int steps = (nb + 31) / 32;
-  const int per_warp = (E + nwarps - 1) / nwarps;
+  const int R = E + 1;   // the experts' rows, then the z-loss row
+  const int per_warp = (R + nwarps - 1) / nwarps;
   const int pairs = per_warp * steps;   // expert-major: steps of one expert are consecutive
   float ps = 0.f;
   int cur = -1;
@@ -474,6 +492,10 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
     float p = ps;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+    if (e == E) {
+      if (lane == 0 && a.z) *a.z = p / static_cast<float>(a.T);
+      return;
+    }
     if (lane == 0) {
       const float Pe = p / static_cast<float>(a.T);
       const int cnt = (a.aux_f == AUXF_ARGMAX) ? s_am[e] : (s_cnt ? s_cnt[e] : __ldg(a.counts + e));
@@ -490,7 +512,7 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
       const int p = p0 + i;
       const int e = warp + nwarps * (p / steps);
       const int b = (p % steps) * 32 + lane;
-      const bool ok = p < pairs && e < E && b < nb;
+      const bool ok = p < pairs && e < R && b < nb;
       float* src = a.p_part + static_cast<int64_t>(ok ? e : 0) * nb + (ok ? b : 0);
       pv[i] = ok ? __ldcg(src) : 0.f;
       if (ok) *src = 0.f;   // zero for the next call
@@ -499,7 +521,7 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
     for (int i = 0; i < kBatch; ++i) {
       const int p = p0 + i;
       const int e = warp + nwarps * (p / steps);
-      if (p < pairs && e < E) {          // warp-uniform
+      if (p < pairs && e < R) {          // warp-uniform
         if (e != cur) {
           if (cur >= 0) flush(cur);
           cur = e;

@@ -42,6 +42,7 @@ struct RouteTcSmem {
     float lb[EPAD];
     float sb[EPAD];
     int amax[EPAD];
+    float zq[4];
     int hist[4][kMaxExperts];
   };
   static constexpr size_t bytes() { return 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl); }
@@ -49,11 +50,12 @@ struct RouteTcSmem {
 
 // Gates one token in registers.  l[e] holds the logits (+ logit bias) of
 // experts e < E.  Writes the softmax into prow (shared, E entries), and returns
-// the arg-max of the logits, the chosen experts and their weights.
+// the arg-max of the logits, the chosen experts, their weights and the
+// log-sum-exp of the logits.
 template <int EPAD, int KMAX>
 __device__ __forceinline__ void gate_thread(float (&l)[EPAD], int E, int k, int route, int renorm,
                                             const float* sb, float* prow, int& amax,
-                                            int (&sel)[KMAX], float (&wsel)[KMAX]) {
+                                            int (&sel)[KMAX], float (&wsel)[KMAX], float& lse) {
   const float NEG_INF = -__int_as_float(0x7f800000);
   float m = NEG_INF;
   amax = 0;
@@ -78,6 +80,7 @@ __device__ __forceinline__ void gate_thread(float (&l)[EPAD], int E, int k, int 
     p[e] = (e < E) ? expf(l[e] - m) : 0.f;
     s += p[e];
   }
+  lse = m + logf(s);
   const float inv_s = 1.0f / s;
 #pragma unroll
   for (int e = 0; e < EPAD; ++e) {
@@ -183,6 +186,7 @@ k_route_tc(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUten
     c.sb[e] = (a.select_bias && e < E) ? a.select_bias[e] : 0.f;
     c.amax[e] = 0;
   }
+  if (threadIdx.x < 4) c.zq[threadIdx.x] = 0.f;
   for (int i = threadIdx.x; i < 4 * kMaxExperts; i += blockDim.x) (&c.hist[0][0])[i] = 0;
   tc_fence_before();
   __syncthreads();
@@ -288,8 +292,14 @@ k_route_tc(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUten
       int amax;
       int sel[KMAX];
       float wsel[KMAX];
+      float lse;
       float* prow = sP + row * L::P_LD;
-      gate_thread<EPAD, KMAX>(l, E, a.k, a.route, a.renorm, c.sb, prow, amax, sel, wsel);
+      gate_thread<EPAD, KMAX>(l, E, a.k, a.route, a.renorm, c.sb, prow, amax, sel, wsel, lse);
+      // z-loss term of this warp's tokens, a fixed shuffle tree
+      float zz = valid ? lse * lse : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+      if (lane == 0) c.zq[q] = zz;
       if (!valid) {
 #pragma unroll
         for (int e = 0; e < EPAD; ++e)
@@ -324,6 +334,10 @@ k_route_tc(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUten
     if (ok && ecol < E && part == 0) {
       if (ps != 0.f) atomicAdd(a.p_part + static_cast<int64_t>(ecol) * gridDim.x + blockIdx.x, ps);
       if (c.amax[ecol]) atomicAdd(a.a_tot + ecol, static_cast<unsigned int>(c.amax[ecol]));
+    }
+    if (ok && eth == 0) {   // z-loss row: the four warps in order
+      const float zs = ((c.zq[0] + c.zq[1]) + c.zq[2]) + c.zq[3];
+      if (zs != 0.f) atomicAdd(a.p_part + static_cast<int64_t>(E) * gridDim.x + blockIdx.x, zs);
     }
   }
 

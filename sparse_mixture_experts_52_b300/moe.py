@@ -68,14 +68,14 @@ _CFG = ctypes.POINTER(Config)
 _SIGNATURES = {
     "moe_workspace_size": [_CFG, ctypes.POINTER(ctypes.c_size_t)],
     "moe_workspace_init": [_P, ctypes.c_size_t, _P],
-    "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_permute": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_permute_noalloc": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_grouped_ffn": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                         ctypes.c_size_t, _P],
     "moe_combine": [_CFG, _P, _P, _P, _P, _P, _P],
     "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                    _P, _P, _P, _P, ctypes.c_size_t, _P],
+                    _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_check_status": [_P, _P],
 }
 
@@ -152,7 +152,7 @@ def check_status(ws: torch.Tensor, stream=None) -> None:
 
 # ------------------------------------------------------------------ steps
 def route(cfg, x, w_g, topk_idx, topk_w, f, P, aux, ws, logit_bias=None, select_bias=None,
-          logits=None, stream=None):
+          logits=None, z_loss=None, stream=None):
     T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
     dt = TORCH_DTYPES[cfg["dtype"]]
     _want(x, "x", (T, d), dt)
@@ -165,9 +165,10 @@ def route(cfg, x, w_g, topk_idx, topk_w, f, P, aux, ws, logit_bias=None, select_
     _want(logit_bias, "logit_bias", (E,), torch.float32, allow_none=True)
     _want(select_bias, "select_bias", (E,), torch.float32, allow_none=True)
     _want(logits, "logits", (T, E), torch.float32, allow_none=True)
+    _want(z_loss, "z_loss", (1,), torch.float32, allow_none=True)
     _call("moe_route", ctypes.byref(make_config(cfg)), _p(x), _p(w_g), _p(logit_bias),
           _p(select_bias), _p(logits), _p(topk_idx), _p(topk_w), _p(f), _p(P), _p(aux),
-          _p(ws), ws.numel(), _stream(stream))
+          _p(z_loss), _p(ws), ws.numel(), _stream(stream))
 
 
 def permute(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm, ws,
@@ -256,7 +257,7 @@ def combine(cfg, y_perm, slot_of, topk_w, out, y_shared=None, stream=None):
 
 def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None, ws2=None,
             wsb2=None, logit_bias=None, select_bias=None, topk_idx=None, topk_w=None,
-            counts=None, f=None, P=None, aux=None, stream=None):
+            counts=None, f=None, P=None, aux=None, z_loss=None, stream=None):
     """The whole layer in one call (route -> permute -> grouped FFN -> combine)."""
     T, d, F, E, k, S = (cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"], cfg["k"],
                         cfg.get("n_shared", 0))
@@ -272,13 +273,14 @@ def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None,
     for n, t in (("f", f), ("P", P)):
         _want(t, n, (E,), torch.float32, allow_none=True)
     _want(aux, "aux", (1,), torch.float32, allow_none=True)
+    _want(z_loss, "z_loss", (1,), torch.float32, allow_none=True)
     if S:
         _want(ws1, "ws1", (S, F, d), dt)
         _want(ws2, "ws2", (S, d, F), dt)
     _call("moe_forward", ctypes.byref(make_config(cfg)), _p(x), _p(w_g), _p(logit_bias),
           _p(select_bias), _p(w1), _p(b1), _p(w2), _p(b2), _p(ws1), _p(wsb1), _p(ws2),
           _p(wsb2), _p(out), _p(topk_idx), _p(topk_w), _p(counts), _p(f), _p(P), _p(aux),
-          _p(ws), ws.numel(), _stream(stream))
+          _p(z_loss), _p(ws), ws.numel(), _stream(stream))
 
 
 class MoELayer:
@@ -303,6 +305,7 @@ class MoELayer:
         self.f = torch.empty((E,), dtype=torch.float32, device=self.device)
         self.P = torch.empty((E,), dtype=torch.float32, device=self.device)
         self.aux = torch.empty((1,), dtype=torch.float32, device=self.device)
+        self.z_loss = torch.empty((1,), dtype=torch.float32, device=self.device)
 
     def __call__(self, x: torch.Tensor, stream=None) -> dict:
         w = self.w
@@ -310,9 +313,13 @@ class MoELayer:
                 b2=w.get("b2"), ws1=w.get("ws1"), wsb1=w.get("wsb1"), ws2=w.get("ws2"),
                 wsb2=w.get("wsb2"), logit_bias=w.get("logit_bias"),
                 select_bias=w.get("select_bias"), topk_idx=self.topk_idx, topk_w=self.topk_w,
-                counts=self.counts, f=self.f, P=self.P, aux=self.aux, stream=stream)
+                counts=self.counts, f=self.f, P=self.P, aux=self.aux, z_loss=self.z_loss,
+                stream=stream)
+        return self._outputs()
+
+    def _outputs(self) -> dict:
         return dict(out=self.out, topk_idx=self.topk_idx, topk_w=self.topk_w,
-                    counts=self.counts, f=self.f, P=self.P, aux=self.aux)
+                    counts=self.counts, f=self.f, P=self.P, aux=self.aux, z_loss=self.z_loss)
 
 
 class GraphedMoELayer(MoELayer):
@@ -344,5 +351,4 @@ class GraphedMoELayer(MoELayer):
         if x is not None:
             self.x_static.copy_(x, non_blocking=True)
         self.graph.replay()
-        return dict(out=self.out, topk_idx=self.topk_idx, topk_w=self.topk_w,
-                    counts=self.counts, f=self.f, P=self.P, aux=self.aux)
+        return self._outputs()

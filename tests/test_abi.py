@@ -88,14 +88,15 @@ def test_missing_workspace_is_rejected_before_any_launch(lib):
     cfg = synth.workload("tiny_fp32_top2")
     c = moe.make_config(cfg)
     # no CUDA call happens: the workspace check fails first
-    s = lib.moe_route(ctypes.byref(c), 1, 1, None, None, None, 1, 1, 1, 1, 1, None, 0, None)
+    s = lib.moe_route(ctypes.byref(c), 1, 1, None, None, None, 1, 1, 1, 1, 1, None, None, 0,
+                      None)
     assert s == 3
     big = moe.workspace_size(cfg)
     s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, 1, 1, 1, None, None, None, None,
-                        1, None, None, None, None, None, None, 256, big - 1, None)
+                        1, None, None, None, None, None, None, None, 256, big - 1, None)
     assert s == 3  # too small
     s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, 1, 1, 1, None, None, None, None,
-                        1, None, None, None, None, None, None, 257, big, None)
+                        1, None, None, None, None, None, None, None, 257, big, None)
     assert s == 3  # misaligned
 
 
@@ -105,11 +106,11 @@ def test_null_required_pointers_rejected(lib):
     big = moe.workspace_size(cfg)
     # out == NULL
     s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, 1, 1, 1, None, None, None, None,
-                        None, None, None, None, None, None, None, 256, big, None)
+                        None, None, None, None, None, None, None, None, 256, big, None)
     assert s == 1
     # missing expert biases while has_bias = 1
     s = lib.moe_forward(ctypes.byref(c), 1, 1, None, None, 1, None, 1, None, None, None, None,
-                        None, 1, None, None, None, None, None, None, 256, big, None)
+                        None, 1, None, None, None, None, None, None, None, 256, big, None)
     assert s == 1
     s = lib.moe_combine(ctypes.byref(c), None, 1, 1, None, 1, None)
     assert s == 1

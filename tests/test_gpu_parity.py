@@ -38,14 +38,15 @@ def run_steps(cfg, inp):
     z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
     o = dict(logits=z((T, E), torch.float32), topk_idx=z((T, k), torch.int32),
              topk_w=z((T, k), torch.float32), f=z((E,), torch.float32),
-             P=z((E,), torch.float32), aux=z((1,), torch.float32), counts=z((E,), torch.int32),
+             P=z((E,), torch.float32), aux=z((1,), torch.float32),
+             z_loss=z((1,), torch.float32), counts=z((E,), torch.int32),
              kept=z((E,), torch.int32), offsets=z((E + 1,), torch.int32),
              perm_token=z((T * k,), torch.int32), slot_of=z((T * k,), torch.int32),
              x_perm=z((T * k, d), dt), y_perm=z((T * k, d), dt), out=z((T, d), dt))
     o["y_shared"] = z((S, T, d), dt) if S else None
     moe.route(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["f"], o["P"], o["aux"],
               ws, logit_bias=inp.get("logit_bias"), select_bias=inp.get("select_bias"),
-              logits=o["logits"])
+              logits=o["logits"], z_loss=o["z_loss"])
     moe.permute(cfg, inp["x"], o["topk_idx"], o["counts"], o["kept"], o["offsets"],
                 o["perm_token"], o["slot_of"], o["x_perm"], ws)
     moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws,
@@ -74,6 +75,8 @@ def check_steps(cfg, inp, st, rep_ref):
     bound = (d * u / (1 - d * u)) * (np.abs(x64) @ np.abs(wg64)) + u * np.abs(ref.logits)
     excess = np.abs(lg - ref.logits) - bound
     assert excess.max() <= 0, f"logits beyond the fp32 dot-product bound by {excess.max():.3e}"
+    zr = float(ref.extra["z_loss"])
+    assert abs(float(st["z_loss"][0]) - zr) <= compare.TOL_Z_REL * abs(zr), "z_loss differs"
     compare.compare_dispatch(ref, st)
     n = int(ref.disp.offsets[-1])
     # x_perm rows are exact copies of x[perm_token]
@@ -244,6 +247,7 @@ def test_tiny_token_counts(T):
     fw = run_forward(cfg, inp)
     if T == 0:
         assert np.all(fw["counts"] == 0) and float(fw["aux"][0]) == 0.0
+        assert float(fw["z_loss"][0]) == 0.0
         return
     compare.check_layer(cfg, inp, fw)
 
