@@ -50,7 +50,7 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 GEMM_SOURCES = ["gemm_tc.cuh", "ptx_sm100.cuh", "groups.cuh"]
 # oracle rows (tokens whose FFN output the CPU baseline computes) per workload
 CPU_SAMPLE_ROWS = {"tiny_fp32_top2": 256, "switch_top1_cap": 4096, "mixtral_top2": 128,
-                   "deepseek_v3_top8": 16, "decode_zipf_top2": 64}
+                   "deepseek_v3_top8": 16, "decode_zipf_top2": 64, "mixtral_swiglu_top2": 128}
 
 
 def parse():
@@ -164,11 +164,12 @@ class ClockSampler:
 def algorithmic_ffn(cfg, kept, elem):
     """Bytes and FLOPs the grouped FFN must move / do at least, for this batch."""
     d, F, S, T = cfg["d_model"], cfg["d_ff"], cfg.get("n_shared", 0), cfg["T"]
+    F1 = 2 * F if cfg.get("act", "gelu") == "swiglu" else F   # SwiGLU: gate and up rows
     n_a = int(sum(kept))
     active = int(sum(1 for v in kept if v > 0))
-    weights = (active + S) * 2 * d * F * elem
+    weights = (active + S) * (F1 + F) * d * elem
     acts = (n_a + S * T) * (d + F + F + d) * elem
-    flops = 2 * 2 * (n_a + S * T) * d * F
+    flops = 2 * (n_a + S * T) * d * (F1 + F)
     return weights + acts, flops, n_a, active
 
 
@@ -396,6 +397,7 @@ def emit_ours(args, res, world):
         "dtype": cfg["dtype"], "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))",
         "config": {"workload": cfg["name"], "T": T, "d_model": cfg["d_model"],
                    "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"],
+                   "act": cfg.get("act", "gelu"),
                    "n_shared": cfg.get("n_shared", 0), "capacity_factor": cfg["capacity_factor"],
                    "route": cfg["route"], "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MB write) before every step, outside the step events"},
@@ -447,7 +449,8 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))",
             "config": {"workload": cfg["name"], "T": cfg["T"], "d_model": cfg["d_model"],
-                       "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"]},
+                       "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"],
+                       "act": cfg.get("act", "gelu")},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
                              "cores": cpu["cores"], "kind": "oracle", "sample": cpu["sample"]},

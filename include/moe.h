@@ -11,14 +11,16 @@
  *   C      = max(floor(CF * T / E), min_capacity) when CF > 0; the assignments
  *            of an expert are ranked in ascending t*k + j and kept iff rank < C
  *   y      = sum_kept w[t,j] * FFN_{idx[t,j]}(x_t) + sum_s FFN_s(x_t)
- *   FFN(v) = GELU_erf(v W1^T + b1) W2^T + b2
+ *   FFN(v) = act(v W1^T + b1) W2^T + b2, act = GELU_erf (default) or SiLU;
+ *            SwiGLU: (SiLU(v W1g^T + b1g) * (v W1u^T + b1u)) W2^T + b2
  *   f_i, P_i, aux = alpha * E * sum_i f_i P_i          (Switch load balance)
  *   z      = mean_t logsumexp_e(logits[t, e])^2        (router z-loss)
  *
  * Sources: "混合专家大模型MoE架构选型与部署实践教程" §五 (SparseMoEGate,
  * SimpleMoELayer); "[BEE-30064] 混合專家架構與服務", 專家路由工作原理 (routing
  * steps 1-5, load_balance_loss); "AI-Research-SKILLs MoE 训练实战…全指南" §3.1,
- * §4.3, §7.1, §8.2; "第7章 Mixture of Experts" §7.1-§7.4.
+ * §4.3, §6.1 (SiLU experts; SwiGLU named for Mixtral), §7.1, §8.2;
+ * "第7章 Mixture of Experts" §7.1-§7.4.
  *
  * Conventions for every entry point
  *  - Ownership: the caller owns every buffer.  Unless stated otherwise a
@@ -76,6 +78,14 @@ typedef enum {
   MOE_AUX_ARGMAX = 1        /* f_i = (#tokens whose largest logit is i) / T */
 } moe_aux_f;
 
+typedef enum {
+  MOE_ACT_GELU = 0,     /* GELU_erf(h), h = x W1^T + b1                       */
+  MOE_ACT_SILU = 1,     /* h * sigmoid(h)                                     */
+  MOE_ACT_SWIGLU = 2    /* W1 holds 2F rows: the gate projection's F rows, then
+                           the up projection's F rows (b1 likewise 2F); the
+                           hidden activation is SiLU(h_gate) * h_up, F wide  */
+} moe_act;
+
 /* The problem statement.  All fields are read by every entry point. */
 typedef struct {
   int32_t T;               /* tokens, >= 0                                  */
@@ -92,6 +102,7 @@ typedef struct {
   int32_t has_bias;        /* 1: expert biases b1 [E,F], b2 [E,d] are given  */
   float aux_alpha;         /* alpha of the aux loss                         */
   int32_t aux_f;           /* moe_aux_f                                     */
+  int32_t act;             /* moe_act: the experts' hidden activation        */
 } moe_config;
 
 /* Bytes of workspace the entry points below need for `cfg` (host only). */
@@ -167,13 +178,14 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
 
 /* Expert MLPs as a grouped GEMM over the expert-contiguous rows.
  *   x_perm [T*k, d], offsets [E+1] (device; read on the device only).
- *   w1 [E,F,d], b1 [E,F] or NULL, w2 [E,d,F], b2 [E,d] or NULL.
- *   Shared experts (cfg.n_shared > 0): x [T,d], ws1 [S,F,d], wsb1 [S,F] or
+ *   w1 [E,F1,d], b1 [E,F1] or NULL, w2 [E,d,F], b2 [E,d] or NULL, where
+ *   F1 = 2F for MOE_ACT_SWIGLU (gate rows, then up rows) and F otherwise.
+ *   Shared experts (cfg.n_shared > 0): x [T,d], ws1 [S,F1,d], wsb1 [S,F1] or
  *   NULL, ws2 [S,d,F], wsb2 [S,d] or NULL, output y_shared [S,T,d] dtype.
  *   Output y_perm [T*k, d] dtype: row r = FFN_e(x_perm[r]) for the expert e
  *   whose range holds r; rows >= offsets[E] unspecified.  Both GEMMs
- *   accumulate in fp32; the hidden activation GELU(x W1^T + b1) (in `ws`) and
- *   the expert outputs are rounded once to dtype. */
+ *   accumulate in fp32; the hidden activation [rows, F] (in `ws`) and the
+ *   expert outputs are rounded once to dtype. */
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                            const void* w1, const void* b1, const void* w2, const void* b2,
                            const void* x, const void* ws1, const void* wsb1,

@@ -253,17 +253,26 @@ struct SimtArgs {
   float* out;        // routed groups' rows
   float* out1;       // shared groups' rows
   int64_t ldo;
-  int gelu;
+  int act;           // SIMT_ACT_*
 };
 
+// Epilogue of k_gemm_simt_f32.  SIMT_ACT_SWIGLU: B (and the bias) hold 2N
+// rows, the gate projection's then the up projection's, and the output is
+// SiLU(gate) * up over N columns.
+enum : int { SIMT_ACT_NONE = 0, SIMT_ACT_GELU = 1, SIMT_ACT_SILU = 2, SIMT_ACT_SWIGLU = 3 };
+
+__device__ __forceinline__ float simt_silu(float v) { return v / (1.0f + expf(-v)); }
+
+template <bool GLU>
 __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
   constexpr int BM = 64, BN = 64, BK = 16;
   constexpr int LA = BK * BM / 256, LB = BK * BN / 256;   // elements per thread per k-step
+  constexpr int NB = GLU ? 2 : 1;                         // B tiles: gate (and up)
   griddep_wait();
   griddep_launch_dependents();
   __shared__ GroupTable tb;
   __shared__ float As[2][BK][BM + 4];
-  __shared__ float Bs[2][BK][BN + 4];
+  __shared__ float Bs[2][NB][BK][BN + 4];
   const GroupSpec& gs = a.gs;
   const int G = gs.E + gs.n_shared;
   const int n_tiles = (a.N + BN - 1) / BN;
@@ -276,15 +285,15 @@ __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
     const bool routed = g < gs.E;
     const float* A = (routed || gs.shared_a_sel == 0) ? a.A0 : a.A1;
     const int gi = routed ? (gs.offsets ? g : 0) : g - gs.E;
-    const float* B = (routed ? a.B0 : a.B1) + static_cast<int64_t>(gi) * a.N * a.K;
+    const float* B = (routed ? a.B0 : a.B1) + static_cast<int64_t>(gi) * NB * a.N * a.K;
     const float* bias = routed ? a.bias0 : a.bias1;
-    if (bias) bias += static_cast<int64_t>(gi) * a.N;
+    if (bias) bias += static_cast<int64_t>(gi) * NB * a.N;
     const int rows = tb.rows[g];
     const int m0 = m_blk * BM, n0 = n_blk * BN;
     const int64_t arow0 = tb.a_row0[g];
     // global -> registers for k-step k0 (the next step's loads are in flight
     // while the current step computes from shared memory)
-    float ra[LA], rb[LB];
+    float ra[LA], rb[NB][LB];
     auto fetch = [&](int k0) {
 #pragma unroll
       for (int q = 0; q < LA; ++q) {
@@ -294,12 +303,16 @@ __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
         ra[q] = (gr < rows && gk < a.K) ? __ldg(A + (arow0 + gr) * a.lda + gk) : 0.f;
       }
 #pragma unroll
-      for (int q = 0; q < LB; ++q) {
-        const int i = tid + 256 * q;
-        const int n = i / BK, kk = i % BK;
-        const int gn = n0 + n, gk = k0 + kk;
-        rb[q] = (gn < a.N && gk < a.K) ? __ldg(B + static_cast<int64_t>(gn) * a.K + gk) : 0.f;
-      }
+      for (int h = 0; h < NB; ++h)
+#pragma unroll
+        for (int q = 0; q < LB; ++q) {
+          const int i = tid + 256 * q;
+          const int n = i / BK, kk = i % BK;
+          const int gn = n0 + n, gk = k0 + kk;
+          rb[h][q] = (gn < a.N && gk < a.K)
+                         ? __ldg(B + (static_cast<int64_t>(h) * a.N + gn) * a.K + gk)
+                         : 0.f;
+        }
     };
     auto stash = [&](int buf) {
 #pragma unroll
@@ -308,12 +321,14 @@ __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
         As[buf][i % BK][i / BK] = ra[q];
       }
 #pragma unroll
-      for (int q = 0; q < LB; ++q) {
-        const int i = tid + 256 * q;
-        Bs[buf][i % BK][i / BK] = rb[q];
-      }
+      for (int h = 0; h < NB; ++h)
+#pragma unroll
+        for (int q = 0; q < LB; ++q) {
+          const int i = tid + 256 * q;
+          Bs[buf][h][i % BK][i / BK] = rb[h][q];
+        }
     };
-    float acc[4][4] = {};
+    float acc[NB][4][4] = {};
     fetch(0);
     stash(0);
     __syncthreads();
@@ -323,16 +338,19 @@ __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
       if (more) fetch(k0 + BK);
 #pragma unroll
       for (int kk = 0; kk < BK; ++kk) {
-        float av[4], bv[4];
+        float av[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          av[i] = As[buf][kk][ty * 4 + i];
-          bv[i] = Bs[buf][kk][tx * 4 + i];
+        for (int i = 0; i < 4; ++i) av[i] = As[buf][kk][ty * 4 + i];
+#pragma unroll
+        for (int h = 0; h < NB; ++h) {
+          float bv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bv[j] = Bs[buf][h][kk][tx * 4 + j];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[h][i][j] = fmaf(av[i], bv[j], acc[h][i][j]);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
       }
       if (more) stash(buf ^ 1);
       __syncthreads();
@@ -347,8 +365,15 @@ __global__ void __launch_bounds__(256) k_gemm_simt_f32(const SimtArgs a) {
       for (int j = 0; j < 4; ++j) {
         const int gn = n0 + tx * 4 + j;
         if (gn >= a.N) continue;
-        float v = acc[i][j] + (bias ? bias[gn] : 0.f);
-        if (a.gelu) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+        float v = acc[0][i][j] + (bias ? bias[gn] : 0.f);
+        if (GLU) {
+          const float up = acc[NB - 1][i][j] + (bias ? bias[a.N + gn] : 0.f);
+          v = simt_silu(v) * up;
+        } else if (a.act == SIMT_ACT_GELU) {
+          v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+        } else if (a.act == SIMT_ACT_SILU) {
+          v = simt_silu(v);
+        }
         o[gn] = v;
       }
     }

@@ -8,8 +8,8 @@
 // (groups.cuh).  Warp roles inside a CTA (192 threads):
 //   warp 0     : TMA producer (one lane) - A and B tiles into a STAGES-deep ring
 //   warp 1     : TMEM owner and MMA issuer (one lane) - 128 x BN x 16 MMAs
-//   warps 2..5 : epilogue - tcgen05.ld, bias / GELU, convert, store
-//                (GELU output in bf16: the next GEMM's A operand; others in fp32)
+//   warps 2..5 : epilogue - tcgen05.ld, bias / activation, convert, store
+//                (bf16 activations: the next GEMM's A operand; logits in fp32)
 // The accumulator is double-buffered in TMEM (2 x BN fp32 columns) so the
 // epilogue of one segment overlaps the main loop of the next.
 //
@@ -38,10 +38,21 @@
 
 namespace moe {
 
-// Epilogues: fp32 logits (router); GELU(acc + b1) in bf16 (up-projection);
-// acc + b2 in bf16 (down-projection); and the down-projection fused with the
-// top-1 combine: out[token of the row] = w[token] * (acc + b2) in bf16.
-enum : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_BIAS_BF16 = 2, EPI_SCATTER_BF16 = 3 };
+// Epilogues: fp32 logits (router); GELU(acc + b1) or SiLU(acc + b1) in bf16
+// (up-projection); acc + b2 in bf16 (down-projection); the down-projection
+// fused with the top-1 combine: out[token of the row] = w[token] * (acc + b2)
+// in bf16; and SwiGLU, where the tile's BN accumulator columns are two halves
+// - the gate projection's BN/2 columns, then the up projection's same BN/2
+// columns (B rows n and N + n of a [2N, K] weight) - and the output is
+// SiLU(gate) * up, BN/2 columns wide.
+enum : int {
+  EPI_F32 = 0,
+  EPI_GELU_BF16 = 1,
+  EPI_BIAS_BF16 = 2,
+  EPI_SCATTER_BF16 = 3,
+  EPI_SILU_BF16 = 4,
+  EPI_SWIGLU_BF16 = 5
+};
 enum : int {
   DEV_ERR_WAIT_PRODUCER = 1,
   DEV_ERR_WAIT_MMA = 2,
@@ -81,6 +92,9 @@ __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uin
 __device__ __forceinline__ float gelu_erf(float v) {
   return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
 }
+
+// v * sigmoid(v); for v -> -inf the quotient goes to -0, for v -> +inf to v
+__device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 
 // The segments (tile, [kb0, kb1)) a CTA processes, in order; every warp role
 // walks the same sequence.
@@ -180,7 +194,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GroupSpec& gs = args.gs;
   const int G = gs.E + gs.n_shared;
-  const int n_tiles = (args.N + BN - 1) / BN;
+  constexpr bool GLU = EPI == EPI_SWIGLU_BF16;
+  constexpr int BNO = GLU ? BN / 2 : BN;   // output columns of a tile
+  const int n_tiles = (args.N + BNO - 1) / BNO;
   const int KB = (args.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -241,7 +257,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         const CUtensorMap* mb = routed ? &mB0 : &mB1;
         const int bz = routed ? (gs.offsets ? g : 0) : g - gs.E;
         const int arow = c.tb.a_row0[g] + m_blk * BM;
-        const int ncol = n_blk * BN;
+        const int ncol = n_blk * BNO;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&c.empty[stage], phase ^ 1u, abort_flag, args.err,
                                  DEV_ERR_WAIT_PRODUCER, kWaitLimitNs)) {
@@ -251,6 +267,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           mbar_arrive_expect_tx(&c.full[stage], L::STAGE_BYTES);
           tma_load_2d(sA + stage * L::A_BYTES, ma, &c.full[stage], kb * BK, arow);
           tma_load_3d(sB + stage * L::B_BYTES, mb, &c.full[stage], kb * BK, ncol, bz);
+          if (GLU)   // the up projection's rows into the second half of the B tile
+            tma_load_3d(sB + stage * L::B_BYTES + (BN / 2) * BK * 2, mb, &c.full[stage], kb * BK,
+                        args.N + ncol, bz);
 #pragma unroll
           for (int s = 0; s < STAGES; ++s) armed[s] += (s == stage) ? 1u : 0u;
           if (++stage == STAGES) {
@@ -403,31 +422,41 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       }
       const __nv_bfloat16* bias = nullptr;
       if (EPI != EPI_F32) {
-        if (routed && args.bias0) bias = args.bias0 + static_cast<int64_t>(gs.offsets ? g : 0) * args.N;
-        if (!routed && args.bias1) bias = args.bias1 + static_cast<int64_t>(g - gs.E) * args.N;
+        const int64_t bstride = GLU ? 2 * static_cast<int64_t>(args.N) : args.N;
+        if (routed && args.bias0) bias = args.bias0 + static_cast<int64_t>(gs.offsets ? g : 0) * bstride;
+        if (!routed && args.bias1) bias = args.bias1 + static_cast<int64_t>(g - gs.E) * bstride;
       }
+      // later k-blocks of this tile from the following CTAs' partials, in order
+      auto add_partials = [&](int chunk, float(&v)[16]) {
+        for (int p = blockIdx.x + 1; p <= last; ++p) {
+          const float4* src = reinterpret_cast<const float4*>(
+              args.partial + (static_cast<int64_t>(p) * NCC * BM + static_cast<int64_t>(chunk) * BM + row) * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 w = __ldcg(src + i);
+            v[4 * i] += w.x;
+            v[4 * i + 1] += w.y;
+            v[4 * i + 2] += w.z;
+            v[4 * i + 3] += w.w;
+          }
+        }
+      };
+      constexpr int NOUT = GLU ? NCC / 2 : NCC;   // 16-column output chunks
 #pragma unroll 1
-      for (int cc = 0; cc < NCC; ++cc) {
-        uint32_t r[16];
+      for (int cc = 0; cc < NOUT; ++cc) {
+        uint32_t r[16], ru[GLU ? 16 : 1];
         tmem_ld_32x32b_x16(trow + cc * 16, r);
         tmem_wait_ld(r);
-        const int col = n_blk * BN + cc * 16;
+        if constexpr (GLU) {   // the up half's matching columns
+          tmem_ld_32x32b_x16(trow + (cc + NCC / 2) * 16, ru);
+          tmem_wait_ld(ru);
+        }
+        const int col = n_blk * BNO + cc * 16;
         if (!valid || col >= args.N) continue;
         float v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-        for (int p = blockIdx.x + 1; p <= last; ++p) {   // later k-blocks, in order
-          const float4* src = reinterpret_cast<const float4*>(
-              args.partial + (static_cast<int64_t>(p) * NCC * BM + static_cast<int64_t>(cc) * BM + row) * 16);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 u = __ldcg(src + i);
-            v[4 * i] += u.x;
-            v[4 * i + 1] += u.y;
-            v[4 * i + 2] += u.z;
-            v[4 * i + 3] += u.w;
-          }
-        }
+        add_partials(cc, v);
         if (EPI != EPI_F32 && bias) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -443,7 +472,22 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
             for (int i = 0; i < 16 && col + i < args.N; ++i) o[i] = v[i];
           }
         } else {
-          if (EPI == EPI_GELU_BF16) {
+          if constexpr (GLU) {
+            float w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __uint_as_float(ru[i]);
+            add_partials(cc + NCC / 2, w);
+            if (bias) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (col + i < args.N) w[i] += __bfloat162float(bias[args.N + col + i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = silu(v[i]) * w[i];
+          } else if (EPI == EPI_SILU_BF16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = silu(v[i]);
+          } else if (EPI == EPI_GELU_BF16) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = gelu_erf(v[i]);
           } else if (EPI == EPI_SCATTER_BF16) {

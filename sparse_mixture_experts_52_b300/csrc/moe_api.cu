@@ -60,6 +60,7 @@ moe_status validate(const moe_config* c) {
   if (c->aux_f != MOE_AUX_TOPK_COUNT && c->aux_f != MOE_AUX_ARGMAX) return MOE_ERR_INVALID_ARG;
   if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_INVALID_ARG;
   if (c->has_bias != 0 && c->has_bias != 1) return MOE_ERR_INVALID_ARG;
+  if (c->act < MOE_ACT_GELU || c->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha))
     return MOE_ERR_INVALID_ARG;
   const int64_t Tk = static_cast<int64_t>(c->T) * c->k;
@@ -146,10 +147,6 @@ moe_status check_ws(const moe_config& c, void* ws, size_t ws_bytes, const Layout
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   (void)c;
   return MOE_OK;
-}
-
-inline moe_status launch_ok() {
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // Launches `kern` with programmatic stream serialisation: it may begin while
@@ -252,7 +249,8 @@ moe_status launch_tc_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CU
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t n_tiles = (args.N + BN - 1) / BN;
+  constexpr int BNO = (EPI == EPI_SWIGLU_BF16) ? BN / 2 : BN;   // output columns per tile
+  const int64_t n_tiles = (args.N + BNO - 1) / BNO;
   const int64_t ub = std::max<int64_t>(1, row_tiles_ub * n_tiles);
   // stream-K: one CTA per SM (at most one partial slot each) whatever the tile
   // count; round-robin: no more CTAs than tiles
@@ -297,14 +295,6 @@ FfnSplit pick_ffn_split(int N, int64_t row_tiles, int sms) {
   return FfnSplit{best, 0};
 }
 
-int pick_bn(int N, bool allow_small) {
-  if (N >= 256) return 256;
-  if (N >= 128) return 128;
-  if (N >= 64 || !allow_small) return 64;
-  if (N >= 32) return 32;
-  return 16;
-}
-
 moe_status launch_tc(int epi, const CUtensorMap& a0, const CUtensorMap& a1,
                      const CUtensorMap& b0, const CUtensorMap& b1, const TcArgs& args, int BN,
                      int64_t row_tiles_ub, cudaStream_t st) {
@@ -316,25 +306,24 @@ moe_status launch_tc(int epi, const CUtensorMap& a0, const CUtensorMap& a1,
       case 128: return launch_tc_inst<128, 6, EPI_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
       case 256: return launch_tc_inst<256, 4, EPI_F32>(a0, a1, b0, b1, args, row_tiles_ub, st);
     }
-  } else if (epi == EPI_BIAS_BF16) {
-    switch (BN) {
-      case 64: return launch_tc_inst<64, 8, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 128: return launch_tc_inst<128, 6, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 256: return launch_tc_inst<256, 4, EPI_BIAS_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-    }
-  } else if (epi == EPI_SCATTER_BF16) {
-    switch (BN) {
-      case 64: return launch_tc_inst<64, 8, EPI_SCATTER_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 128: return launch_tc_inst<128, 6, EPI_SCATTER_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 256: return launch_tc_inst<256, 4, EPI_SCATTER_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-    }
-  } else if (epi == EPI_GELU_BF16) {
-    switch (BN) {
-      case 64: return launch_tc_inst<64, 8, EPI_GELU_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 128: return launch_tc_inst<128, 6, EPI_GELU_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-      case 256: return launch_tc_inst<256, 4, EPI_GELU_BF16>(a0, a1, b0, b1, args, row_tiles_ub, st);
-    }
+    return MOE_ERR_UNSUPPORTED;
   }
+  // bf16 epilogues: tiles 64, 128 or 256 wide with 8, 6 or 4 pipeline stages
+#define MOE_BF16_EPI(EPI)                                                                 \
+  if (epi == EPI) {                                                                       \
+    switch (BN) {                                                                         \
+      case 64: return launch_tc_inst<64, 8, EPI>(a0, a1, b0, b1, args, row_tiles_ub, st);   \
+      case 128: return launch_tc_inst<128, 6, EPI>(a0, a1, b0, b1, args, row_tiles_ub, st); \
+      case 256: return launch_tc_inst<256, 4, EPI>(a0, a1, b0, b1, args, row_tiles_ub, st); \
+    }                                                                                     \
+    return MOE_ERR_UNSUPPORTED;                                                           \
+  }
+  MOE_BF16_EPI(EPI_GELU_BF16)
+  MOE_BF16_EPI(EPI_BIAS_BF16)
+  MOE_BF16_EPI(EPI_SCATTER_BF16)
+  MOE_BF16_EPI(EPI_SILU_BF16)
+  MOE_BF16_EPI(EPI_SWIGLU_BF16)
+#undef MOE_BF16_EPI
   return MOE_ERR_UNSUPPORTED;
 }
 
@@ -671,16 +660,20 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   const void* wsb1 = c.has_bias ? in.wsb1 : nullptr;
   const void* wsb2 = c.has_bias ? in.wsb2 : nullptr;
   moe_status s;
+  const bool glu = c.act == MOE_ACT_SWIGLU;
+  const int F1 = glu ? 2 * F : F;   // rows of W1: SwiGLU stacks the gate and up projections
   if (c.dtype == MOE_BF16) {
     CUtensorMap ma0, ma1, mb0, mb1;
-    // up-projection + GELU:  H = GELU(x_perm W1^T + b1)
+    // up-projection + activation:  H = act(x_perm W1^T + b1)
     if (!map_a(&ma0, in.x_perm, d, std::max<int64_t>(Tk, 1))) return MOE_ERR_CUDA;
     const int64_t rt = est_row_tiles(Tk, c.E) + S * ((T + 127) / 128);
-    const FfnSplit sp_up = pick_ffn_split(F, rt, num_sms());
+    const FfnSplit sp_up = pick_ffn_split(F1, rt, num_sms());
     const int bn_up = sp_up.bn;
-    if (!map_b(&mb0, in.w1, d, F, c.E, bn_up)) return MOE_ERR_CUDA;
+    // SwiGLU: each B tile is two boxes of bn_up / 2 rows (gate rows n.., up rows F + n..)
+    const int box_up = glu ? bn_up / 2 : bn_up;
+    if (!map_b(&mb0, in.w1, d, F1, c.E, box_up)) return MOE_ERR_CUDA;
     if (S > 0) {
-      if (!map_a(&ma1, in.x, d, T) || !map_b(&mb1, in.ws1, d, F, S, bn_up)) return MOE_ERR_CUDA;
+      if (!map_a(&ma1, in.x, d, T) || !map_b(&mb1, in.ws1, d, F1, S, box_up)) return MOE_ERR_CUDA;
     } else {
       ma1 = ma0;
       mb1 = mb0;
@@ -699,7 +692,9 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     up.streamk = sp_up.streamk;
     up.partial = at<float>(ws, L.sk_part);
     up.flags = at<int>(ws, L.status + kFlagsOffset);
-    if ((s = launch_tc(EPI_GELU_BF16, ma0, ma1, mb0, mb1, up, bn_up, row_tiles_ub, st)) != MOE_OK)
+    const int epi_up = glu ? EPI_SWIGLU_BF16
+                           : (c.act == MOE_ACT_SILU ? EPI_SILU_BF16 : EPI_GELU_BF16);
+    if ((s = launch_tc(epi_up, ma0, ma1, mb0, mb1, up, bn_up, row_tiles_ub, st)) != MOE_OK)
       return s;
     // down-projection:  y = H W2^T + b2
     CUtensorMap ha, hb0, hb1;
@@ -749,10 +744,11 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   up.out = static_cast<float*>(H);
   up.out1 = static_cast<float*>(H_shared);
   up.ldo = F;
-  up.gelu = 1;
+  up.act = glu ? SIMT_ACT_SWIGLU : (c.act == MOE_ACT_SILU ? SIMT_ACT_SILU : SIMT_ACT_GELU);
   int grid = static_cast<int>(std::min<int64_t>(tiles_ub * ((F + 63) / 64), num_sms() * 4));
-  if ((s = launch_pdl(k_gemm_simt_f32, dim3(std::max(grid, 1)), dim3(256), 0, st, up)) != MOE_OK)
-    return s;
+  s = glu ? launch_pdl(k_gemm_simt_f32<true>, dim3(std::max(grid, 1)), dim3(256), 0, st, up)
+          : launch_pdl(k_gemm_simt_f32<false>, dim3(std::max(grid, 1)), dim3(256), 0, st, up);
+  if (s != MOE_OK) return s;
   SimtArgs dn{};
   dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0, c.T};
   dn.N = d;
@@ -767,9 +763,9 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
   dn.out = static_cast<float*>(y_perm);
   dn.out1 = static_cast<float*>(y_shared);
   dn.ldo = d;
-  dn.gelu = 0;
+  dn.act = SIMT_ACT_NONE;
   grid = static_cast<int>(std::min<int64_t>(tiles_ub * ((d + 63) / 64), num_sms() * 4));
-  return launch_pdl(k_gemm_simt_f32, dim3(std::max(grid, 1)), dim3(256), 0, st, dn);
+  return launch_pdl(k_gemm_simt_f32<false>, dim3(std::max(grid, 1)), dim3(256), 0, st, dn);
 }
 
 moe_status do_combine(const moe_config& c, const void* y_perm, const int32_t* slot_of,

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 ROUTES = {"softmax_topk": 0, "topk_softmax": 1, "biased_softmax": 2}
 DTYPES = {"f32": 0, "bf16": 1}
 AUX_F = {"topk_count": 0, "argmax": 1}
+ACTS = {"gelu": 0, "silu": 1, "swiglu": 2}
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -40,6 +41,7 @@ class Config(ctypes.Structure):
         ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
         ("route", ctypes.c_int32), ("renorm", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("has_bias", ctypes.c_int32), ("aux_alpha", ctypes.c_float), ("aux_f", ctypes.c_int32),
+        ("act", ctypes.c_int32),
     ]
 
 
@@ -59,7 +61,15 @@ def make_config(cfg: dict) -> Config:
     c.aux_alpha = float(cfg.get("aux_alpha", 0.01))
     af = cfg.get("aux_f", "topk_count")
     c.aux_f = AUX_F[af] if isinstance(af, str) else int(af)
+    a = cfg.get("act", "gelu")
+    c.act = ACTS[a] if isinstance(a, str) else int(a)
     return c
+
+
+def w1_rows(cfg: dict) -> int:
+    """Rows of each expert's first weight: 2 d_ff for SwiGLU (the gate
+    projection's rows, then the up projection's), else d_ff."""
+    return 2 * cfg["d_ff"] if cfg.get("act", "gelu") in ("swiglu", ACTS["swiglu"]) else cfg["d_ff"]
 
 
 _lib = None
@@ -225,16 +235,18 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
     T, d, F, E, k, S = (cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"], cfg["k"],
                         cfg.get("n_shared", 0))
     dt = TORCH_DTYPES[cfg["dtype"]]
+    F1 = w1_rows(cfg)
     _want(x_perm, "x_perm", (T * k, d), dt)
     _want(offsets, "offsets", (E + 1,), torch.int32)
-    _want(w1, "w1", (E, F, d), dt)
+    _want(w1, "w1", (E, F1, d), dt)
     _want(w2, "w2", (E, d, F), dt)
-    _want(b1, "b1", (E, F), dt, allow_none=not cfg.get("has_bias", 0))
+    _want(b1, "b1", (E, F1), dt, allow_none=not cfg.get("has_bias", 0))
     _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
     _want(y_perm, "y_perm", (T * k, d), dt)
     if S:
         _want(x, "x", (T, d), dt)
-        _want(ws1, "ws1", (S, F, d), dt)
+        _want(ws1, "ws1", (S, F1, d), dt)
+        _want(wsb1, "wsb1", (S, F1), dt, allow_none=True)
         _want(ws2, "ws2", (S, d, F), dt)
         _want(y_shared, "y_shared", (S, T, d), dt)
     _call("moe_grouped_ffn", ctypes.byref(make_config(cfg)), _p(x_perm), _p(offsets), _p(w1),
@@ -264,8 +276,10 @@ def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None,
     dt = TORCH_DTYPES[cfg["dtype"]]
     _want(x, "x", (T, d), dt)
     _want(w_g, "w_g", (d, E), dt)
-    _want(w1, "w1", (E, F, d), dt)
+    F1 = w1_rows(cfg)
+    _want(w1, "w1", (E, F1, d), dt)
     _want(w2, "w2", (E, d, F), dt)
+    _want(b1, "b1", (E, F1), dt, allow_none=True)
     _want(out, "out", (T, d), dt)
     _want(topk_idx, "topk_idx", (T, k), torch.int32, allow_none=True)
     _want(topk_w, "topk_w", (T, k), torch.float32, allow_none=True)
@@ -275,7 +289,8 @@ def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None,
     _want(aux, "aux", (1,), torch.float32, allow_none=True)
     _want(z_loss, "z_loss", (1,), torch.float32, allow_none=True)
     if S:
-        _want(ws1, "ws1", (S, F, d), dt)
+        _want(ws1, "ws1", (S, F1, d), dt)
+        _want(wsb1, "wsb1", (S, F1), dt, allow_none=True)
         _want(ws2, "ws2", (S, d, F), dt)
     _call("moe_forward", ctypes.byref(make_config(cfg)), _p(x), _p(w_g), _p(logit_bias),
           _p(select_bias), _p(w1), _p(b1), _p(w2), _p(b2), _p(ws1), _p(wsb1), _p(ws2),

@@ -7,8 +7,9 @@ that will hold it, then (for bf16 workloads) rounded to bf16 once; a test hands
 the very same values to both sides.
 
 Recipe (per workload, in draw order): x ~ N(0, 1) [T, d]; W_g ~ N(0, 1/d)
-[d, E]; per routed expert e = 0..E-1: W1_e ~ N(0, 1/d) [d_ff, d], then
-W2_e ~ N(0, 1/d_ff) [d, d_ff]; then the shared experts in the same way; then
+[d, E]; per routed expert e = 0..E-1: W1_e ~ N(0, 1/d) [d_ff, d] ([2 d_ff, d]
+for SwiGLU experts: gate rows, then up rows), then W2_e ~ N(0, 1/d_ff)
+[d, d_ff]; then the shared experts in the same way; then
 the optional biases and the DeepSeek-style selection bias ~ N(0, 0.01^2) [E].
 Biases are zero unless ``nonzero_bias`` (then N(0, 0.1^2)).  The skewed decode
 workload adds a fixed logit offset log(Zipf(s=1.2) over the experts), expert 0
@@ -59,9 +60,13 @@ WORKLOADS = {
         logit_bias="zipf1.2", select_bias_std=0.0),
 }
 
+# The Mixtral shape with SwiGLU experts, the activation named for Mixtral's
+# FFN (its W1 holds the gate and up projections: 2 x 14336 rows).
+WORKLOADS["mixtral_swiglu_top2"] = dict(WORKLOADS["mixtral_top2"], act="swiglu")
+
 LAYER_KEYS = ("T", "d_model", "d_ff", "E", "k", "n_shared", "capacity_factor",
               "min_capacity", "route", "renorm", "dtype", "has_bias",
-              "aux_alpha", "aux_f")
+              "aux_alpha", "aux_f", "act")
 
 
 def workload(name: str, **overrides) -> dict:
@@ -89,7 +94,8 @@ def make_inputs(cfg: dict, device="cpu", seed: Optional[int] = None,
                 nonzero_bias: bool = False) -> dict:
     """Draw every input of one layer call on ``device``.
 
-    Returns a dict of tensors: x, w_g, w1 [E,F,d], w2 [E,d,F], b1/b2 (or None),
+    Returns a dict of tensors: x, w_g, w1 [E,F1,d] (F1 = 2F for SwiGLU, else
+    F), w2 [E,d,F], b1/b2 (or None),
     ws1/ws2/wsb1/wsb2 for shared experts (or None), logit_bias, select_bias
     (float32 [E] or None).
     """
@@ -99,21 +105,22 @@ def make_inputs(cfg: dict, device="cpu", seed: Optional[int] = None,
     g.manual_seed(int(seed))
     dt = torch.float32 if cfg["dtype"] == "f32" else torch.bfloat16
     T, d, F, E, S = cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"], cfg["n_shared"]
+    F1 = 2 * F if cfg.get("act", "gelu") == "swiglu" else F   # rows of W1
 
     out = {}
     out["x"] = _draw(g, (T, d), 1.0, device, dt)
     out["w_g"] = _draw(g, (d, E), 1.0 / math.sqrt(d), device, dt)
-    w1 = torch.empty((E, F, d), device=device, dtype=dt)
+    w1 = torch.empty((E, F1, d), device=device, dtype=dt)
     w2 = torch.empty((E, d, F), device=device, dtype=dt)
     for e in range(E):
-        w1[e] = _draw(g, (F, d), 1.0 / math.sqrt(d), device, dt)
+        w1[e] = _draw(g, (F1, d), 1.0 / math.sqrt(d), device, dt)
         w2[e] = _draw(g, (d, F), 1.0 / math.sqrt(F), device, dt)
     out["w1"], out["w2"] = w1, w2
     if S > 0:
-        ws1 = torch.empty((S, F, d), device=device, dtype=dt)
+        ws1 = torch.empty((S, F1, d), device=device, dtype=dt)
         ws2 = torch.empty((S, d, F), device=device, dtype=dt)
         for s in range(S):
-            ws1[s] = _draw(g, (F, d), 1.0 / math.sqrt(d), device, dt)
+            ws1[s] = _draw(g, (F1, d), 1.0 / math.sqrt(d), device, dt)
             ws2[s] = _draw(g, (d, F), 1.0 / math.sqrt(F), device, dt)
         out["ws1"], out["ws2"] = ws1, ws2
     else:
@@ -122,16 +129,16 @@ def make_inputs(cfg: dict, device="cpu", seed: Optional[int] = None,
     out["b1"] = out["b2"] = out["wsb1"] = out["wsb2"] = None
     if cfg["has_bias"]:
         if nonzero_bias:
-            out["b1"] = _draw(g, (E, F), 0.1, device, dt)
+            out["b1"] = _draw(g, (E, F1), 0.1, device, dt)
             out["b2"] = _draw(g, (E, d), 0.1, device, dt)
             if S > 0:
-                out["wsb1"] = _draw(g, (S, F), 0.1, device, dt)
+                out["wsb1"] = _draw(g, (S, F1), 0.1, device, dt)
                 out["wsb2"] = _draw(g, (S, d), 0.1, device, dt)
         else:
-            out["b1"] = torch.zeros((E, F), device=device, dtype=dt)
+            out["b1"] = torch.zeros((E, F1), device=device, dtype=dt)
             out["b2"] = torch.zeros((E, d), device=device, dtype=dt)
             if S > 0:
-                out["wsb1"] = torch.zeros((S, F), device=device, dtype=dt)
+                out["wsb1"] = torch.zeros((S, F1), device=device, dtype=dt)
                 out["wsb2"] = torch.zeros((S, d), device=device, dtype=dt)
 
     sb = cfg.get("select_bias_std", 0.0)

@@ -40,10 +40,18 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_config_struct_layout(lib):
-    # 14 four-byte fields, no padding
-    assert ctypes.sizeof(moe.Config) == 56
+    # 15 four-byte fields, no padding
+    assert ctypes.sizeof(moe.Config) == 60
     assert moe.Config.capacity_factor.offset == 24
     assert moe.Config.aux_f.offset == 52
+    assert moe.Config.act.offset == 56
+
+
+def test_activation_value_is_validated(lib):
+    for act, want in ((0, 0), (1, 0), (2, 0), (3, 1), (-1, 1)):
+        c = moe.make_config(synth.workload("tiny_fp32_top2", act=act))
+        n = ctypes.c_size_t(0)
+        assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == want, act
 
 
 def test_status_strings(lib):

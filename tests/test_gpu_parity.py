@@ -91,7 +91,8 @@ def check_steps(cfg, inp, st, rep_ref):
         a, b = int(ref.disp.offsets[e]), int(ref.disp.offsets[e + 1])
         if a == b:
             continue
-        yr = om.expert_ffn(x64[ref.disp.perm_token[a:b]], *experts(e))
+        yr = om.expert_ffn(x64[ref.disp.perm_token[a:b]], *experts(e),
+                           act=cfg.get("act", om.ACT_GELU))
         rel = np.linalg.norm(yp[a:b] - yr) / max(np.linalg.norm(yr), 1e-30)
         tol = compare.TOL_F32_REL_L2 if cfg["dtype"] == "f32" else compare.TOL_BF16_REL_L2
         assert rel <= tol, f"expert {e}: y_perm rel-L2 {rel:.3e}"
@@ -118,6 +119,15 @@ SMALL = {
     "cap_min_capacity": dict(name="switch_top1_cap", T=512, d_model=64, d_ff=64, E=16, k=2,
                              capacity_factor=0.25, min_capacity=5, route="softmax_topk",
                              renorm=1, aux_f="topk_count"),
+    # expert activations: SiLU, and SwiGLU (gate and up halves in one up-GEMM)
+    "silu_small": dict(name="mixtral_top2", T=600, d_model=256, d_ff=512, act="silu"),
+    "swiglu_bias_shared_ragged": dict(name="deepseek_v3_top8", T=300, d_model=128, d_ff=200,
+                                      E=8, k=2, has_bias=1, nonzero_bias=True, act="swiglu"),
+    "swiglu_top1_fused_combine": dict(name="switch_top1_cap", T=1000, d_model=128, d_ff=256,
+                                      E=16, k=1, renorm=1, act="swiglu"),
+    "swiglu_fp32_bias": dict(name="tiny_fp32_top2", T=300, d_model=64, d_ff=96, E=8, k=2,
+                             nonzero_bias=True, act="swiglu"),
+    "silu_fp32": dict(name="tiny_fp32_top2", T=200, d_model=64, d_ff=80, E=4, k=2, act="silu"),
 }
 
 
@@ -161,7 +171,8 @@ def test_full_workload_all_tokens(name):
     print(name, rep.summary())
 
 
-@pytest.mark.parametrize("name,nrows", [("mixtral_top2", 48), ("deepseek_v3_top8", 24)])
+@pytest.mark.parametrize("name,nrows", [("mixtral_top2", 48), ("deepseek_v3_top8", 24),
+                                        ("mixtral_swiglu_top2", 24)])
 def test_full_workload_sampled_tokens(name, nrows):
     """Routing, statistics and dispatch on every token; the layer output on a
     fixed sample of tokens (no capacity limit, so each token's output depends
