@@ -50,7 +50,8 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 GEMM_SOURCES = ["gemm_tc.cuh", "ptx_sm100.cuh", "groups.cuh"]
 # oracle rows (tokens whose FFN output the CPU baseline computes) per workload
 CPU_SAMPLE_ROWS = {"tiny_fp32_top2": 256, "switch_top1_cap": 4096, "mixtral_top2": 128,
-                   "deepseek_v3_top8": 16, "decode_zipf_top2": 64, "mixtral_swiglu_top2": 128}
+                   "deepseek_v3_top8": 16, "decode_zipf_top2": 64, "mixtral_swiglu_top2": 128,
+                   "switch_expert_choice": 4096}
 
 
 def parse():
@@ -174,14 +175,23 @@ def algorithmic_ffn(cfg, kept, elem):
 
 
 def kernel_launches_per_step(cfg) -> int:
-    """Kernels one moe_forward enqueues (see moe_api.cu): routing grid (plus the
-    W_g transpose and tensor-core router GEMM ahead of it for bf16 layers with
-    E > 64 or T > 512), permute, up-projection, down-projection, and the
-    combine unless a bf16 top-1 layer without shared experts folds it into
-    the down-projection."""
-    tc_router = cfg["dtype"] == "bf16" and (cfg["E"] > 64 or cfg["T"] > 512)
-    route = 3 if tc_router else 1
-    fused = cfg["dtype"] == "bf16" and cfg["k"] == 1 and cfg.get("n_shared", 0) == 0
+    """Kernels one moe_forward enqueues (see moe_api.cu).
+    Top-k routing: the routing grid, with the W_g transpose ahead of it for
+    bf16 layers with E > 64 or T > 512 - then either the tensor-core router
+    with the gating in its epilogue (E <= 16) or the router GEMM plus a gating
+    grid - the permute, the up- and down-projections, and the combine unless a
+    bf16 top-1 layer without shared experts folds it into the down-projection.
+    Expert Choice: (W_g transpose and router GEMM for bf16), the per-token
+    scores, the per-expert selection, the row gather, the two projections and
+    the combine."""
+    bf16 = cfg["dtype"] == "bf16"
+    if cfg.get("route") == "expert_choice":
+        return (2 if bf16 else 0) + 2 + 1 + 2 + 1
+    tc_router = bf16 and (cfg["E"] > 64 or cfg["T"] > 512)
+    fused_router = (tc_router and cfg["E"] <= 16
+                    and ((cfg["T"] + 127) // 128) * (cfg["E"] + 1) <= 257 * 512)
+    route = 2 if fused_router else (3 if tc_router else 1)
+    fused = bf16 and cfg["k"] == 1 and cfg.get("n_shared", 0) == 0
     return route + 1 + 2 + (0 if fused else 1)
 
 
@@ -228,14 +238,27 @@ def run_ours(args, rank, world, local_rank):
     # ---- the dominant kernel pair (grouped FFN) and the combine on the same
     # workspace state, each in its own graph, for the roofline and the split
     z = lambda shape, t: torch.empty(shape, dtype=t, device=dev)
+    ec = moe.expert_choice(cfg)
+    R = moe.routed_rows(cfg)
     o = dict(counts=z((E,), torch.int32), kept=z((E,), torch.int32),
              offsets=z((E + 1,), torch.int32), perm_token=z((T * k,), torch.int32),
-             slot_of=z((T * k,), torch.int32), x_perm=z((T * k, d), dt),
-             y_perm=z((T * k, d), dt), out=z((T, d), dt))
+             slot_of=z((T * k,), torch.int32), x_perm=z((R, d), dt),
+             y_perm=z((R, d), dt), out=z((T, d), dt))
     y_sh = z((S, T, d), dt) if S else None
     ws2 = moe.new_workspace(cfg, dev)
-    moe.permute(cfg, inp["x"], layer.topk_idx, o["counts"], o["kept"], o["offsets"],
-                o["perm_token"], o["slot_of"], o["x_perm"], ws2)
+    if ec:
+        # the slot table of the same selection (moe_forward keeps it in its workspace)
+        C = moe.expert_capacity(cfg)
+        o["ec_slot"] = z((E, T), torch.int32)
+        moe.route_expert_choice(cfg, inp["x"], inp["w_g"], z((E, C), torch.int32),
+                                z((E, C), torch.float32), o["ec_slot"], z((E,), torch.float32),
+                                z((E,), torch.float32), z((1,), torch.float32), ws2,
+                                logit_bias=inp.get("logit_bias"))
+        moe.permute_expert_choice(cfg, inp["x"], layer.topk_idx, o["offsets"], o["x_perm"])
+        o["kept"].fill_(C)
+    else:
+        moe.permute(cfg, inp["x"], layer.topk_idx, o["counts"], o["kept"], o["offsets"],
+                    o["perm_token"], o["slot_of"], o["x_perm"], ws2)
 
     def part_ffn():
         moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws2,
@@ -244,7 +267,11 @@ def run_ours(args, rank, world, local_rank):
                         y_shared=y_sh)
 
     def part_combine():
-        moe.combine(cfg, o["y_perm"], o["slot_of"], layer.topk_w, o["out"], y_shared=y_sh)
+        if ec:
+            moe.combine_expert_choice(cfg, o["y_perm"], o["ec_slot"], layer.topk_w, o["out"],
+                                      y_shared=y_sh)
+        else:
+            moe.combine(cfg, o["y_perm"], o["slot_of"], layer.topk_w, o["out"], y_shared=y_sh)
 
     part_ffn()
     part_combine()

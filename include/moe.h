@@ -15,6 +15,10 @@
  *            SwiGLU: (SiLU(v W1g^T + b1g) * (v W1u^T + b1u)) W2^T + b2
  *   f_i, P_i, aux = alpha * E * sum_i f_i P_i          (Switch load balance)
  *   z      = mean_t logsumexp_e(logits[t, e])^2        (router z-loss)
+ *   Expert Choice: C = min(max(floor(CF * T / E), min_capacity), T); expert e
+ *            takes the C tokens with the largest logits[t, e] (lower t first
+ *            on equal logits); y = sum over the experts e that took t of
+ *            p[t, e] * FFN_e(x_t) + shared, p = softmax over the experts
  *
  * Sources: "混合专家大模型MoE架构选型与部署实践教程" §五 (SparseMoEGate,
  * SimpleMoELayer); "[BEE-30064] 混合專家架構與服務", 專家路由工作原理 (routing
@@ -67,8 +71,11 @@ typedef enum {
 typedef enum {
   MOE_ROUTE_SOFTMAX_TOPK = 0,    /* softmax over E, top-k, renormalise if cfg.renorm */
   MOE_ROUTE_TOPK_SOFTMAX = 1,    /* top-k on logits, softmax over the k              */
-  MOE_ROUTE_BIASED_SOFTMAX = 2   /* select on softmax + select_bias; weights = unbiased
+  MOE_ROUTE_BIASED_SOFTMAX = 2,  /* select on softmax + select_bias; weights = unbiased
                                     softmax renormalised over the k                  */
+  MOE_ROUTE_EXPERT_CHOICE = 3    /* every expert takes its C tokens of largest logit;
+                                    weight = the token's softmax probability; needs
+                                    capacity_factor > 0; k is not used            */
 } moe_route_kind;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -201,6 +208,41 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
                        const float* topk_w, const void* y_shared, void* out,
                        moe_stream stream);
 
+/* Tokens per expert (host only): the capacity C of the configuration, or -1
+ * when the top-k routing has no capacity limit (capacity_factor <= 0).  Under
+ * MOE_ROUTE_EXPERT_CHOICE this is the number of tokens every expert takes. */
+moe_status moe_expert_capacity(const moe_config* cfg, int32_t* C);
+
+/* Expert Choice routing ("AI-Research-SKILLs MoE 训练实战…全指南" §4.2, "第7章
+ * Mixture of Experts" §7.2): the router logits transposed to (experts, tokens)
+ * and a top-C over the tokens of each expert, C = moe_expert_capacity().
+ * cfg->route must be MOE_ROUTE_EXPERT_CHOICE.
+ *   x [T,d] dtype; w_g [d,E] dtype; logit_bias [E] fp32 or NULL.
+ *   Outputs: logits [T,E] fp32 or NULL; ec_token [E,C] int32 (the tokens
+ *   expert e took, ascending); ec_w [E,C] fp32 (their gate weights p[t,e]);
+ *   ec_slot [E,T] int32 (row e*C + r of x_perm holding token t for expert e,
+ *   or -1); f [E] (= C/T with MOE_AUX_TOPK_COUNT), P [E], aux [1], z_loss [1]
+ *   or NULL as in moe_route. */
+moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const void* w_g,
+                                   const float* logit_bias, float* logits,
+                                   int32_t* ec_token, float* ec_w, int32_t* ec_slot,
+                                   float* f, float* P, float* aux, float* z_loss,
+                                   void* ws, size_t ws_bytes, moe_stream stream);
+
+/* Expert Choice dispatch: x_perm [E*C, d] with row e*C + r = x[ec_token[e,r]],
+ * and offsets [E+1] = e*C for moe_grouped_ffn. */
+moe_status moe_permute_expert_choice(const moe_config* cfg, const void* x,
+                                     const int32_t* ec_token, int32_t* offsets,
+                                     void* x_perm, moe_stream stream);
+
+/* Expert Choice combine: out[t] = sum over e ascending with ec_slot[e,t] >= 0
+ * of ec_w[ec_slot[e,t]] * y_perm[ec_slot[e,t]] + sum_s y_shared[s,t],
+ * accumulated in fp32 and stored once in dtype (0 plus the shared experts for
+ * a token no expert took). */
+moe_status moe_combine_expert_choice(const moe_config* cfg, const void* y_perm,
+                                     const int32_t* ec_slot, const float* ec_w,
+                                     const void* y_shared, void* out, moe_stream stream);
+
 /* The whole layer: route -> permute -> grouped FFN -> combine, all stream
  * ordered with no host synchronisation.  Intermediates live in `ws`.  For a
  * bf16 top-1 layer without shared experts the combine is folded into the
@@ -209,7 +251,9 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
  * step-by-step entry points do.
  *   Outputs: out [T,d] dtype; topk_idx [T,k]; topk_w [T,k]; counts [E];
  *   f [E]; P [E]; aux [1]; z_loss [1] (as in moe_route).  Any of topk_idx ..
- *   z_loss may be NULL; out may not. */
+ *   z_loss may be NULL; out may not.  Under MOE_ROUTE_EXPERT_CHOICE topk_idx
+ *   and topk_w receive ec_token [E,C] and ec_w [E,C] of
+ *   moe_route_expert_choice, counts[e] = C, and select_bias is not used. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
                        const float* logit_bias, const float* select_bias,
                        const void* w1, const void* b1, const void* w2, const void* b2,

@@ -205,12 +205,73 @@ def compare_output(cfg: dict, ref: om.ForwardResult, out_gpu: np.ndarray, rep: R
         assert mx <= TOL_BF16_MAX_ABS_RMS, f"bf16 max-abs/RMS {mx:.3e} > {TOL_BF16_MAX_ABS_RMS}"
 
 
+def compare_stats(cfg: dict, ref: om.ForwardResult, gpu: dict) -> None:
+    """f exact; P, aux and z_loss within their tolerances (no near-tie slack)."""
+    if "f" in gpu:
+        f_gpu = np.asarray(gpu["f"], np.float32)
+        assert np.array_equal(f_gpu, ref.f.astype(np.float32)), "f differs"
+    if "P" in gpu:
+        P = np.asarray(gpu["P"], np.float64)
+        err = np.abs(P - ref.P) / np.maximum(np.abs(ref.P), 1e-30)
+        assert err.max() <= TOL_P_REL, f"P relative error {err.max():.3e}"
+    if "aux" in gpu:
+        a = float(np.asarray(gpu["aux"]).reshape(-1)[0])
+        assert abs(a - ref.aux) <= TOL_AUX_REL * abs(ref.aux) + 1e-12, f"aux {a} vs {ref.aux}"
+    if gpu.get("z_loss") is not None:
+        z = float(np.asarray(gpu["z_loss"]).reshape(-1)[0])
+        zr = float(ref.extra["z_loss"])
+        assert abs(z - zr) <= TOL_Z_REL * abs(zr) + 1e-12, f"z_loss {z} vs {zr}"
+
+
+def check_layer_expert_choice(cfg: dict, inputs: dict, gpu: dict,
+                              rows: Optional[Sequence[int]] = None) -> Report:
+    """Expert Choice: each expert's taken tokens bit-exact, except experts
+    whose C-th and (C+1)-th largest logits are closer than NEAR_TIE.  For
+    those the device's set must still be a top-C up to that margin, and the
+    oracle is re-run with it.  ``gpu`` holds topk_idx / topk_w as [E, C]
+    token lists and weights, counts, f, P, aux, z_loss and out."""
+    rep = Report()
+    ref = run_oracle(cfg, inputs, rows=rows)
+    ec = ref.extra["ec"]
+    C, E = ec.C, cfg["E"]
+    tok = np.asarray(gpu["topk_idx"]).astype(np.int64).reshape(E, C)
+    rep.near_tie = [int(e) for e in np.nonzero(ec.margin < NEAR_TIE)[0]]
+    override = {}
+    for e in range(E):
+        if np.array_equal(tok[e], ec.tokens[e]):
+            continue
+        assert ec.margin[e] < NEAR_TIE, (
+            f"expert {e} took other tokens (margin {ec.margin[e]:.3e}): "
+            f"gpu-only {sorted(set(tok[e]) - set(ec.tokens[e]))[:5]} "
+            f"oracle-only {sorted(set(ec.tokens[e]) - set(tok[e]))[:5]}")
+        col = ref.logits[:, e]
+        kth = np.sort(col)[::-1][C - 1]
+        assert len(set(tok[e].tolist())) == C and np.all(np.diff(tok[e]) > 0)
+        assert col[tok[e]].min() >= kth - NEAR_TIE, f"expert {e}: not a top-C set"
+        override[e] = tok[e]
+    if override:
+        rep.overridden = sorted(override)
+        ref = run_oracle(cfg, inputs, rows=rows, idx_override=override)
+        ec = ref.extra["ec"]
+    if "topk_w" in gpu:
+        dw = np.abs(np.asarray(gpu["topk_w"], np.float64).reshape(E, C) - ec.w)
+        assert dw.size == 0 or dw.max() <= TOL_W_ABS, f"gate weights differ by {dw.max():.3e}"
+    if "counts" in gpu:
+        assert np.all(np.asarray(gpu["counts"]) == C), "counts must all be C"
+    compare_stats(cfg, ref, gpu)
+    if "out" in gpu:
+        compare_output(cfg, ref, gpu["out"], rep)
+    return rep
+
+
 def check_layer(cfg: dict, inputs: dict, gpu: dict, rows: Optional[Sequence[int]] = None
                 ) -> Report:
     """Full acceptance check of one device run against the oracle.
 
     ``gpu`` maps output names to numpy arrays: topk_idx, topk_w, counts, f, P,
     aux, out (and optionally kept, offsets, perm_token, slot_of)."""
+    if cfg.get("route") == om.ROUTE_EXPERT_CHOICE:
+        return check_layer_expert_choice(cfg, inputs, gpu, rows)
     rep = Report()
     ref = run_oracle(cfg, inputs, rows=rows)
     rep.near_tie, override = _near_tie_and_override(ref, np.asarray(gpu["topk_idx"]))

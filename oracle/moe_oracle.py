@@ -27,9 +27,13 @@ Sources (page title, then section / listing / formula):
   (shared experts always computed and added with weight one), §8.2 the
   capacity formula ``int((tokens / num_experts) * capacity_factor)``.
   §6.1 ``MixtralMoEBlock`` (experts Linear -> SiLU -> Linear without bias,
-  and the text naming SwiGLU as Mixtral's FFN activation).
+  and the text naming SwiGLU as Mixtral's FFN activation).  §4.2 Expert
+  Choice routing: the router's scores transposed to (experts, tokens) and a
+  top-k over the tokens of each expert, k = its capacity.
 * [CH7]    "第7章 Mixture of Experts": §7.1 MoE(x) = sum_i G(x)_i * E_i(x);
-  §7.2 ``top_k_gating`` (top-k on logits, softmax over the k); §7.3 shared +
+  §7.2 ``top_k_gating`` (top-k on logits, softmax over the k) and Expert
+  Choice (each expert takes its top-C tokens, so every expert processes the
+  same number; a token may be taken by several experts or by none); §7.3 shared +
   fine-grained experts; §7.4 the balance loss N * sum f_i p_i and capacity
   C = CF * n / N with ``int(...)``.
 
@@ -50,6 +54,7 @@ from scipy.special import erf, expit
 ROUTE_SOFTMAX_TOPK = "softmax_topk"      # [BAIDU] SparseMoEGate, [SKILLS] §3.1
 ROUTE_TOPK_SOFTMAX = "topk_softmax"      # [BEE] steps 2-3, [CH7] §7.2 top_k_gating
 ROUTE_BIASED_SOFTMAX = "biased_softmax"  # [SKILLS] §4.3 / §7.1 DeepSeek-V3 bias
+ROUTE_EXPERT_CHOICE = "expert_choice"    # [SKILLS] §4.2, [CH7] §7.2 Expert Choice (R19)
 AUX_TOPK_COUNT = "topk_count"            # [BAIDU] one-hot of the top-k, summed
 AUX_ARGMAX = "argmax"                    # [BEE] load_balance_loss, argmax routing
 ACT_GELU = "gelu"                        # [BAIDU] §五, [SKILLS] §3.1 nn.GELU()
@@ -240,6 +245,53 @@ def dispatch(idx: np.ndarray, E: int, C: Optional[int]) -> Dispatch:
 
 
 # --------------------------------------------------------------------------
+# Expert Choice.  [SKILLS] §4.2: expert_scores = router(x) transposed to
+# (experts, tokens), then topk over the tokens with k = the capacity per
+# expert; [CH7] §7.2: each expert takes the Top-C tokens most related to it.
+# --------------------------------------------------------------------------
+@dataclass
+class ExpertChoice:
+    C: int                  # tokens per expert
+    tokens: np.ndarray      # [E, C] int64 chosen tokens of each expert, ascending
+    w: np.ndarray           # [E, C] float64 gate weight p[token, e]
+    p: np.ndarray           # [T, E] float64 softmax of the logits over experts
+    margin: np.ndarray      # [E] C-th minus (C+1)-th largest logit of the expert
+
+
+def expert_choice_capacity(cfg: OracleConfig) -> int:
+    """C = the top-k capacity C of ``capacity`` (floor(CF * T / E), raised to
+    min_capacity), at most T.  Expert Choice needs CF > 0 (R19)."""
+    C = capacity(cfg)
+    if C is None:
+        raise ValueError("Expert Choice routing needs a capacity factor > 0")
+    return min(C, cfg.T)
+
+
+def expert_choice(logits: np.ndarray, C: int,
+                  override: Optional[dict] = None) -> ExpertChoice:
+    """Each expert e takes the C tokens with the largest logit l[t, e] of its
+    column, the lower token index first among equal logits (R4, R19).  The
+    gate weight of a chosen pair is the token's softmax probability over the
+    experts, p[t, e] (R19).  ``override`` maps an expert to the token set to
+    use instead (near ties, as for top-k)."""
+    l = np.asarray(logits, np.float64)
+    T, E = l.shape
+    p = softmax(l)
+    tokens = np.empty((E, C), np.int64)
+    margin = np.full(E, np.inf)
+    for e in range(E):
+        order = np.lexsort((np.arange(T), -l[:, e]))   # logit descending, then token
+        if 0 < C < T:
+            margin[e] = l[order[C - 1], e] - l[order[C], e]
+        chosen = order[:C]
+        if override is not None and e in override:
+            chosen = np.asarray(override[e], np.int64)
+        tokens[e] = np.sort(chosen)
+    w = p[tokens, np.arange(E)[:, None]]
+    return ExpertChoice(C=C, tokens=tokens, w=w, p=p, margin=margin)
+
+
+# --------------------------------------------------------------------------
 # Experts.  [BAIDU] nn.Sequential(Linear(d, d_ff), GELU(), Linear(d_ff, d));
 # [SKILLS] §3.1 the same with 4x width; Dropout of the [xdnf] Expert is the
 # identity in a forward/eval pass.
@@ -364,6 +416,8 @@ def moe_forward(cfg: OracleConfig, x: np.ndarray, w_g: np.ndarray,
     T = x.shape[0]
     assert T == cfg.T
     logits = router_logits(x, w_g, logit_bias)
+    if cfg.route == ROUTE_EXPERT_CHOICE:
+        return _expert_choice_forward(cfg, x, logits, experts, shared, rows, idx_override)
     g = gate(logits, cfg, select_bias, idx_override)
     C = capacity(cfg)
     disp = dispatch(g.idx, cfg.E, C)
@@ -393,3 +447,41 @@ def moe_forward(cfg: OracleConfig, x: np.ndarray, w_g: np.ndarray,
 
     return ForwardResult(logits=logits, gate=g, disp=disp, C=C, f=f, P=P,
                          aux=aux, rows=rows, out=out, extra={"z_loss": z})
+
+
+def _expert_choice_forward(cfg, x, logits, experts, shared, rows, override):
+    """The layer under Expert Choice routing:
+    MoE(x_t) = sum over experts e that chose t of p[t, e] * E_e(x_t)
+               + sum over shared s of S_s(x_t).
+    Statistics: every expert processes exactly C tokens, so with topk_count
+    f_e = C / T; P and aux as for top-k routing.  ``disp`` lists the experts'
+    rows in order (offsets e * C); its per-assignment fields are empty."""
+    T, E = logits.shape
+    C = expert_choice_capacity(cfg)
+    ec = expert_choice(logits, C, override)
+    counts = np.full(E, C, np.int64)
+    f, P, aux = load_balance(cfg, logits, ec.p, counts)
+    z = router_z_loss(logits)
+    empty = np.zeros(0, np.int64)
+    disp = Dispatch(counts=counts, kept=counts.copy(),
+                    offsets=np.arange(E + 1, dtype=np.int64) * C,
+                    perm_token=ec.tokens.reshape(-1).copy(), slot_of=empty, rank=empty)
+
+    rows = np.arange(T) if rows is None else np.asarray(rows, np.int64)
+    out = np.zeros((len(rows), cfg.d_model), np.float64)
+    x64_rows = np.asarray(x[rows], np.float64)
+    pos_of = {int(t): i for i, t in enumerate(rows)}
+    for e in range(E):
+        pick = [(pos_of[int(t)], j) for j, t in enumerate(ec.tokens[e]) if int(t) in pos_of]
+        if not pick:
+            continue
+        ii = np.array([a for a, _ in pick], np.int64)
+        jj = np.array([b for _, b in pick], np.int64)
+        w1, b1, w2, b2 = experts(e)
+        y = expert_ffn(x64_rows[ii], w1, b1, w2, b2, act=cfg.act)
+        np.add.at(out, ii, ec.w[e, jj][:, None] * y)
+    for s in range(cfg.n_shared):
+        w1, b1, w2, b2 = shared(s)
+        out += expert_ffn(x64_rows, w1, b1, w2, b2, act=cfg.act)
+    return ForwardResult(logits=logits, gate=None, disp=disp, C=C, f=f, P=P, aux=aux,
+                         rows=rows, out=out, extra={"z_loss": z, "ec": ec})

@@ -13,6 +13,7 @@
 
 #include "moe.h"
 #include "dispatch.cuh"
+#include "expert_choice.cuh"
 #include "gemm_tc.cuh"
 #include "groups.cuh"
 #include "route.cuh"
@@ -54,7 +55,7 @@ moe_status validate(const moe_config* c) {
   if (c->k < 1 || c->k > c->E || c->k > kMaxK) return MOE_ERR_INVALID_ARG;
   if (c->n_shared < 0 || c->n_shared > kMaxShared) return MOE_ERR_INVALID_ARG;
   if (c->min_capacity < 0) return MOE_ERR_INVALID_ARG;
-  if (c->route < MOE_ROUTE_SOFTMAX_TOPK || c->route > MOE_ROUTE_BIASED_SOFTMAX)
+  if (c->route < MOE_ROUTE_SOFTMAX_TOPK || c->route > MOE_ROUTE_EXPERT_CHOICE)
     return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->aux_f != MOE_AUX_TOPK_COUNT && c->aux_f != MOE_AUX_ARGMAX) return MOE_ERR_INVALID_ARG;
@@ -63,8 +64,12 @@ moe_status validate(const moe_config* c) {
   if (c->act < MOE_ACT_GELU || c->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha))
     return MOE_ERR_INVALID_ARG;
+  // Expert Choice needs a capacity: each expert takes C = floor(CF * T / E) tokens
+  if (c->route == MOE_ROUTE_EXPERT_CHOICE && !(c->capacity_factor > 0.f))
+    return MOE_ERR_INVALID_ARG;
   const int64_t Tk = static_cast<int64_t>(c->T) * c->k;
-  const int64_t rows_h = Tk + static_cast<int64_t>(c->n_shared) * c->T;
+  const int64_t rows_ec = static_cast<int64_t>(c->E) * c->T;   // E * C <= E * T
+  const int64_t rows_h = std::max(Tk, rows_ec) + static_cast<int64_t>(c->n_shared) * c->T;
   if (rows_h > (INT_MAX / 2)) return MOE_ERR_INVALID_ARG;
   // 16-byte rows for vector loads and TMA strides
   if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -79,6 +84,18 @@ int capacity_of(const moe_config& c) {
   return std::max(cap, c.min_capacity);
 }
 
+bool expert_choice(const moe_config& c) { return c.route == MOE_ROUTE_EXPERT_CHOICE; }
+
+// Tokens each expert takes under Expert Choice: the capacity, at most T.
+int ec_capacity(const moe_config& c) { return std::min(capacity_of(c), c.T); }
+
+// Expert-ordered rows the grouped FFN runs on: T*k assignments (top-k), or
+// E*C (Expert Choice).
+int64_t routed_rows(const moe_config& c) {
+  return expert_choice(c) ? static_cast<int64_t>(c.E) * ec_capacity(c)
+                          : static_cast<int64_t>(c.T) * c.k;
+}
+
 // bf16 routers over more than 64 experts or more tokens than the small-batch
 // router takes run on the tensor cores
 bool use_tc_router(const moe_config& c) {
@@ -88,9 +105,11 @@ bool use_tc_router(const moe_config& c) {
 struct Layout {
   size_t status, logits, wgT, crank, hist;
   size_t idx, w, counts, kept, offsets, perm_token, slot_of, f, P, aux;
+  size_t scoresT, tok_stats, ec_token, ec_w, ec_slot;   // Expert Choice
   size_t x_perm, H, Y, Ys, sk_part, total;
   int nb, E_pad;
-  bool tc_router;
+  bool tc_router;   // the top-k router runs on the tensor cores
+  bool tc_logits;   // the logits buffer and transposed W_g exist
 };
 
 Layout make_layout(const moe_config& c) {
@@ -99,7 +118,11 @@ Layout make_layout(const moe_config& c) {
   const size_t eb = elem_bytes(c);
   L.nb = route_blocks(c.T);
   L.E_pad = next_pow2_min16(c.E);
-  L.tc_router = use_tc_router(c);
+  L.tc_router = !expert_choice(c) && use_tc_router(c);
+  L.tc_logits = c.dtype == MOE_BF16 && (L.tc_router || expert_choice(c));
+  const bool ec = expert_choice(c);
+  const size_t C = ec ? static_cast<size_t>(ec_capacity(c)) : 0;
+  const size_t rows = static_cast<size_t>(routed_rows(c));
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -112,8 +135,8 @@ Layout make_layout(const moe_config& c) {
                                                          : kSmallRouteMaxT) * 4 <=
                     kHeaderBytes,
                 "per-block partials must fit the header");
-  L.logits = take(L.tc_router ? T * L.E_pad * 4 : 0);
-  L.wgT = take(L.tc_router ? static_cast<size_t>(L.E_pad) * d * 2 : 0);
+  L.logits = take(L.tc_logits ? T * L.E_pad * 4 : 0);
+  L.wgT = take(L.tc_logits ? static_cast<size_t>(L.E_pad) * d * 2 : 0);
   L.crank = take(T * k * 4);
   L.hist = take(static_cast<size_t>(chunk_stride(c.T)) * E * 4);
   L.idx = take(T * k * 4);
@@ -126,9 +149,14 @@ Layout make_layout(const moe_config& c) {
   L.f = take(E * 4);
   L.P = take(E * 4);
   L.aux = take(4);
-  L.x_perm = take(T * k * d * eb);
-  L.H = take((T * k + S * T) * F * eb);
-  L.Y = take(T * k * d * eb);
+  L.scoresT = take(ec ? E * T * 4 : 0);
+  L.tok_stats = take(ec ? 2 * T * 4 : 0);   // per-token softmax max, then sum
+  L.ec_token = take(E * C * 4);
+  L.ec_w = take(E * C * 4);
+  L.ec_slot = take(ec ? E * T * 4 : 0);
+  L.x_perm = take(rows * d * eb);
+  L.H = take((rows + S * T) * F * eb);
+  L.Y = take(rows * d * eb);
   L.Ys = take(S * T * d * eb);
   // stream-K partial tiles of the tensor-core FFN: one 128 x 256 fp32 slot per CTA
   L.sk_part = take(c.dtype == MOE_BF16 ? static_cast<size_t>(kMaxGemmCtas) * 128 * 256 * 4 : 0);
@@ -472,6 +500,29 @@ moe_status launch_route_tc_k(int km, const CUtensorMap& mx, const CUtensorMap& m
 
 // Router, gating, statistics and the dispatch ranking in one routing grid
 // (plus the tensor-core router GEMM ahead of it for wide or long batches).
+// logits [T, E_pad] fp32 in the workspace = x . W_g on the tensor cores, from
+// the transposed W_g already in the workspace.  Expert columns go in tiles of
+// at most 64: a wide router (E = 256) then spreads over four times as many
+// CTAs as row tiles.
+moe_status tc_logits_gemm(const moe_config& c, const Layout& L, void* ws, const void* x,
+                          cudaStream_t st) {
+  const int bn_r = std::min(L.E_pad, 64);
+  CUtensorMap ma, mb;
+  if (!map_a(&ma, x, c.d_model, c.T) ||
+      !map_b(&mb, at<__nv_bfloat16>(ws, L.wgT), c.d_model, L.E_pad, 1, bn_r))
+    return MOE_ERR_CUDA;
+  float* logits_ws = at<float>(ws, L.logits);
+  TcArgs ta{};
+  ta.gs = GroupSpec{nullptr, 1, c.T, 0, 0, 0, 0, 0, 0};
+  ta.N = L.E_pad;
+  ta.K = c.d_model;
+  ta.out = logits_ws;
+  ta.out1 = logits_ws;
+  ta.ldo = L.E_pad;
+  ta.err = at<int>(ws, L.status);
+  return launch_tc(EPI_F32, ma, ma, mb, mb, ta, bn_r, (c.T + 127) / 128 + 1, st);
+}
+
 moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* x,
                     const void* w_g, const float* lb, const float* sb, const RouteOut& o,
                     cudaStream_t st) {
@@ -521,22 +572,7 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
       if (L.E_pad == 32) return launch_route_tc_k<32>(km, mx, mw, grid, ra, st);
       return launch_route_tc_k<64>(km, mx, mw, grid, ra, st);
     }
-    // expert columns in tiles of at most 64: a wide router (E = 256) then
-    // spreads over four times as many CTAs as row tiles
-    const int bn_r = std::min(L.E_pad, 64);
-    CUtensorMap ma, mb;
-    if (!map_a(&ma, x, c.d_model, c.T) || !map_b(&mb, wgT, c.d_model, L.E_pad, 1, bn_r))
-      return MOE_ERR_CUDA;
-    TcArgs ta{};
-    ta.gs = GroupSpec{nullptr, 1, c.T, 0, 0, 0, 0, 0, 0};
-    ta.N = L.E_pad;
-    ta.K = c.d_model;
-    ta.out = logits_ws;
-    ta.out1 = logits_ws;
-    ta.ldo = L.E_pad;
-    ta.err = at<int>(ws, L.status);
-    s = launch_tc(EPI_F32, ma, ma, mb, mb, ta, bn_r, (c.T + 127) / 128 + 1, st);
-    if (s != MOE_OK) return s;
+    if ((s = tc_logits_gemm(c, L, ws, x, st)) != MOE_OK) return s;
     ra.logits_in = logits_ws;
     ra.ld_in = L.E_pad;
     if (c.E <= 32) return launch_gate<1>(km, nb, st, ra);
@@ -550,6 +586,120 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
   }
   // fp32 batches beyond the small-batch router (bf16 ones take the tensor cores)
   return launch_route_warp_e<float>(c, nb, st, ra, x, w_g);
+}
+
+// ---------------------------------------------------------------- Expert Choice
+struct EcOut {
+  float* logits;      // [T, E] or null
+  int32_t* ec_token;  // [E, C]
+  float* ec_w;        // [E, C]
+  int32_t* ec_slot;   // [E, T]
+  int32_t* offsets;   // [E + 1]
+  int32_t* counts;    // [E] or null
+  float *f, *P, *aux, *z;
+};
+
+int ec_scores_grid(const moe_config& c) {
+  return std::max(1, std::min((c.T + kRouteWarps - 1) / kRouteWarps, kRouteMaxBlocks));
+}
+
+template <typename TE, int EP>
+moe_status launch_ec_scores(int grid, const EcArgs& a, const void* x, const void* w_g,
+                            cudaStream_t st) {
+  constexpr int NPL = (EP + 31) / 32;
+  return launch_pdl(k_ec_scores<TE, EP, NPL>, dim3(grid), dim3(kRouteThreads), 0, st, a,
+                    static_cast<const TE*>(x), static_cast<const TE*>(w_g));
+}
+
+template <int NPL>
+moe_status launch_ec_scores_from_logits(int grid, const EcArgs& a, cudaStream_t st) {
+  return launch_pdl(k_ec_scores<__nv_bfloat16, 0, NPL>, dim3(grid), dim3(kRouteThreads), 0, st,
+                    a, static_cast<const __nv_bfloat16*>(nullptr),
+                    static_cast<const __nv_bfloat16*>(nullptr));
+}
+
+// Expert Choice routing: logits (tensor cores for bf16, CUDA cores for fp32),
+// per-token softmax statistics, then one block per expert selects its tokens.
+moe_status do_route_ec(const moe_config& c, const Layout& L, void* ws, const void* x,
+                       const void* w_g, const float* lb, const EcOut& o, cudaStream_t st) {
+  EcArgs a{};
+  a.T = c.T;
+  a.d = c.d_model;
+  a.E = c.E;
+  a.C = ec_capacity(c);
+  a.logit_bias = lb;
+  a.logits_out = o.logits;
+  a.scoresT = at<float>(ws, L.scoresT);
+  a.tok_max = at<float>(ws, L.tok_stats);
+  a.tok_sum = at<float>(ws, L.tok_stats) + c.T;
+  a.ec_token = o.ec_token;
+  a.ec_w = o.ec_w;
+  a.ec_slot = o.ec_slot;
+  a.offsets = o.offsets;
+  a.counts = o.counts;
+  a.done = at<unsigned int>(ws, L.status + kRouteCounterOffset);
+  const int grid = ec_scores_grid(c);
+  StatsArgs& sa = a.st;
+  sa.p_part = at<float>(ws, L.status + kPartOffset);
+  sa.nb = grid;
+  sa.a_tot = at<unsigned int>(ws, L.status + kArgmaxOffset);
+  sa.counts = nullptr;
+  sa.T = c.T;
+  sa.E = c.E;
+  sa.aux_f = c.aux_f;
+  sa.alpha = c.aux_alpha;
+  sa.f = o.f;
+  sa.P = o.P;
+  sa.aux = o.aux;
+  sa.z = o.z;
+  moe_status s;
+  if (c.dtype == MOE_BF16) {
+    dim3 tgrid((c.d_model + 31) / 32, (L.E_pad + 31) / 32);
+    if ((s = launch_pdl(k_transpose_wg, tgrid, dim3(32, 8), 0, st,
+                        static_cast<const __nv_bfloat16*>(w_g), c.d_model, c.E, L.E_pad,
+                        at<__nv_bfloat16>(ws, L.wgT))) != MOE_OK)
+      return s;
+    if ((s = tc_logits_gemm(c, L, ws, x, st)) != MOE_OK) return s;
+    a.logits_in = at<float>(ws, L.logits);
+    a.ld_in = L.E_pad;
+    if (c.E <= 32) s = launch_ec_scores_from_logits<1>(grid, a, st);
+    else if (c.E <= 64) s = launch_ec_scores_from_logits<2>(grid, a, st);
+    else if (c.E <= 128) s = launch_ec_scores_from_logits<4>(grid, a, st);
+    else s = launch_ec_scores_from_logits<8>(grid, a, st);
+  } else if (c.E <= 16) {
+    s = launch_ec_scores<float, 16>(grid, a, x, w_g, st);
+  } else if (c.E <= 32) {
+    s = launch_ec_scores<float, 32>(grid, a, x, w_g, st);
+  } else {
+    s = launch_ec_scores<float, 64>(grid, a, x, w_g, st);
+  }
+  if (s != MOE_OK) return s;
+  return launch_pdl(k_ec_select, dim3(c.E), dim3(kEcThreads), 0, st, a);
+}
+
+moe_status do_permute_ec(const moe_config& c, const void* x, const int32_t* ec_token,
+                         int32_t* offsets, void* x_perm, cudaStream_t st) {
+  const int C = ec_capacity(c);
+  const int rows = c.E * C;
+  const int grid = std::max(1, std::min((rows + 7) / 8, num_sms() * 8));
+  return launch_pdl(k_ec_gather, dim3(grid), dim3(256), 0, st, ec_token, rows,
+                    static_cast<int>(c.d_model * elem_bytes(c)), C, c.E,
+                    static_cast<const uint8_t*>(x), static_cast<uint8_t*>(x_perm), offsets);
+}
+
+moe_status do_combine_ec(const moe_config& c, const void* y_perm, const int32_t* ec_slot,
+                         const float* ec_w, const void* y_shared, void* out, cudaStream_t st) {
+  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
+  const int S = y_shared ? c.n_shared : 0;
+  if (c.dtype == MOE_BF16)
+    return launch_pdl(k_ec_combine<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(y_perm), ec_slot, ec_w,
+                      static_cast<const __nv_bfloat16*>(y_shared), S, c.T, c.E, c.d_model,
+                      static_cast<__nv_bfloat16*>(out));
+  return launch_pdl(k_ec_combine<float>, dim3(grid), dim3(256), 0, st,
+                    static_cast<const float*>(y_perm), ec_slot, ec_w,
+                    static_cast<const float*>(y_shared), S, c.T, c.E, c.d_model,
+                    static_cast<float*>(out));
 }
 
 // Slot resolution and row gather from the ranks a routing or ranking grid
@@ -649,7 +799,7 @@ struct FfnScatter {
 
 moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& in, void* y_perm,
                   void* y_shared, cudaStream_t st, const FfnScatter* scatter = nullptr) {
-  const int64_t T = c.T, Tk = static_cast<int64_t>(c.T) * c.k, S = c.n_shared;
+  const int64_t T = c.T, Tk = routed_rows(c), S = c.n_shared;
   const int d = c.d_model, F = c.d_ff;
   void* H = at<uint8_t>(ws, L.H);
   const size_t eb = elem_bytes(c);
@@ -833,6 +983,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
   const moe_config& c = *cfg;
   const Layout L = make_layout(c);
   if ((s = check_ws(c, ws, ws_bytes, L)) != MOE_OK) return s;
+  if (expert_choice(c)) return MOE_ERR_INVALID_ARG;   // moe_route_expert_choice
   if (!f || !P || !aux) return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);
   if (c.T == 0) {
@@ -855,6 +1006,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   const moe_config& c = *cfg;
   const Layout L = make_layout(c);
   if ((s = check_ws(c, ws, ws_bytes, L)) != MOE_OK) return s;
+  if (expert_choice(c)) return MOE_ERR_INVALID_ARG;   // moe_permute_expert_choice
   if (!counts || !kept || !offsets) return MOE_ERR_INVALID_ARG;
   auto st = static_cast<cudaStream_t>(stream);
   if (c.T == 0) return zero_stats(c, counts, nullptr, nullptr, nullptr, offsets, kept, st);
@@ -874,6 +1026,7 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(c.T) * c.k > kNoallocAssignments ||
       static_cast<int64_t>(chunk_stride(c.T)) * c.E > kNoallocChunkCounts)
     return MOE_ERR_UNSUPPORTED;
@@ -914,6 +1067,7 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
   moe_status s = validate(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
+  if (expert_choice(c)) return MOE_ERR_INVALID_ARG;   // moe_combine_expert_choice
   if (c.T == 0) return MOE_OK;
   if (!y_perm || !slot_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
@@ -948,6 +1102,25 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   if (c.has_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && (!ws1 || !ws2)) return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && c.has_bias && (!wsb1 || !wsb2)) return MOE_ERR_INVALID_ARG;
+  void* Y = at<uint8_t>(ws, L.Y);
+  void* Ys = at<uint8_t>(ws, L.Ys);
+
+  if (expert_choice(c)) {
+    // topk_idx / topk_w carry the [E, C] taken tokens and their weights
+    int32_t* tok = topk_idx ? topk_idx : at<int32_t>(ws, L.ec_token);
+    float* ew = topk_w ? topk_w : at<float>(ws, L.ec_w);
+    int32_t* slot = at<int32_t>(ws, L.ec_slot);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    void* x_perm = at<uint8_t>(ws, L.x_perm);
+    if ((s = do_route_ec(c, L, ws, x, w_g, logit_bias,
+                         EcOut{nullptr, tok, ew, slot, offsets, cnt, fo, Po, ao, z_loss}, st)) !=
+        MOE_OK)
+      return s;
+    if ((s = do_permute_ec(c, x, tok, offsets, x_perm, st)) != MOE_OK) return s;
+    FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
+    if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
+    return do_combine_ec(c, Y, slot, ew, c.n_shared > 0 ? Ys : nullptr, out, st);
+  }
 
   int32_t* kept = at<int32_t>(ws, L.kept);
   int32_t* offsets = at<int32_t>(ws, L.offsets);
@@ -980,8 +1153,6 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
                           offsets, perm_token, slot_of, x, x_perm, st,
                           fused_combine ? out : nullptr, sa)) != MOE_OK)
     return s;
-  void* Y = at<uint8_t>(ws, L.Y);
-  void* Ys = at<uint8_t>(ws, L.Ys);
   FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
   if (fused_combine) {
     const FfnScatter sc{out, perm_token, w};
@@ -989,6 +1160,67 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   }
   if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
   return do_combine(c, Y, slot_of, w, c.n_shared > 0 ? Ys : nullptr, out, st);
+}
+
+moe_status moe_expert_capacity(const moe_config* cfg, int32_t* C) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  if (!C) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = *cfg;
+  *C = expert_choice(c) ? ec_capacity(c) : (c.capacity_factor > 0.f ? capacity_of(c) : -1);
+  return MOE_OK;
+}
+
+moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const void* w_g,
+                                   const float* logit_bias, float* logits, int32_t* ec_token,
+                                   float* ec_w, int32_t* ec_slot, float* f, float* P, float* aux,
+                                   float* z_loss, void* ws, size_t ws_bytes, moe_stream stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(c);
+  if ((s = check_ws(c, ws, ws_bytes, L)) != MOE_OK) return s;
+  if (!f || !P || !aux) return MOE_ERR_INVALID_ARG;
+  auto st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) {
+    if (z_loss && cudaMemsetAsync(z_loss, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return zero_stats(c, nullptr, f, P, aux, nullptr, nullptr, st);
+  }
+  if (!x || !w_g || !ec_slot) return MOE_ERR_INVALID_ARG;
+  if (ec_capacity(c) > 0 && (!ec_token || !ec_w)) return MOE_ERR_INVALID_ARG;
+  return do_route_ec(c, L, ws, x, w_g, logit_bias,
+                     EcOut{logits, ec_token, ec_w, ec_slot, at<int32_t>(ws, L.offsets), nullptr,
+                           f, P, aux, z_loss},
+                     st);
+}
+
+moe_status moe_permute_expert_choice(const moe_config* cfg, const void* x,
+                                     const int32_t* ec_token, int32_t* offsets, void* x_perm,
+                                     moe_stream stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  auto st = static_cast<cudaStream_t>(stream);
+  if (ec_capacity(c) > 0 && (!x || !ec_token || !x_perm)) return MOE_ERR_INVALID_ARG;
+  return do_permute_ec(c, x, ec_token, offsets, x_perm, st);
+}
+
+moe_status moe_combine_expert_choice(const moe_config* cfg, const void* y_perm,
+                                     const int32_t* ec_slot, const float* ec_w,
+                                     const void* y_shared, void* out, moe_stream stream) {
+  moe_status s = validate(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!expert_choice(c)) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  if (!ec_slot || !out) return MOE_ERR_INVALID_ARG;
+  if (ec_capacity(c) > 0 && (!y_perm || !ec_w)) return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+  return do_combine_ec(c, y_perm, ec_slot, ec_w, c.n_shared > 0 ? y_shared : nullptr, out,
+                       static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_check_status(void* ws, moe_stream stream) {

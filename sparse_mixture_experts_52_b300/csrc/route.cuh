@@ -602,9 +602,41 @@ __global__ void __launch_bounds__(kRouteThreads) k_gate(const RouteArgs a) {
   route_block_tail<NPL, KMAX>(a, st);
 }
 
-// Fused router + gating on the CUDA cores for E <= EP <= 64: lane l sums the
-// products of d-indices l, l+32, ... for all experts (fp32 FMA), a butterfly
-// all-reduce completes the E logits, then the token is gated in registers.
+// Router logits of one token on the CUDA cores for E <= EP <= 64: lane l sums
+// the products of d-indices l, l+32, ... for all experts (fp32 FMA), a
+// butterfly all-reduce completes the E sums; l[i] is the logit of expert
+// lane + 32*i plus lb[i].
+template <typename TE, int EP>
+__device__ __forceinline__ void warp_logits(const TE* __restrict__ xr, const TE* __restrict__ w_g,
+                                            int d, int E, int lane,
+                                            const float (&lb)[(EP + 31) / 32],
+                                            float (&l)[(EP + 31) / 32]) {
+  constexpr int NPL = (EP + 31) / 32;
+  float acc[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int i = lane; i < d; i += 32) {
+    const float xv = to_f32<TE>(xr[i]);
+    const TE* wr = w_g + static_cast<int64_t>(i) * E;
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E) acc[e] = fmaf(xv, to_f32<TE>(wr[e]), acc[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    float v = 0.f;
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e == lane + 32 * i) v = acc[e];
+    l[i] = v + lb[i];
+  }
+}
+
+// Fused router + gating on the CUDA cores for E <= EP <= 64: the logits of
+// each token (warp_logits), then the token is gated in registers.
 template <typename TE, int EP, int KMAX>
 __global__ void __launch_bounds__(kRouteThreads)
 k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__ w_g) {
@@ -620,28 +652,10 @@ k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__
   const int t0 = blockIdx.x * a.dp.cpb * kChunk;
   const int t1 = min(t0 + a.dp.cpb * kChunk, a.T);
   for (int t = t0 + warp; t < t1; t += kRouteWarps) {
-    float acc[EP];
-#pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = 0.f;
-    const TE* xr = x + static_cast<int64_t>(t) * d;
-#pragma unroll 4
-    for (int i = lane; i < d; i += 32) {
-      const float xv = to_f32<TE>(xr[i]);
-      const TE* wr = w_g + static_cast<int64_t>(i) * E;
-#pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e < E) acc[e] = fmaf(xv, to_f32<TE>(wr[e]), acc[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);
     float l[NPL];
+    warp_logits<TE, EP>(x + static_cast<int64_t>(t) * d, w_g, d, E, lane, lb, l);
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      float v = 0.f;
-#pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e == lane + 32 * i) v = acc[e];
-      l[i] = v + lb[i];
       const int e = lane + 32 * i;
       if (a.logits_out && e < E) a.logits_out[static_cast<int64_t>(t) * E + e] = l[i];
     }

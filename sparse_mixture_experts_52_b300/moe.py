@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
-ROUTES = {"softmax_topk": 0, "topk_softmax": 1, "biased_softmax": 2}
+ROUTES = {"softmax_topk": 0, "topk_softmax": 1, "biased_softmax": 2, "expert_choice": 3}
 DTYPES = {"f32": 0, "bf16": 1}
 AUX_F = {"topk_count": 0, "argmax": 1}
 ACTS = {"gelu": 0, "silu": 1, "swiglu": 2}
@@ -87,6 +87,11 @@ _SIGNATURES = {
     "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                     _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_check_status": [_P, _P],
+    "moe_expert_capacity": [_CFG, ctypes.POINTER(ctypes.c_int32)],
+    "moe_route_expert_choice": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                ctypes.c_size_t, _P],
+    "moe_permute_expert_choice": [_CFG, _P, _P, _P, _P, _P],
+    "moe_combine_expert_choice": [_CFG, _P, _P, _P, _P, _P, _P],
 }
 
 
@@ -158,6 +163,23 @@ def new_workspace(cfg: dict, device="cuda", stream=None) -> torch.Tensor:
 
 def check_status(ws: torch.Tensor, stream=None) -> None:
     _call("moe_check_status", _p(ws), _stream(stream))
+
+
+def expert_choice(cfg: dict) -> bool:
+    return cfg.get("route") in ("expert_choice", ROUTES["expert_choice"])
+
+
+def expert_capacity(cfg: dict) -> int:
+    """C of the configuration (tokens per expert under Expert Choice), or -1
+    for top-k routing without a capacity limit."""
+    c = ctypes.c_int32(0)
+    _call("moe_expert_capacity", ctypes.byref(make_config(cfg)), ctypes.byref(c))
+    return int(c.value)
+
+
+def routed_rows(cfg: dict) -> int:
+    """Expert-ordered rows of x_perm / y_perm: T*k, or E*C under Expert Choice."""
+    return cfg["E"] * expert_capacity(cfg) if expert_choice(cfg) else cfg["T"] * cfg["k"]
 
 
 # ------------------------------------------------------------------ steps
@@ -236,13 +258,14 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
                         cfg.get("n_shared", 0))
     dt = TORCH_DTYPES[cfg["dtype"]]
     F1 = w1_rows(cfg)
-    _want(x_perm, "x_perm", (T * k, d), dt)
+    R = routed_rows(cfg)
+    _want(x_perm, "x_perm", (R, d), dt)
     _want(offsets, "offsets", (E + 1,), torch.int32)
     _want(w1, "w1", (E, F1, d), dt)
     _want(w2, "w2", (E, d, F), dt)
     _want(b1, "b1", (E, F1), dt, allow_none=not cfg.get("has_bias", 0))
     _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
-    _want(y_perm, "y_perm", (T * k, d), dt)
+    _want(y_perm, "y_perm", (R, d), dt)
     if S:
         _want(x, "x", (T, d), dt)
         _want(ws1, "ws1", (S, F1, d), dt)
@@ -252,6 +275,53 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
     _call("moe_grouped_ffn", ctypes.byref(make_config(cfg)), _p(x_perm), _p(offsets), _p(w1),
           _p(b1), _p(w2), _p(b2), _p(x), _p(ws1), _p(wsb1), _p(ws2), _p(wsb2), _p(y_perm),
           _p(y_shared), _p(ws), ws.numel(), _stream(stream))
+
+
+def route_expert_choice(cfg, x, w_g, ec_token, ec_w, ec_slot, f, P, aux, ws, logit_bias=None,
+                        logits=None, z_loss=None, stream=None):
+    T, d, E = cfg["T"], cfg["d_model"], cfg["E"]
+    C = expert_capacity(cfg)
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x, "x", (T, d), dt)
+    _want(w_g, "w_g", (d, E), dt)
+    _want(ec_token, "ec_token", (E, C), torch.int32)
+    _want(ec_w, "ec_w", (E, C), torch.float32)
+    _want(ec_slot, "ec_slot", (E, T), torch.int32)
+    for n, t in (("f", f), ("P", P)):
+        _want(t, n, (E,), torch.float32)
+    _want(aux, "aux", (1,), torch.float32)
+    _want(logit_bias, "logit_bias", (E,), torch.float32, allow_none=True)
+    _want(logits, "logits", (T, E), torch.float32, allow_none=True)
+    _want(z_loss, "z_loss", (1,), torch.float32, allow_none=True)
+    _call("moe_route_expert_choice", ctypes.byref(make_config(cfg)), _p(x), _p(w_g),
+          _p(logit_bias), _p(logits), _p(ec_token), _p(ec_w), _p(ec_slot), _p(f), _p(P),
+          _p(aux), _p(z_loss), _p(ws), ws.numel(), _stream(stream))
+
+
+def permute_expert_choice(cfg, x, ec_token, offsets, x_perm, stream=None):
+    T, d, E = cfg["T"], cfg["d_model"], cfg["E"]
+    C = expert_capacity(cfg)
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(x, "x", (T, d), dt)
+    _want(ec_token, "ec_token", (E, C), torch.int32)
+    _want(offsets, "offsets", (E + 1,), torch.int32)
+    _want(x_perm, "x_perm", (E * C, d), dt)
+    _call("moe_permute_expert_choice", ctypes.byref(make_config(cfg)), _p(x), _p(ec_token),
+          _p(offsets), _p(x_perm), _stream(stream))
+
+
+def combine_expert_choice(cfg, y_perm, ec_slot, ec_w, out, y_shared=None, stream=None):
+    T, d, E, S = cfg["T"], cfg["d_model"], cfg["E"], cfg.get("n_shared", 0)
+    C = expert_capacity(cfg)
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    _want(y_perm, "y_perm", (E * C, d), dt)
+    _want(ec_slot, "ec_slot", (E, T), torch.int32)
+    _want(ec_w, "ec_w", (E, C), torch.float32)
+    _want(out, "out", (T, d), dt)
+    if S:
+        _want(y_shared, "y_shared", (S, T, d), dt)
+    _call("moe_combine_expert_choice", ctypes.byref(make_config(cfg)), _p(y_perm), _p(ec_slot),
+          _p(ec_w), _p(y_shared), _p(out), _stream(stream))
 
 
 def combine(cfg, y_perm, slot_of, topk_w, out, y_shared=None, stream=None):
@@ -281,8 +351,10 @@ def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None,
     _want(w2, "w2", (E, d, F), dt)
     _want(b1, "b1", (E, F1), dt, allow_none=True)
     _want(out, "out", (T, d), dt)
-    _want(topk_idx, "topk_idx", (T, k), torch.int32, allow_none=True)
-    _want(topk_w, "topk_w", (T, k), torch.float32, allow_none=True)
+    # under Expert Choice topk_idx / topk_w carry the [E, C] taken tokens and weights
+    sel = (E, expert_capacity(cfg)) if expert_choice(cfg) else (T, k)
+    _want(topk_idx, "topk_idx", sel, torch.int32, allow_none=True)
+    _want(topk_w, "topk_w", sel, torch.float32, allow_none=True)
     _want(counts, "counts", (E,), torch.int32, allow_none=True)
     for n, t in (("f", f), ("P", P)):
         _want(t, n, (E,), torch.float32, allow_none=True)
@@ -314,8 +386,10 @@ class MoELayer:
         T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
         dt = TORCH_DTYPES[cfg["dtype"]]
         self.out = torch.empty((T, d), dtype=dt, device=self.device)
-        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=self.device)
-        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        # Expert Choice: the [E, C] taken tokens and their weights instead
+        sel = (E, expert_capacity(cfg)) if expert_choice(cfg) else (T, k)
+        self.topk_idx = torch.empty(sel, dtype=torch.int32, device=self.device)
+        self.topk_w = torch.empty(sel, dtype=torch.float32, device=self.device)
         self.counts = torch.empty((E,), dtype=torch.int32, device=self.device)
         self.f = torch.empty((E,), dtype=torch.float32, device=self.device)
         self.P = torch.empty((E,), dtype=torch.float32, device=self.device)

@@ -64,6 +64,11 @@ WORKLOADS = {
 # FFN (its W1 holds the gate and up projections: 2 x 14336 rows).
 WORKLOADS["mixtral_swiglu_top2"] = dict(WORKLOADS["mixtral_top2"], act="swiglu")
 
+# The Switch shape under Expert Choice routing: each of the 64 experts takes
+# its C = floor(2.0 * 4096 / 64) = 128 highest-scoring tokens.
+WORKLOADS["switch_expert_choice"] = dict(WORKLOADS["switch_top1_cap"], route="expert_choice",
+                                         capacity_factor=2.0, aux_f="topk_count")
+
 LAYER_KEYS = ("T", "d_model", "d_ff", "E", "k", "n_shared", "capacity_factor",
               "min_capacity", "route", "renorm", "dtype", "has_bias",
               "aux_alpha", "aux_f", "act")

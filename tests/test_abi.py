@@ -122,3 +122,44 @@ def test_null_required_pointers_rejected(lib):
     assert s == 1
     s = lib.moe_combine(ctypes.byref(c), None, 1, 1, None, 1, None)
     assert s == 1
+
+
+def test_expert_choice_host_checks(lib):
+    """Expert Choice needs a capacity; the top-k and Expert Choice entry points
+    refuse each other's configurations; moe_expert_capacity gives C."""
+    ec = synth.workload("switch_expert_choice")
+    assert moe.expert_capacity(ec) == 128                       # floor(2.0 * 4096 / 64)
+    assert moe.expert_capacity(dict(ec, capacity_factor=100.0)) == 4096   # at most T
+    assert moe.expert_capacity(dict(ec, capacity_factor=0.001, min_capacity=7)) == 7
+    assert moe.expert_capacity(synth.workload("switch_top1_cap")) == 80
+    assert moe.expert_capacity(synth.workload("mixtral_top2")) == -1   # no limit
+    n = ctypes.c_size_t(0)
+    bad = moe.make_config(dict(ec, capacity_factor=0.0))
+    assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+    c = moe.make_config(ec)
+    big = moe.workspace_size(ec)
+    # top-k entry points refuse an Expert Choice configuration (nothing enqueued)
+    s = lib.moe_route(ctypes.byref(c), 1, 1, None, None, None, 1, 1, 1, 1, 1, None, 256, big,
+                      None)
+    assert s == 1
+    s = lib.moe_combine(ctypes.byref(c), 1, 1, 1, None, 1, None)
+    assert s == 1
+    # and the Expert Choice ones a top-k configuration
+    tk = moe.make_config(synth.workload("switch_top1_cap"))
+    s = lib.moe_route_expert_choice(ctypes.byref(tk), 1, 1, None, None, 1, 1, 1, 1, 1, 1, None,
+                                    256, big, None)
+    assert s == 1
+    s = lib.moe_combine_expert_choice(ctypes.byref(tk), 1, 1, 1, None, 1, None)
+    assert s == 1
+    # missing slot table
+    s = lib.moe_route_expert_choice(ctypes.byref(c), 1, 1, None, None, 1, 1, None, 1, 1, 1, None,
+                                    256, big, None)
+    assert s == 1
+
+
+def test_expert_choice_workspace_holds_its_rows(lib):
+    cfg = synth.workload("switch_expert_choice")
+    T, d, F, E = cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"]
+    rows = E * moe.expert_capacity(cfg)
+    # x_perm + H + Y for the E*C expert rows, plus the [E, T] logits and slot table
+    assert moe.workspace_size(cfg) >= rows * (2 * d + F) * 2 + 2 * E * T * 4

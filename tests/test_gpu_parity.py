@@ -307,3 +307,112 @@ def test_out_of_range_expert_index_is_dropped_and_reported():
     assert torch.equal(o["counts"].cpu(), want.to(torch.int32))
     assert int(o["offsets"][-1]) == T * k - 2
     assert int((slot >= 0).sum()) == T * k - 2
+
+
+# ---------------------------------------------------------------- Expert Choice
+def run_steps_ec(cfg, inp):
+    """route -> permute -> grouped_ffn -> combine through the Expert Choice
+    entry points."""
+    T, d, E, S = cfg["T"], cfg["d_model"], cfg["E"], cfg.get("n_shared", 0)
+    C = moe.expert_capacity(cfg)
+    dt = moe.TORCH_DTYPES[cfg["dtype"]]
+    ws = moe.new_workspace(cfg, DEV)
+    z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
+    o = dict(logits=z((T, E), torch.float32), topk_idx=z((E, C), torch.int32),
+             topk_w=z((E, C), torch.float32), ec_slot=z((E, T), torch.int32),
+             f=z((E,), torch.float32), P=z((E,), torch.float32), aux=z((1,), torch.float32),
+             z_loss=z((1,), torch.float32), offsets=z((E + 1,), torch.int32),
+             x_perm=z((E * C, d), dt), y_perm=z((E * C, d), dt), out=z((T, d), dt))
+    o["y_shared"] = z((S, T, d), dt) if S else None
+    moe.route_expert_choice(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["ec_slot"],
+                            o["f"], o["P"], o["aux"], ws, logit_bias=inp.get("logit_bias"),
+                            logits=o["logits"], z_loss=o["z_loss"])
+    moe.permute_expert_choice(cfg, inp["x"], o["topk_idx"], o["offsets"], o["x_perm"])
+    moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws,
+                    b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
+                    wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
+                    y_shared=o["y_shared"])
+    moe.combine_expert_choice(cfg, o["y_perm"], o["ec_slot"], o["topk_w"], o["out"],
+                              y_shared=o["y_shared"])
+    moe.check_status(ws)
+    return {kk: (v if kk in ("x_perm", "y_perm", "y_shared") else _np(v))
+            for kk, v in o.items() if v is not None}
+
+
+def check_steps_ec(cfg, inp, st, fw):
+    """Step-wise Expert Choice path: the same selection, slot table, rows and
+    output as moe_forward (same kernels, same order), and the slot table is
+    the inverse of the token lists."""
+    E, T = cfg["E"], cfg["T"]
+    C = moe.expert_capacity(cfg)
+    assert np.array_equal(st["topk_idx"], fw["topk_idx"])
+    assert np.array_equal(st["topk_w"], fw["topk_w"])
+    assert np.array_equal(st["offsets"], np.arange(E + 1) * C)
+    want = np.full((E, T), -1, np.int64)
+    for e in range(E):
+        want[e, st["topk_idx"][e]] = e * C + np.arange(C)
+    assert np.array_equal(st["ec_slot"], want), "slot table is not the inverse of the lists"
+    xp = st["x_perm"]
+    assert torch.equal(xp, inp["x"][torch.as_tensor(st["topk_idx"].reshape(-1), device=DEV).long()])
+    assert np.array_equal(st["out"], fw["out"]), "steps and forward differ"
+    for k in ("f", "P", "aux", "z_loss"):
+        assert np.array_equal(st[k], fw[k]), k
+
+
+EC_SMALL = {
+    "ec_bf16_ragged": dict(name="switch_expert_choice", T=1000, d_model=128, d_ff=256, E=16),
+    "ec_fp32_bias": dict(name="tiny_fp32_top2", T=300, d_model=64, d_ff=96, E=8,
+                         route="expert_choice", capacity_factor=1.5, nonzero_bias=True),
+    "ec_shared_e64_swiglu": dict(name="deepseek_v3_top8", T=600, d_model=128, d_ff=128, E=64,
+                                 route="expert_choice", capacity_factor=4.0, act="swiglu",
+                                 select_bias_std=0.0),
+    "ec_argmax_f_min_capacity": dict(name="switch_expert_choice", T=256, d_model=64, d_ff=64,
+                                     E=8, capacity_factor=0.01, min_capacity=5,
+                                     aux_f="argmax"),
+    "ec_every_token": dict(name="switch_expert_choice", T=200, d_model=64, d_ff=64, E=4,
+                           capacity_factor=4.0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EC_SMALL))
+def test_expert_choice_small(case):
+    cfg, inp = _case(EC_SMALL[case])
+    fw = run_forward(cfg, inp)
+    rep = compare.check_layer(cfg, inp, fw)
+    st = run_steps_ec(cfg, inp)
+    check_steps_ec(cfg, inp, st, fw)
+    C = moe.expert_capacity(cfg)
+    assert fw["topk_idx"].shape == (cfg["E"], C)
+    print(case, "C =", C, rep.summary())
+
+
+def test_expert_choice_ties_and_empty_capacity():
+    """W_g = 0: every logit is 0, so every expert takes tokens 0..C-1 with
+    weight 1/E.  A capacity of 0 takes nothing: the output is the shared
+    expert alone."""
+    cfg = synth.workload("switch_expert_choice", T=300, d_model=64, d_ff=64, E=8,
+                         capacity_factor=1.0)
+    inp = synth.make_inputs(cfg, device=DEV)
+    inp["w_g"].zero_()
+    fw = run_forward(cfg, inp)
+    C = moe.expert_capacity(cfg)
+    assert C == 37
+    assert np.array_equal(fw["topk_idx"], np.tile(np.arange(C), (8, 1)))
+    assert np.all(fw["topk_w"] == np.float32(1 / 8))
+    compare.check_layer(cfg, inp, fw)
+    cfg = synth.workload("switch_expert_choice", T=100, d_model=64, d_ff=64, E=8,
+                         capacity_factor=0.05, n_shared=1)
+    inp = synth.make_inputs(cfg, device=DEV)
+    assert moe.expert_capacity(cfg) == 0
+    fw = run_forward(cfg, inp)
+    assert np.all(fw["counts"] == 0)
+    compare.check_layer(cfg, inp, fw)
+
+
+def test_expert_choice_full_workload():
+    cfg = synth.workload("switch_expert_choice")
+    inp = synth.make_inputs(cfg, device=DEV)
+    fw = run_forward(cfg, inp)
+    rep = compare.check_layer(cfg, inp, fw)
+    assert moe.expert_capacity(cfg) == 128
+    print("switch_expert_choice", rep.summary())

@@ -551,6 +551,87 @@ def test_router_z_loss():
     check_router_z_loss()
 
 
+# ---------------------------------------------------------------- Expert Choice
+def _ec_brute(col, C):
+    """Among all C-subsets of the tokens, the one with the largest logit sum,
+    the lexicographically smallest on equal sums (the lower tokens win ties)."""
+    best = None
+    for sub in itertools.combinations(range(len(col)), C):
+        key = (Fraction(0) + sum(Fraction(float(col[t])) for t in sub), [-t for t in sub])
+        if best is None or key > best[0]:
+            best = (key, sub)
+    return list(best[1])
+
+
+def check_expert_choice_selection(seed=13):
+    """Each expert's chosen tokens against subset enumeration (random logits,
+    then columns with ties); weights against a hand example: logits (0, log 3)
+    give p = (1/4, 3/4)."""
+    rng = np.random.default_rng(seed)
+    for T, E, C in ((7, 3, 3), (6, 4, 1), (5, 2, 5)):
+        l = rng.standard_normal((T, E)).astype(np.float32)
+        ec = om.expert_choice(l, C)
+        for e in range(E):
+            assert list(ec.tokens[e]) == _ec_brute(l[:, e], C), (T, E, C, e)
+    l = np.array([[1, 0], [2, 2], [2, 0], [0, 5], [2, 1]], np.float32)
+    ec = om.expert_choice(l, 2)
+    assert ec.tokens.tolist() == [[1, 2], [1, 3]]
+    assert ec.tokens.tolist() == [_ec_brute(l[:, 0], 2), _ec_brute(l[:, 1], 2)]
+    l = np.array([[0.0, LN3], [LN3, 0.0]])
+    ec = om.expert_choice(l, 1)
+    assert ec.tokens.tolist() == [[1], [0]]
+    np.testing.assert_allclose(ec.w, [[0.75], [0.75]], rtol=1e-15)
+    # selection is on the logits, not on the softmax: token 1 has the larger
+    # logit for expert 0 (2 > 1) but the smaller probability (0.27 < 0.73)
+    ec = om.expert_choice(np.array([[1.0, 0.0], [2.0, 3.0]]), 1)
+    assert ec.tokens[0].tolist() == [1]
+
+
+def test_expert_choice_selection():
+    check_expert_choice_selection()
+
+
+def check_expert_choice_layer(seed=14):
+    """Expert Choice layer pins: every expert processes exactly C tokens;
+    f = C/T and aux = alpha * E * C / T; E = 1 with C = T is one dense FFN;
+    identical experts with C = T give FFN(x) (the probabilities sum to one);
+    W_g = 0 makes every expert take tokens 0..C-1, each with weight 1/E;
+    a brute-force layer on tiny inputs."""
+    rng = np.random.default_rng(seed)
+    T, d, F = 10, 5, 7
+    ec_cfg = lambda **kw: _cfg(T=T, d_model=d, d_ff=F, k=1, route=om.ROUTE_EXPERT_CHOICE, **kw)
+    x, w_g, ex, _ = _rand_layer(rng, T, d, F, 1)
+    r = om.moe_forward(ec_cfg(E=1, capacity_factor=1.0), x, w_g, lambda e: ex[e])
+    assert r.C == T
+    np.testing.assert_allclose(r.out, _torch_ffn(x, *ex[0]), rtol=1e-12, atol=1e-12)
+    E = 4
+    x, w_g, ex, _ = _rand_layer(rng, T, d, F, E)
+    r = om.moe_forward(ec_cfg(E=E, capacity_factor=float(E)), x, w_g, lambda e: ex[0])
+    np.testing.assert_allclose(r.out, _torch_ffn(x, *ex[0]), rtol=1e-12, atol=1e-12)
+    cfg = ec_cfg(E=E, capacity_factor=1.2, aux_alpha=0.01)
+    C = 3                                     # floor(1.2 * 10 / 4)
+    r = om.moe_forward(cfg, x, np.zeros_like(w_g), lambda e: ex[0])
+    assert r.C == C and r.extra["ec"].tokens.tolist() == [[0, 1, 2]] * E
+    assert np.all(r.disp.counts == C) and r.disp.offsets.tolist() == [0, 3, 6, 9, 12]
+    np.testing.assert_allclose(r.out[:C], _torch_ffn(x[:C], *ex[0]), rtol=1e-12, atol=1e-12)
+    assert np.all(r.out[C:] == 0)
+    np.testing.assert_allclose(r.f, np.full(E, C / T), rtol=0, atol=0)
+    assert abs(r.aux - 0.01 * E * C / T) < 1e-15
+    # brute force: subsets per expert, torch softmax and torch FFNs
+    r = om.moe_forward(cfg, x, w_g, lambda e: ex[e])
+    l = np.asarray(r.logits)
+    p = torch.softmax(torch.as_tensor(l, dtype=torch.float64), dim=-1).numpy()
+    want = np.zeros((T, d))
+    for e in range(E):
+        for t in _ec_brute(l[:, e], C):
+            want[t] += p[t, e] * _torch_ffn(x[t:t + 1], *ex[e])[0]
+    np.testing.assert_allclose(r.out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_layer():
+    check_expert_choice_layer()
+
+
 # ---------------------------------------------------------------- planted mistakes
 ALL_CHECKS = [check_golden_pages_values, check_selection_bruteforce, check_hand_gate_examples,
               check_softmax_topk_equals_topk_softmax, check_weights_sum_to_one,
@@ -559,7 +640,7 @@ ALL_CHECKS = [check_golden_pages_values, check_selection_bruteforce, check_hand_
               check_aux_nonnegative_and_argmax, check_capacity_hand_example,
               check_dispatch_invariants, check_forward_bruteforce,
               check_dropped_tokens_output_zero, check_router_z_loss, check_silu_closed_form,
-              check_glu_experts]
+              check_glu_experts, check_expert_choice_selection, check_expert_choice_layer]
 
 
 def _some_pin_fails():
@@ -605,6 +686,33 @@ def _capacity_ceil(cfg):
 
 _orig_load_balance = om.load_balance
 _orig_expert_ffn = om.expert_ffn
+_orig_expert_choice = om.expert_choice
+
+
+def _ec_highest_token_on_ties(logits, C, override=None):
+    l = np.asarray(logits, np.float64)
+    T = l.shape[0]
+    flipped = _orig_expert_choice(l[::-1], C, override)
+    flipped.tokens = np.sort(T - 1 - flipped.tokens, axis=1)
+    flipped.p = flipped.p[::-1]
+    flipped.w = flipped.p[flipped.tokens, np.arange(l.shape[1])[:, None]]
+    return flipped
+
+
+def _ec_on_softmax(logits, C, override=None):
+    p = om.softmax(np.asarray(logits, np.float64))
+    r = _orig_expert_choice(p, C, override)
+    r.p = p
+    r.w = p[r.tokens, np.arange(p.shape[1])[:, None]]
+    return r
+
+
+def _ec_renormalised(logits, C, override=None):
+    r = _orig_expert_choice(logits, C, override)
+    tot = np.zeros(r.p.shape[0])
+    np.add.at(tot, r.tokens.reshape(-1), r.w.reshape(-1))
+    r.w = r.w / tot[r.tokens]
+    return r
 
 
 def _silu_as_sigmoid(v):
@@ -639,6 +747,9 @@ def _z_without_max(logits):
     ("z-loss not squared", ("router_z_loss", _z_without_square)),
     ("SiLU as the plain sigmoid", ("silu", _silu_as_sigmoid)),
     ("SwiGLU gate and up halves swapped", ("expert_ffn", _swiglu_halves_swapped)),
+    ("Expert Choice ties to the highest token", ("expert_choice", _ec_highest_token_on_ties)),
+    ("Expert Choice on the softmax", ("expert_choice", _ec_on_softmax)),
+    ("Expert Choice weights renormalised per token", ("expert_choice", _ec_renormalised)),
     ("z-loss without the max term", ("router_z_loss", _z_without_max)),
     ("aux without the E factor", ("load_balance",
                                   lambda c, l, p, n: (lambda r: (r[0], r[1], r[2] / c.E))(
