@@ -11,11 +11,15 @@
 //                statistics.
 //  k_ec_select   block per expert: radix select of the C-th largest logit of
 //                the column, then one pass in ascending token order that
-//                lists the taken tokens and writes the slot table [E, T]; the
-//                last block reduces the statistics.
+//                lists the taken tokens and writes the slot table [E, T]; one
+//                extra block reduces the statistics meanwhile
+//                (k_ec_select_reg keeps a column of up to 8192 tokens in
+//                registers).
 //  k_ec_gather   x_perm[r] = x[ec_token[r]] for the E*C expert-ordered rows.
 //  k_ec_combine  out[t] = sum over the experts that took t (ascending) of
-//                w * y[slot] + sum_s y_shared[s, t], fp32, rounded once.
+//                w * y[slot] + sum_s y_shared[s, t], fp32, rounded once; in a
+//                whole-layer pass the weights come from an [E, T] copy that
+//                k_ec_select writes beside the slot table.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -38,9 +42,9 @@ struct EcArgs {
   int32_t* ec_token;         // [E, C] taken tokens of each expert, ascending
   float* ec_w;               // [E, C] their gate weights
   int32_t* ec_slot;          // [E, T] row e*C + r of (t, e), or -1
+  float* ec_wt;              // [E, T] gate weight of (t, e) where taken (else unspecified)
   int32_t* offsets;          // [E + 1] = e * C
   int32_t* counts;           // [E] = C, or null
-  unsigned int* done;        // last-block counter (zero between calls)
   StatsArgs st;              // p_part, a_tot, nb = grid of k_ec_scores, outputs
 };
 
@@ -141,10 +145,158 @@ __device__ __forceinline__ uint32_t ec_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block e: the C-th largest key of column e by a most-significant-digit radix
-// select (four 8-bit digits, a shared histogram per digit), then the taken
-// tokens in ascending order: every token above that key, and the first
-// `need` tokens equal to it.
+// Warp 0 of a select block, after the histogram of digit `shift` of the keys
+// that match `prefix`: finds the digit holding the need-th largest of them and
+// publishes the longer prefix and the rank left inside it.
+__device__ __forceinline__ void ec_pick_digit(const unsigned int* s_hist, int lane,
+                                              uint32_t prefix, int shift, int need,
+                                              uint32_t* s_prefix, int* s_need) {
+  // lane l holds digits 255 - 8l .. 248 - 8l, from the top
+  int c[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = static_cast<int>(s_hist[255 - 8 * lane - j]);
+    sum += c[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int acc = incl - sum;   // keys in higher digits than this lane's
+  if (acc < need && need <= incl) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (acc < need && need <= acc + c[j]) {
+        *s_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - j) << shift);
+        *s_need = need - acc;
+      }
+      acc += c[j];
+    }
+  }
+}
+
+// Common end of both select kernels: offsets and counts of expert e.
+__device__ __forceinline__ void ec_select_tail(const EcArgs& a, int e) {
+  if (threadIdx.x == 0) {
+    a.offsets[e + 1] = (e + 1) * a.C;
+    if (e == 0) a.offsets[0] = 0;
+    if (a.counts) a.counts[e] = a.C;
+  }
+}
+
+// The extra block E of both select kernels reduces the routing statistics
+// from the per-block partials of k_ec_scores while the other blocks select:
+// every expert has C rows, so f needs nothing from the selection.
+__device__ __forceinline__ bool ec_stats_block(const EcArgs& a) {
+  if (static_cast<int>(blockIdx.x) != a.E) return false;
+  __shared__ int s_cnt[kMaxExperts];
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_cnt[i] = a.C;
+  __syncthreads();
+  stats_finalize(a.st, s_cnt);
+  return true;
+}
+
+// Block e, columns of at most kEcThreads * VPT tokens: thread i keeps the keys
+// of tokens i*VPT .. i*VPT + VPT - 1 in registers.  Most-significant-digit
+// radix select of the C-th largest key (four 8-bit digits; lanes that share a
+// digit add to the shared histogram once, through __match_any_sync, since the
+// top digit of similar logits falls into a handful of bins), then one ordered
+// compaction: every token above that key and the first `need` tokens equal
+// to it, positions from two block-wide exclusive scans.
+template <int VPT>
+__global__ void __launch_bounds__(kEcThreads) k_ec_select_reg(const EcArgs a) {
+  __shared__ unsigned int s_hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  __shared__ int s_wsum[kEcThreads / 32];
+  griddep_wait();
+  griddep_launch_dependents();
+  if (ec_stats_block(a)) return;
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, C = a.C;
+  const float* col = a.scoresT + static_cast<int64_t>(e) * T;
+  const int t0 = tid * VPT;
+  uint32_t key[VPT];
+  float val[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    val[v] = (t0 + v < T) ? col[t0 + v] : 0.f;
+    key[v] = (t0 + v < T) ? ec_key(val[v]) : 0u;
+  }
+  // C == 0 takes nothing: no key exceeds 0xffffffff (NaN maps to 0) and need is 0
+  uint32_t prefix = C > 0 ? 0u : 0xffffffffu, mask = 0u;
+  int need = C;
+  for (int shift = 24; C > 0 && shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const bool in = (t0 + v < T) && (key[v] & mask) == prefix;
+      const int bin = in ? static_cast<int>((key[v] >> shift) & 255u) : 256;
+      const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) ec_pick_digit(s_hist, lane, prefix, shift, need, &s_prefix, &s_need);
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    mask |= 255u << shift;
+  }
+  const uint32_t thr = prefix;
+
+  // block-wide exclusive scan of one count per thread (thread order = token order)
+  auto excl_scan = [&](int x) {
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int before = incl - x;
+    for (int w = 0; w < warp; ++w) before += s_wsum[w];
+    __syncthreads();   // s_wsum is reused by the next scan
+    return before;
+  };
+  int n_eq = 0;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) n_eq += (t0 + v < T && key[v] == thr) ? 1 : 0;
+  int eq_rank = excl_scan(n_eq);
+  bool take[VPT];
+  int n_take = 0;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const bool valid = t0 + v < T;
+    const bool eq = valid && key[v] == thr;
+    take[v] = (valid && key[v] > thr) || (eq && eq_rank < need);
+    eq_rank += eq ? 1 : 0;
+    n_take += take[v] ? 1 : 0;
+  }
+  int pos = excl_scan(n_take);
+  const int64_t row0 = static_cast<int64_t>(e) * C;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int t = t0 + v;
+    if (t >= T) break;
+    if (take[v]) {
+      const float w = expf(val[v] - a.tok_max[t]) / a.tok_sum[t];   // softmax p[t, e]
+      a.ec_token[row0 + pos] = t;
+      a.ec_w[row0 + pos] = w;
+      if (a.ec_wt) a.ec_wt[static_cast<int64_t>(e) * T + t] = w;
+    }
+    a.ec_slot[static_cast<int64_t>(e) * T + t] = take[v] ? static_cast<int32_t>(row0 + pos) : -1;
+    pos += take[v] ? 1 : 0;
+  }
+  ec_select_tail(a, e);
+}
+
+// The same selection for columns of any length: the column is streamed from
+// memory for every digit and for the compaction, kEcThreads tokens at a time.
 __global__ void __launch_bounds__(kEcThreads) k_ec_select(const EcArgs a) {
   __shared__ unsigned int s_hist[256];
   __shared__ uint32_t s_prefix;
@@ -152,12 +304,12 @@ __global__ void __launch_bounds__(kEcThreads) k_ec_select(const EcArgs a) {
   __shared__ int s_wcnt[2][kEcThreads / 32];
   griddep_wait();
   griddep_launch_dependents();
+  if (ec_stats_block(a)) return;
   const int e = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = a.T, C = a.C;
   const float* col = a.scoresT + static_cast<int64_t>(e) * T;
 
-  // C == 0 takes nothing: no key exceeds 0xffffffff (NaN maps to 0) and need is 0
   uint32_t prefix = C > 0 ? 0u : 0xffffffffu, mask = 0u;
   int need = C;   // rank from the top still to find inside the keys matching prefix
   for (int shift = 24; C > 0 && shift >= 0; shift -= 8) {
@@ -168,32 +320,7 @@ __global__ void __launch_bounds__(kEcThreads) k_ec_select(const EcArgs a) {
       if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255u], 1u);
     }
     __syncthreads();
-    if (warp == 0) {
-      // lane l holds digits 255 - 8l .. 248 - 8l, from the top
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = static_cast<int>(s_hist[255 - 8 * lane - j]);
-        sum += c[j];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int acc = incl - sum;   // keys in higher digits than this lane's
-      if (acc < need && need <= incl) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (acc < need && need <= acc + c[j]) {
-            s_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - j) << shift);
-            s_need = need - acc;
-          }
-          acc += c[j];
-        }
-      }
-    }
+    if (warp == 0) ec_pick_digit(s_hist, lane, prefix, shift, need, &s_prefix, &s_need);
     __syncthreads();
     prefix = s_prefix;
     need = s_need;
@@ -230,26 +357,17 @@ __global__ void __launch_bounds__(kEcThreads) k_ec_select(const EcArgs a) {
     }
     const int64_t row = static_cast<int64_t>(e) * C + pos;
     if (take) {
+      const float w = expf(v - a.tok_max[t]) / a.tok_sum[t];   // the token's softmax p[t, e]
       a.ec_token[row] = t;
-      a.ec_w[row] = expf(v - a.tok_max[t]) / a.tok_sum[t];   // the token's softmax p[t, e]
+      a.ec_w[row] = w;
+      if (a.ec_wt) a.ec_wt[static_cast<int64_t>(e) * T + t] = w;
     }
     if (valid) a.ec_slot[static_cast<int64_t>(e) * T + t] = take ? static_cast<int32_t>(row) : -1;
     eq_carry += eq_total;
     take_carry += take_total;
     __syncthreads();   // s_wcnt is rewritten by the next chunk
   }
-  if (tid == 0) {
-    a.offsets[e + 1] = (e + 1) * C;
-    if (e == 0) a.offsets[0] = 0;
-    if (a.counts) a.counts[e] = C;
-  }
-  if (arrive_last_block(a.done)) {
-    __shared__ int s_cnt[kMaxExperts];
-    for (int i = tid; i < a.E; i += blockDim.x) s_cnt[i] = C;
-    __syncthreads();
-    stats_finalize(a.st, s_cnt);
-    if (tid == 0) *a.done = 0u;   // ready for the next grid on this workspace
-  }
+  ec_select_tail(a, e);
 }
 
 // Row gather of the expert-ordered rows: x_perm[r] = x[ec_token[r]], warp per
@@ -273,66 +391,119 @@ k_ec_gather(const int32_t* __restrict__ ec_token, int rows, int row_bytes, int C
   }
 }
 
-// out[t] = sum over e ascending with ec_slot[e, t] >= 0 of ec_w[slot] * y[slot]
-//          + sum_s y_shared[s, t]; warp per token, fp32 sums, one rounding.
-// Lane l holds the slots of experts l, l + 32, ... (E <= 32 * kEcMaxNJ).
-constexpr int kEcMaxNJ = kMaxExperts / 32;
-
+// Eight consecutive elements of a row kept as loaded (bf16 packed in one
+// 16-byte vector), converted to fp32 only when they are summed.
 template <typename TE>
-__global__ void __launch_bounds__(256)
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    v = __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ __forceinline__ void fma_into(float w, float (&acc)[8]) const {
+    const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(w, __uint_as_float(h[i] << 16), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, __uint_as_float(h[i] & 0xffff0000u), acc[2 * i + 1]);
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void fma_into(float w, float (&acc)[8]) const {
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+  }
+};
+
+// out[t] = sum over e ascending with ec_slot[e, t] >= 0 of w[e, t] * y[slot]
+//          + sum_s y_shared[s, t]; fp32 sums, one rounding.  One warp per
+// token: lane l reads the slots and weights of experts l, l + 32, ... (NJ
+// groups of 32 experts; the two [E, T] tables side by side when the weight
+// table is given, else the weights from the [E, C] list through the slots),
+// then the rows of the taken experts are summed in ascending expert order,
+// the loads of two experts' rows (U 16-byte vectors per lane each) in flight
+// together.
+template <typename TE, int U, int NJ>
+__global__ void __launch_bounds__(256, 3)
 k_ec_combine(const TE* __restrict__ y, const int32_t* __restrict__ ec_slot,
-             const float* __restrict__ ec_w, const TE* __restrict__ y_shared, int n_shared,
-             int T, int E, int d, TE* __restrict__ out) {
+             const float* __restrict__ ec_wt, const float* __restrict__ ec_w,
+             const TE* __restrict__ y_shared, int n_shared, int T, int E, int d,
+             TE* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = gridDim.x * (blockDim.x >> 5);
   const int nchunk = d / 8;
-  const int nj = (E + 31) / 32;
   for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += nw) {
-    int slot[kEcMaxNJ];
-    float wt[kEcMaxNJ];
+    int slot[NJ];
+    float wt[NJ];
 #pragma unroll
-    for (int j = 0; j < kEcMaxNJ; ++j) {
+    for (int j = 0; j < NJ; ++j) {
       const int e = lane + 32 * j;
-      slot[j] = (j < nj && e < E) ? __ldg(ec_slot + static_cast<int64_t>(e) * T + t) : -1;
-      wt[j] = slot[j] >= 0 ? __ldg(ec_w + slot[j]) : 0.f;
+      const int64_t at = static_cast<int64_t>(e) * T + t;
+      slot[j] = e < E ? __ldg(ec_slot + at) : -1;
+      if (ec_wt)
+        wt[j] = e < E ? __ldg(ec_wt + at) : 0.f;
+      else   // only the [E, C] weights: one more dependent load
+        wt[j] = slot[j] >= 0 ? __ldg(ec_w + slot[j]) : 0.f;
     }
-    constexpr int U = 2;
     for (int c0 = 0; c0 < nchunk; c0 += 32 * U) {
       float acc[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+      constexpr int Q = 2;   // experts whose rows are loaded together
 #pragma unroll
-      for (int j = 0; j < kEcMaxNJ; ++j) {
-        if (j >= nj) break;
+      for (int j = 0; j < NJ; ++j) {
         unsigned int taken = __ballot_sync(0xffffffffu, slot[j] >= 0);
         while (taken) {
-          const int b = __ffs(taken) - 1;
-          taken &= taken - 1u;
-          const int s = __shfl_sync(0xffffffffu, slot[j], b);
-          const float w = __shfl_sync(0xffffffffu, wt[j], b);
-          float v[U][8];
+          int s[Q];
+          float w[Q];
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int c = c0 + lane + 32 * u;
-            if (c < nchunk) load8(y + static_cast<int64_t>(s) * d + c * 8, v[u]);
+          for (int q = 0; q < Q; ++q) {
+            s[q] = -1;
+            w[q] = 0.f;
+            if (taken) {
+              const int b = __ffs(taken) - 1;
+              taken &= taken - 1u;
+              s[q] = __shfl_sync(0xffffffffu, slot[j], b);
+              w[q] = __shfl_sync(0xffffffffu, wt[j], b);
+            }
           }
+          Raw8<TE> v[Q][U];
 #pragma unroll
-          for (int u = 0; u < U; ++u)
+          for (int q = 0; q < Q; ++q)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(w, v[u][i], acc[u][i]);
+            for (int u = 0; u < U; ++u) {
+              const int c = c0 + lane + 32 * u;
+              if (s[q] >= 0 && c < nchunk) v[q][u].load(y + static_cast<int64_t>(s[q]) * d + c * 8);
+            }
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            if (s[q] < 0) break;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (c0 + lane + 32 * u < nchunk) v[q][u].fma_into(w[q], acc[u]);
+          }
         }
       }
-      for (int s = 0; s < n_shared; ++s) {
+      for (int sh = 0; sh < n_shared; ++sh) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int c = c0 + lane + 32 * u;
           if (c < nchunk) {
             float v[8];
-            load8(y_shared + (static_cast<int64_t>(s) * T + t) * d + c * 8, v);
+            load8(y_shared + (static_cast<int64_t>(sh) * T + t) * d + c * 8, v);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[u][i] += v[i];
           }

@@ -105,7 +105,7 @@ bool use_tc_router(const moe_config& c) {
 struct Layout {
   size_t status, logits, wgT, crank, hist;
   size_t idx, w, counts, kept, offsets, perm_token, slot_of, f, P, aux;
-  size_t scoresT, tok_stats, ec_token, ec_w, ec_slot;   // Expert Choice
+  size_t scoresT, tok_stats, ec_token, ec_w, ec_slot, ec_wt;   // Expert Choice
   size_t x_perm, H, Y, Ys, sk_part, total;
   int nb, E_pad;
   bool tc_router;   // the top-k router runs on the tensor cores
@@ -154,6 +154,7 @@ Layout make_layout(const moe_config& c) {
   L.ec_token = take(E * C * 4);
   L.ec_w = take(E * C * 4);
   L.ec_slot = take(ec ? E * T * 4 : 0);
+  L.ec_wt = take(ec ? E * T * 4 : 0);
   L.x_perm = take(rows * d * eb);
   L.H = take((rows + S * T) * F * eb);
   L.Y = take(rows * d * eb);
@@ -594,6 +595,7 @@ struct EcOut {
   int32_t* ec_token;  // [E, C]
   float* ec_w;        // [E, C]
   int32_t* ec_slot;   // [E, T]
+  float* ec_wt;       // [E, T] weight table for the combine, or null
   int32_t* offsets;   // [E + 1]
   int32_t* counts;    // [E] or null
   float *f, *P, *aux, *z;
@@ -635,9 +637,9 @@ moe_status do_route_ec(const moe_config& c, const Layout& L, void* ws, const voi
   a.ec_token = o.ec_token;
   a.ec_w = o.ec_w;
   a.ec_slot = o.ec_slot;
+  a.ec_wt = o.ec_wt;
   a.offsets = o.offsets;
   a.counts = o.counts;
-  a.done = at<unsigned int>(ws, L.status + kRouteCounterOffset);
   const int grid = ec_scores_grid(c);
   StatsArgs& sa = a.st;
   sa.p_part = at<float>(ws, L.status + kPartOffset);
@@ -674,7 +676,14 @@ moe_status do_route_ec(const moe_config& c, const Layout& L, void* ws, const voi
     s = launch_ec_scores<float, 64>(grid, a, x, w_g, st);
   }
   if (s != MOE_OK) return s;
-  return launch_pdl(k_ec_select, dim3(c.E), dim3(kEcThreads), 0, st, a);
+  // one block per expert plus the statistics block; the column in registers
+  // when it fits (up to 16 tokens a thread)
+  const dim3 grid_sel(c.E + 1), block_sel(kEcThreads);
+  const int vpt = (c.T + kEcThreads - 1) / kEcThreads;
+  if (vpt <= 4) return launch_pdl(k_ec_select_reg<4>, grid_sel, block_sel, 0, st, a);
+  if (vpt <= 8) return launch_pdl(k_ec_select_reg<8>, grid_sel, block_sel, 0, st, a);
+  if (vpt <= 16) return launch_pdl(k_ec_select_reg<16>, grid_sel, block_sel, 0, st, a);
+  return launch_pdl(k_ec_select, grid_sel, block_sel, 0, st, a);
 }
 
 moe_status do_permute_ec(const moe_config& c, const void* x, const int32_t* ec_token,
@@ -687,19 +696,41 @@ moe_status do_permute_ec(const moe_config& c, const void* x, const int32_t* ec_t
                     static_cast<const uint8_t*>(x), static_cast<uint8_t*>(x_perm), offsets);
 }
 
+template <typename TE, int U>
+moe_status launch_ec_combine(const moe_config& c, int grid, const void* y_perm,
+                             const int32_t* ec_slot, const float* ec_wt, const float* ec_w,
+                             const void* y_shared, int S, void* out, cudaStream_t st) {
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, dim3(grid), dim3(256), 0, st, static_cast<const TE*>(y_perm),
+                      ec_slot, ec_wt, ec_w, static_cast<const TE*>(y_shared), S, c.T, c.E,
+                      c.d_model, static_cast<TE*>(out));
+  };
+  if (c.E <= 64) return go(k_ec_combine<TE, U, 2>);   // two groups of 32 experts per lane
+  return go(k_ec_combine<TE, U, kMaxExperts / 32>);
+}
+
+// bf16 rows: up to three 16-byte vectors per lane and pass (the whole row in
+// one pass up to d = 768); fp32 rows: one (their loads take twice the registers)
+moe_status launch_ec_combine_dt(const moe_config& c, int grid, const void* y_perm,
+                                const int32_t* ec_slot, const float* ec_wt, const float* ec_w,
+                                const void* y_shared, int S, void* out, cudaStream_t st) {
+  if (c.dtype != MOE_BF16)
+    return launch_ec_combine<float, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+  using B = __nv_bfloat16;
+  const int u = std::min(3, (c.d_model / 8 + 31) / 32);
+  if (u <= 1) return launch_ec_combine<B, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+  if (u == 2) return launch_ec_combine<B, 2>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+  return launch_ec_combine<B, 3>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+}
+
+// ec_wt: the [E, T] weight table k_ec_select wrote in the workspace, or null
+// (then the weights are read from the [E, C] list through the slots)
 moe_status do_combine_ec(const moe_config& c, const void* y_perm, const int32_t* ec_slot,
-                         const float* ec_w, const void* y_shared, void* out, cudaStream_t st) {
-  const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
+                         const float* ec_w, const float* ec_wt, const void* y_shared, void* out,
+                         cudaStream_t st) {
+  const int grid = std::max(1, (c.T + 7) / 8);   // a warp per token
   const int S = y_shared ? c.n_shared : 0;
-  if (c.dtype == MOE_BF16)
-    return launch_pdl(k_ec_combine<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
-                      static_cast<const __nv_bfloat16*>(y_perm), ec_slot, ec_w,
-                      static_cast<const __nv_bfloat16*>(y_shared), S, c.T, c.E, c.d_model,
-                      static_cast<__nv_bfloat16*>(out));
-  return launch_pdl(k_ec_combine<float>, dim3(grid), dim3(256), 0, st,
-                    static_cast<const float*>(y_perm), ec_slot, ec_w,
-                    static_cast<const float*>(y_shared), S, c.T, c.E, c.d_model,
-                    static_cast<float*>(out));
+  return launch_ec_combine_dt(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
 }
 
 // Slot resolution and row gather from the ranks a routing or ranking grid
@@ -1113,13 +1144,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
     int32_t* offsets = at<int32_t>(ws, L.offsets);
     void* x_perm = at<uint8_t>(ws, L.x_perm);
     if ((s = do_route_ec(c, L, ws, x, w_g, logit_bias,
-                         EcOut{nullptr, tok, ew, slot, offsets, cnt, fo, Po, ao, z_loss}, st)) !=
+                         EcOut{nullptr, tok, ew, slot, at<float>(ws, L.ec_wt), offsets, cnt, fo,
+                               Po, ao, z_loss},
+                         st)) !=
         MOE_OK)
       return s;
     if ((s = do_permute_ec(c, x, tok, offsets, x_perm, st)) != MOE_OK) return s;
     FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
     if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
-    return do_combine_ec(c, Y, slot, ew, c.n_shared > 0 ? Ys : nullptr, out, st);
+    return do_combine_ec(c, Y, slot, ew, at<float>(ws, L.ec_wt),
+                         c.n_shared > 0 ? Ys : nullptr, out, st);
   }
 
   int32_t* kept = at<int32_t>(ws, L.kept);
@@ -1190,8 +1224,8 @@ moe_status moe_route_expert_choice(const moe_config* cfg, const void* x, const v
   if (!x || !w_g || !ec_slot) return MOE_ERR_INVALID_ARG;
   if (ec_capacity(c) > 0 && (!ec_token || !ec_w)) return MOE_ERR_INVALID_ARG;
   return do_route_ec(c, L, ws, x, w_g, logit_bias,
-                     EcOut{logits, ec_token, ec_w, ec_slot, at<int32_t>(ws, L.offsets), nullptr,
-                           f, P, aux, z_loss},
+                     EcOut{logits, ec_token, ec_w, ec_slot, nullptr, at<int32_t>(ws, L.offsets),
+                           nullptr, f, P, aux, z_loss},
                      st);
 }
 
@@ -1219,8 +1253,8 @@ moe_status moe_combine_expert_choice(const moe_config* cfg, const void* y_perm,
   if (!ec_slot || !out) return MOE_ERR_INVALID_ARG;
   if (ec_capacity(c) > 0 && (!y_perm || !ec_w)) return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
-  return do_combine_ec(c, y_perm, ec_slot, ec_w, c.n_shared > 0 ? y_shared : nullptr, out,
-                       static_cast<cudaStream_t>(stream));
+  return do_combine_ec(c, y_perm, ec_slot, ec_w, nullptr, c.n_shared > 0 ? y_shared : nullptr,
+                       out, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_check_status(void* ws, moe_stream stream) {

@@ -507,16 +507,21 @@ __device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
   };
   for (int p0 = 0; p0 < pairs; p0 += kBatch) {
     float pv[kBatch];
+    float* src[kBatch];
+    // every load of the batch before any of the zeroing stores: a store between
+    // two loads would order the second load behind it, one latency per pair
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int p = p0 + i;
       const int e = warp + nwarps * (p / steps);
       const int b = (p % steps) * 32 + lane;
       const bool ok = p < pairs && e < R && b < nb;
-      float* src = a.p_part + static_cast<int64_t>(ok ? e : 0) * nb + (ok ? b : 0);
-      pv[i] = ok ? __ldcg(src) : 0.f;
-      if (ok) *src = 0.f;   // zero for the next call
+      src[i] = ok ? a.p_part + static_cast<int64_t>(e) * nb + b : nullptr;
+      pv[i] = ok ? __ldcg(src[i]) : 0.f;
     }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (src[i]) *src[i] = 0.f;   // zero for the next call
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int p = p0 + i;

@@ -371,6 +371,12 @@ EC_SMALL = {
                                      aux_f="argmax"),
     "ec_every_token": dict(name="switch_expert_choice", T=200, d_model=64, d_ff=64, E=4,
                            capacity_factor=4.0),
+    # columns of 6000 tokens (16 in registers per thread) and of 9000 tokens
+    # (beyond the register-resident select: the column is streamed)
+    "ec_t6000": dict(name="switch_expert_choice", T=6000, d_model=64, d_ff=64, E=8,
+                     capacity_factor=1.0),
+    "ec_t9000_streamed": dict(name="switch_expert_choice", T=9000, d_model=64, d_ff=64, E=4,
+                              capacity_factor=0.5),
 }
 
 
