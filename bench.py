@@ -174,6 +174,18 @@ def algorithmic_ffn(cfg, kept, elem):
     return weights + acts, flops, n_a, active
 
 
+def rpc_bytes(cfg, n_a, elem) -> int:
+    """Algorithmic bytes of routing + permute + combine: x read by the router,
+    W_g, the indices and weights; x read and N_a rows written by the permute;
+    N_a rows read and T rows written by the combine (shared-expert rows, when
+    present, read once more)."""
+    T, d, E, k, S = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"], cfg.get("n_shared", 0)
+    route = T * d * elem + d * E * elem + T * k * 8
+    permute = T * d * elem + n_a * d * elem
+    combine = n_a * d * elem + T * d * elem + S * T * d * elem
+    return route + permute + combine
+
+
 def kernel_launches_per_step(cfg) -> int:
     """Kernels one moe_forward enqueues (see moe_api.cu).
     Top-k routing: the routing grid, with the W_g transpose ahead of it for
@@ -273,11 +285,45 @@ def run_ours(args, rank, world, local_rank):
         else:
             moe.combine(cfg, o["y_perm"], o["slot_of"], layer.topk_w, o["out"], y_shared=y_sh)
 
+    # routing and dispatch through their own entry points (the whole-layer pass
+    # runs the same kernels, except that its routing grid also ranks the
+    # assignments, which moe_permute does in one more small kernel)
+    f32 = torch.float32
+    r_stats = dict(f=z((E,), f32), P=z((E,), f32), aux=z((1,), f32))
+    if ec:
+        r_sel = (z((E, C), torch.int32), z((E, C), f32), z((E, T), torch.int32))
+
+        def part_route():
+            moe.route_expert_choice(cfg, inp["x"], inp["w_g"], *r_sel, r_stats["f"],
+                                    r_stats["P"], r_stats["aux"], ws2,
+                                    logit_bias=inp.get("logit_bias"))
+
+        def part_permute():
+            moe.permute_expert_choice(cfg, inp["x"], r_sel[0], o["offsets"], o["x_perm"])
+    else:
+        r_sel = (z((T, k), torch.int32), z((T, k), f32))
+
+        def part_route():
+            moe.route(cfg, inp["x"], inp["w_g"], *r_sel, r_stats["f"], r_stats["P"],
+                      r_stats["aux"], ws2, logit_bias=inp.get("logit_bias"),
+                      select_bias=inp.get("select_bias"))
+
+        def part_permute():
+            moe.permute(cfg, inp["x"], r_sel[0], o["counts"], o["kept"], o["offsets"],
+                        o["perm_token"], o["slot_of"], o["x_perm"], ws2)
+
+    part_route()
+    part_permute()
     part_ffn()
     part_combine()
     torch.cuda.synchronize(dev)
     moe.check_status(ws2)
+    g_route, g_perm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     g_ffn, g_comb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_route):
+        part_route()
+    with torch.cuda.graph(g_perm):
+        part_permute()
     with torch.cuda.graph(g_ffn):
         part_ffn()
     with torch.cuda.graph(g_comb):
@@ -310,6 +356,8 @@ def run_ours(args, rank, world, local_rank):
     _timed_graph_loop(g_ffn, flush, stream, 3)
     ffn_ms = statistics.fmean(_timed_graph_loop(g_ffn, flush, stream, n_part))
     cb_ms = statistics.fmean(_timed_graph_loop(g_comb, flush, stream, n_part))
+    ro_ms = statistics.fmean(_timed_graph_loop(g_route, flush, stream, n_part))
+    pe_ms = statistics.fmean(_timed_graph_loop(g_perm, flush, stream, n_part))
     moe.check_status(ws2)
 
     kept = o["kept"].cpu().tolist()
@@ -348,7 +396,8 @@ def run_ours(args, rank, world, local_rank):
     dev_ms, e2e_ms, ffn_ms = [float(v) for v in times.tolist()]
 
     res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms,
-               rp_ms=dev_ms / args.steps - ffn_ms - cb_ms, cb_ms=cb_ms,
+               ro_ms=ro_ms, pe_ms=pe_ms, cb_ms=cb_ms,
+               rpc_bytes=rpc_bytes(cfg, n_a, elem),
                bytes=byt, flops=flops,
                n_a=n_a, active=active, clocks=clocks, wall_s=t_wall,
                counts=layer.counts.cpu().tolist(), aux=float(layer.aux.cpu()[0]),
@@ -416,6 +465,8 @@ def emit_ours(args, res, world):
     roof["algorithmic_flops"] = res["flops"]
     roof["ms_per_launch"] = round(res["ffn_ms"], 4)
     e2e_val = world * T * args.steps / (res["e2e_ms"] / 1e3)
+    rpc_ms = res["ro_ms"] + res["pe_ms"] + res["cb_ms"]
+    rpc_gbs = res["rpc_bytes"] / (rpc_ms / 1e3) / 1e9
     counts = res["counts"]
     line = {
         "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world,
@@ -439,8 +490,13 @@ def emit_ours(args, res, world):
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"],
                 "api": "GraphedMoELayer (moe_forward captured in a CUDA graph), pinned host x in, out+aux back"},
-        "parts_ms": {"route+permute (step - ffn - combine)": round(res["rp_ms"], 4),
+        "parts_ms": {"route": round(res["ro_ms"], 4), "permute": round(res["pe_ms"], 4),
                      "grouped_ffn": round(res["ffn_ms"], 4), "combine": round(res["cb_ms"], 4)},
+        "route_permute_combine": {
+            "ms": round(rpc_ms, 4), "algorithmic_bytes": res["rpc_bytes"],
+            "achieved": round(rpc_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(rpc_gbs / peaks["hbm_gbs"], 4),
+            "api": "moe_route + moe_permute + moe_combine (each in its own CUDA graph, L2 flushed)"},
         "gpu_launches": kernel_launches_per_step(cfg) * args.steps,
         "clocks": res["clocks"],
         "wall_s_timed": round(res["wall_s"], 3),

@@ -44,9 +44,13 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
   __shared__ int s_n;
   griddep_wait();
   griddep_launch_dependents();
-  if (st.p_part && blockIdx.x == gridDim.x - 1) {   // the extra block: routing statistics
-    stats_finalize(st, nullptr);
-    return;
+  if (st.p_part) {   // the last stats_blocks(E, 8) blocks reduce the routing statistics
+    const int nsb = stats_blocks(st.E, 8);
+    const int sb = static_cast<int>(blockIdx.x) - (static_cast<int>(gridDim.x) - nsb);
+    if (sb >= 0) {
+      stats_reduce(st, sb, nsb);
+      return;
+    }
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * tpb, t1 = min(t0 + tpb, T);

@@ -186,15 +186,13 @@ __device__ __forceinline__ void ec_select_tail(const EcArgs& a, int e) {
   }
 }
 
-// The extra block E of both select kernels reduces the routing statistics
-// from the per-block partials of k_ec_scores while the other blocks select:
-// every expert has C rows, so f needs nothing from the selection.
+// The blocks after the E select blocks reduce the routing statistics from
+// the per-block partials of k_ec_scores while the others select: every expert
+// has C rows (count_all), so f needs nothing from the selection.
 __device__ __forceinline__ bool ec_stats_block(const EcArgs& a) {
-  if (static_cast<int>(blockIdx.x) != a.E) return false;
-  __shared__ int s_cnt[kMaxExperts];
-  for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_cnt[i] = a.C;
-  __syncthreads();
-  stats_finalize(a.st, s_cnt);
+  const int sb = static_cast<int>(blockIdx.x) - a.E;
+  if (sb < 0) return false;
+  stats_reduce(a.st, sb, static_cast<int>(gridDim.x) - a.E);
   return true;
 }
 

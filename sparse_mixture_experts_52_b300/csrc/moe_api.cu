@@ -33,6 +33,7 @@ constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 1 << 20;
 constexpr size_t kRouteCounterOffset = 16;
 constexpr size_t kRankCounterOffset = 20;
+constexpr size_t kStatsCounterOffset = 24;
 constexpr size_t kTotalsOffset = 1024;    // int32 [E <= 256]
 constexpr size_t kArgmaxOffset = 2048;    // uint32 [E <= 256]
 constexpr size_t kFlagsOffset = 4096;     // int32 [kMaxGemmCtas][4] stream-K flags
@@ -367,11 +368,32 @@ struct RouteOut {
   int32_t* counts;
   int32_t* kept;
   int32_t* offsets;
-  int defer_stats;
   float* z;
 };
 
 int kmax_of(int k) { return k <= 2 ? 2 : (k <= 4 ? 4 : (k <= 8 ? 8 : 16)); }
+
+// The statistics reduction over nb per-block partials in the workspace header.
+StatsArgs make_stats(const moe_config& c, void* ws, size_t status, int nb, const int32_t* counts,
+                     float* f, float* P, float* aux, float* z) {
+  StatsArgs sa{};
+  sa.p_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + status + kPartOffset);
+  sa.nb = nb;
+  sa.a_tot = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + status + kArgmaxOffset);
+  sa.counts = counts;
+  sa.count_all = -1;
+  sa.T = c.T;
+  sa.E = c.E;
+  sa.aux_f = c.aux_f;
+  sa.alpha = c.aux_alpha;
+  sa.f = f;
+  sa.P = P;
+  sa.aux = aux;
+  sa.z = z;
+  sa.done =
+      reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + status + kStatsCounterOffset);
+  return sa;
+}
 
 // Ranking state of a grid: chunk ranks and prefixes in `crank` / `hist`.
 DispatchArgs dispatch_args(const moe_config& c, int32_t* crank, int32_t* hist, int32_t* totals,
@@ -546,7 +568,6 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
   ra.f = o.f;
   ra.P = o.P;
   ra.aux = o.aux;
-  ra.defer_stats = o.defer_stats;
   ra.z = o.z;
   ra.dp = dispatch_args(c, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist),
                         at<int32_t>(ws, L.status + kTotalsOffset), o.counts, o.kept, o.offsets,
@@ -641,19 +662,8 @@ moe_status do_route_ec(const moe_config& c, const Layout& L, void* ws, const voi
   a.offsets = o.offsets;
   a.counts = o.counts;
   const int grid = ec_scores_grid(c);
-  StatsArgs& sa = a.st;
-  sa.p_part = at<float>(ws, L.status + kPartOffset);
-  sa.nb = grid;
-  sa.a_tot = at<unsigned int>(ws, L.status + kArgmaxOffset);
-  sa.counts = nullptr;
-  sa.T = c.T;
-  sa.E = c.E;
-  sa.aux_f = c.aux_f;
-  sa.alpha = c.aux_alpha;
-  sa.f = o.f;
-  sa.P = o.P;
-  sa.aux = o.aux;
-  sa.z = o.z;
+  a.st = make_stats(c, ws, L.status, grid, nullptr, o.f, o.P, o.aux, o.z);
+  a.st.count_all = a.C;   // every expert takes C tokens
   moe_status s;
   if (c.dtype == MOE_BF16) {
     dim3 tgrid((c.d_model + 31) / 32, (L.E_pad + 31) / 32);
@@ -676,9 +686,9 @@ moe_status do_route_ec(const moe_config& c, const Layout& L, void* ws, const voi
     s = launch_ec_scores<float, 64>(grid, a, x, w_g, st);
   }
   if (s != MOE_OK) return s;
-  // one block per expert plus the statistics block; the column in registers
+  // one block per expert plus the statistics blocks; the column in registers
   // when it fits (up to 16 tokens a thread)
-  const dim3 grid_sel(c.E + 1), block_sel(kEcThreads);
+  const dim3 grid_sel(c.E + stats_blocks(c.E, kEcThreads / 32)), block_sel(kEcThreads);
   const int vpt = (c.T + kEcThreads - 1) / kEcThreads;
   if (vpt <= 4) return launch_pdl(k_ec_select_reg<4>, grid_sel, block_sel, 0, st, a);
   if (vpt <= 8) return launch_pdl(k_ec_select_reg<8>, grid_sel, block_sel, 0, st, a);
@@ -744,8 +754,9 @@ moe_status launch_permute(const moe_config& c, const int32_t* idx, const int32_t
   const int row_bytes = c.d_model * static_cast<int>(elem_bytes(c));
   int tpb = 32;
   while (tpb > 4 && (c.T + tpb - 1) / tpb < 2 * num_sms()) tpb >>= 1;
-  // plus one block for the routing statistics in a whole-layer pass
-  const int grid = std::max(1, (c.T + tpb - 1) / tpb) + (stats.p_part ? 1 : 0);
+  // plus the blocks of the routing statistics in a whole-layer pass
+  const int grid =
+      std::max(1, (c.T + tpb - 1) / tpb) + (stats.p_part ? stats_blocks(c.E, 8) : 0);
   const int ncs = chunk_stride(c.T);
   const auto* xb = static_cast<const uint8_t*>(x);
   auto* xp = static_cast<uint8_t*>(x_perm);
@@ -1022,10 +1033,15 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
     return zero_stats(c, nullptr, f, P, aux, nullptr, nullptr, st);
   }
   if (!x || !w_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-  return do_route(c, L, ws, x, w_g, logit_bias, select_bias,
-                  RouteOut{logits, topk_idx, topk_w, f, P, aux, at<int32_t>(ws, L.counts),
-                           at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets), 0, z_loss},
-                  st);
+  if ((s = do_route(c, L, ws, x, w_g, logit_bias, select_bias,
+                    RouteOut{logits, topk_idx, topk_w, f, P, aux, at<int32_t>(ws, L.counts),
+                             at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets), z_loss},
+                    st)) != MOE_OK)
+    return s;
+  // the routing statistics: a small grid of their own after the routing grid
+  const StatsArgs sa =
+      make_stats(c, ws, L.status, route_grid(c, L), at<int32_t>(ws, L.counts), f, P, aux, z_loss);
+  return launch_pdl(k_stats, dim3(stats_blocks(c.E, 8)), dim3(256), 0, st, sa);
 }
 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
@@ -1163,23 +1179,11 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   void* x_perm = at<uint8_t>(ws, L.x_perm);
   // the routing grid also ranks the assignments: the permute follows directly
   if ((s = do_route(c, L, ws, x, w_g, logit_bias, select_bias,
-                    RouteOut{nullptr, idx, w, fo, Po, ao, cnt, kept, offsets, 1, z_loss}, st)) !=
+                    RouteOut{nullptr, idx, w, fo, Po, ao, cnt, kept, offsets, z_loss}, st)) !=
       MOE_OK)
     return s;
-  // the permute kernel's extra block reduces the routing statistics
-  StatsArgs sa{};
-  sa.p_part = at<float>(ws, L.status + kPartOffset);
-  sa.nb = route_grid(c, L);
-  sa.a_tot = at<unsigned int>(ws, L.status + kArgmaxOffset);
-  sa.counts = cnt;
-  sa.T = c.T;
-  sa.E = c.E;
-  sa.aux_f = c.aux_f;
-  sa.alpha = c.aux_alpha;
-  sa.f = fo;
-  sa.P = Po;
-  sa.aux = ao;
-  sa.z = z_loss;
+  // the permute kernel's extra blocks reduce the routing statistics
+  const StatsArgs sa = make_stats(c, ws, L.status, route_grid(c, L), cnt, fo, Po, ao, z_loss);
   // top-1 bf16 layers without shared experts: the combine is fused into the
   // down-projection (and the permute writes the zero rows of dropped tokens)
   const bool fused_combine = c.dtype == MOE_BF16 && c.k == 1 && c.n_shared == 0;

@@ -36,6 +36,7 @@ constexpr int kMaxK = 16;
 constexpr int kRouteWarps = 8;          // warps per routing block
 constexpr int kRouteThreads = kRouteWarps * 32;
 constexpr int kRouteMaxBlocks = 296;    // partial-sum rows (fixed: layout must not depend on the GPU)
+constexpr int kSmallRouteMaxT = 512;   // the block-per-token router takes T <= this
 constexpr int kChunk = 32;              // tokens per ranking chunk (one warp's lanes)
 constexpr int kRouteMaxRows = 512;      // routing-grid blocks whose softmax partials the header holds
 
@@ -85,7 +86,6 @@ struct RouteArgs {
   float* aux;                 // [1]
   float* z;                   // [1] router z-loss, or null
   DispatchArgs dp;
-  int defer_stats;            // 1: the combine kernel reduces the statistics instead
 };
 
 // The statistics reduction: P, f and aux from the routing grid's per-block
@@ -94,21 +94,26 @@ struct StatsArgs {
   float* p_part;              // [E + 1, nb]; cleared after reading
   int nb;
   unsigned int* a_tot;        // [E]; cleared after reading
-  const int32_t* counts;      // [E] (read when s_cnt is not given)
+  const int32_t* counts;      // [E] assignments per expert (when count_all < 0)
+  int count_all;              // >= 0: every expert has this many (Expert Choice)
   int T, E, aux_f;
   float alpha;
   float* f;
   float* P;
   float* aux;
   float* z;                   // router z-loss, or null
+  unsigned int* done;         // last-block counter of the reduction (zero between calls)
 };
 
-__host__ __device__ inline StatsArgs stats_args(const RouteArgs& a, int nb) {
+__host__ __device__ inline StatsArgs stats_args(const RouteArgs& a, int nb,
+                                                unsigned int* done) {
   StatsArgs st;
+  st.done = done;
   st.p_part = a.p_part;
   st.nb = nb;
   st.a_tot = a.a_tot;
   st.counts = a.dp.counts;
+  st.count_all = -1;
   st.T = a.T;
   st.E = a.E;
   st.aux_f = a.aux_f;
@@ -462,93 +467,101 @@ __device__ void dispatch_finalize(const DispatchArgs& a, int* s_cnt) {
   __syncthreads();
 }
 
-// P, f and aux (the routing grid's last block, or an extra block of the
-// combine kernel), fp32 throughout (the FP64 pipe
-// of this GPU is 64x slower) and in a fixed order.  Warp w reduces the rows
-// of partials of experts w, w + nwarps, ...: lane l sums blocks l, l+32, ... in
-// ascending order, a fixed shuffle tree combines the lanes.  The loads of up
-// to 16 (expert, 32-block step) pairs per lane are in flight together, and
-// consecutive lanes read consecutive blocks (one 128-byte line per warp load).
-// The arg-max totals are read up front (and cleared for the next call).
-__device__ void stats_finalize(const StatsArgs& a, const int* s_cnt) {
-  constexpr int kBatch = 16;
-  __shared__ float s_fp[kMaxExperts];
-  __shared__ int s_am[kMaxExperts];
-  const int E = a.E, nb = a.nb;
+// The statistics reduction: P, f, aux and the z-loss from the routing grid's
+// per-block partials, fp32 throughout (the FP64 pipe of this GPU is 64x
+// slower) and in a fixed order.  It runs on a few blocks in parallel (extra
+// blocks of the permute or select grid, or its own small grid): each warp
+// takes whole rows of the partials - expert rows, then the z-loss row - and
+// lane l sums blocks l, l+32, ... in ascending order with every load of the
+// row in flight together, a fixed shuffle tree combining the lanes.  The last
+// block to finish adds aux = alpha * E * sum_e f_e P_e.
+constexpr int kStatsMaxSteps = (kRouteMaxBlocks > kSmallRouteMaxT ? kRouteMaxBlocks
+                                                                   : kSmallRouteMaxT) / 32 + 1;
+
+// Blocks of `warps` warps that the reduction of E experts takes.
+__host__ __device__ inline int stats_blocks(int E, int warps) {
+  return (E + 1 + warps - 1) / warps;
+}
+
+__device__ __forceinline__ void stats_row(const StatsArgs& a, int r, int lane) {
+  const int nb = a.nb, steps = (nb + 31) / 32;
+  float* row = a.p_part + static_cast<int64_t>(r) * nb;
+  float pv[kStatsMaxSteps];
+#pragma unroll
+  for (int s = 0; s < kStatsMaxSteps; ++s) {
+    const int b = s * 32 + lane;
+    pv[s] = (s < steps && b < nb) ? __ldcg(row + b) : 0.f;
+  }
+  // the zeroing stores after every load of the row: a store between two loads
+  // would order the second load behind it
+#pragma unroll
+  for (int s = 0; s < kStatsMaxSteps; ++s) {
+    const int b = s * 32 + lane;
+    if (s < steps && b < nb) row[b] = 0.f;   // zero for the next call
+  }
+  float p = 0.f;
+#pragma unroll
+  for (int s = 0; s < kStatsMaxSteps; ++s) p += pv[s];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+  if (lane != 0) return;
+  if (r == a.E) {   // the z-loss row
+    if (a.z) *a.z = p / static_cast<float>(a.T);
+    return;
+  }
+  int cnt;
+  if (a.aux_f == AUXF_ARGMAX) {
+    cnt = static_cast<int>(__ldcg(a.a_tot + r));
+    a.a_tot[r] = 0u;   // cleared for the next call
+  } else {
+    cnt = a.count_all >= 0 ? a.count_all : __ldcg(a.counts + r);
+  }
+  a.P[r] = p / static_cast<float>(a.T);
+  a.f[r] = static_cast<float>(cnt) / static_cast<float>(a.T);
+}
+
+// Block sb of the nblk blocks of the reduction.
+__device__ void stats_reduce(const StatsArgs& a, int sb, int nblk) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {   // all arg-max totals at once
-    s_am[e] = static_cast<int>(__ldcg(a.a_tot + e));
-    a.a_tot[e] = 0u;
+  for (int r = sb * nwarps + warp; r <= a.E; r += nblk * nwarps) stats_row(a, r, lane);
+  if (a.aux_f != AUXF_ARGMAX) {   // arg-max totals unused: clear them for the next call
+    for (int e = sb * blockDim.x + threadIdx.x; e < a.E; e += nblk * blockDim.x) a.a_tot[e] = 0u;
+  }
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(a.done)
+                 : "memory");
+    s_last = (prev == static_cast<unsigned int>(nblk) - 1u) ? 1 : 0;
   }
   __syncthreads();
-  const int steps = (nb + 31) / 32;
-  const int R = E + 1;   // the experts' rows, then the z-loss row
-  const int per_warp = (R + nwarps - 1) / nwarps;
-  const int pairs = per_warp * steps;   // expert-major: steps of one expert are consecutive
-  float ps = 0.f;
-  int cur = -1;
-  auto flush = [&](int e) {
-    float p = ps;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-    if (e == E) {
-      if (lane == 0 && a.z) *a.z = p / static_cast<float>(a.T);
-      return;
-    }
-    if (lane == 0) {
-      const float Pe = p / static_cast<float>(a.T);
-      const int cnt = (a.aux_f == AUXF_ARGMAX) ? s_am[e] : (s_cnt ? s_cnt[e] : __ldg(a.counts + e));
-      const float fe = static_cast<float>(cnt) / static_cast<float>(a.T);
-      a.P[e] = Pe;
-      a.f[e] = fe;
-      s_fp[e] = fe * Pe;
-    }
-  };
-  for (int p0 = 0; p0 < pairs; p0 += kBatch) {
-    float pv[kBatch];
-    float* src[kBatch];
-    // every load of the batch before any of the zeroing stores: a store between
-    // two loads would order the second load behind it, one latency per pair
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int p = p0 + i;
-      const int e = warp + nwarps * (p / steps);
-      const int b = (p % steps) * 32 + lane;
-      const bool ok = p < pairs && e < R && b < nb;
-      src[i] = ok ? a.p_part + static_cast<int64_t>(e) * nb + b : nullptr;
-      pv[i] = ok ? __ldcg(src[i]) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      if (src[i]) *src[i] = 0.f;   // zero for the next call
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int p = p0 + i;
-      const int e = warp + nwarps * (p / steps);
-      if (p < pairs && e < R) {          // warp-uniform
-        if (e != cur) {
-          if (cur >= 0) flush(cur);
-          cur = e;
-          ps = 0.f;
-        }
-        ps += pv[i];
-      }
-    }
-  }
-  if (cur >= 0) flush(cur);
-  __syncthreads();
-  if (warp == 0) {   // aux = alpha * E * sum_e f_e P_e: lane-strided, then a fixed tree
+  if (!s_last) return;
+  if (warp == 0) {   // aux: lane-strided over the experts, then a fixed tree
     float sum = 0.f;
-    for (int x = lane; x < E; x += 32) sum += s_fp[x];
+    for (int e = lane; e < a.E; e += 32) sum += __ldcg(a.f + e) * __ldcg(a.P + e);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) *a.aux = a.alpha * static_cast<float>(E) * sum;
+    if (lane == 0) {
+      *a.aux = a.alpha * static_cast<float>(a.E) * sum;
+      *a.done = 0u;   // ready for the next call on this workspace
+    }
   }
 }
 
+// The reduction as a grid of its own (stats_blocks(E, 8) blocks of 256).
+__global__ void __launch_bounds__(256) k_stats(const StatsArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  stats_reduce(a, blockIdx.x, gridDim.x);
+}
+
 // Common tail of the routing kernels: statistics partials, chunk ranking, and
-// the last block's finalize.
+// the last block's dispatch finalize (the statistics are reduced by a later
+// grid: stats_reduce).
 template <int NPL, int KMAX>
 __device__ __forceinline__ void route_block_tail(const RouteArgs& a, const LaneStats<NPL>& st) {
   flush_stats<NPL>(st, a.E, a.p_part, a.a_tot);
@@ -557,7 +570,6 @@ __device__ __forceinline__ void route_block_tail(const RouteArgs& a, const LaneS
   if (arrive_last_block(a.dp.done)) {
     __shared__ int s_cnt[kMaxExperts];
     dispatch_finalize(a.dp, s_cnt);
-    if (!a.defer_stats) stats_finalize(stats_args(a, gridDim.x), s_cnt);
     if (threadIdx.x == 0) *a.dp.done = 0u;   // ready for the next grid on this workspace
   }
 }
@@ -678,7 +690,6 @@ k_route_warp(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict__
 // the matching W_g rows.  fp32 FMA, a block reduction in a fixed order
 // completes the E logits, warp 0 gates the token.  The last block ranks every
 // chunk of the batch and finalises.
-constexpr int kSmallRouteMaxT = 512;
 
 template <typename TE, int EP, int KMAX>
 __global__ void __launch_bounds__(kRouteThreads)
@@ -782,7 +793,6 @@ k_route_small(const RouteArgs a, const TE* __restrict__ x, const TE* __restrict_
     rank_chunks<KMAX>(a.dp, a.idx, 0, num_chunks(a.T));
     __syncthreads();
     dispatch_finalize(a.dp, s_cnt);
-    if (!a.defer_stats) stats_finalize(stats_args(a, gridDim.x), s_cnt);
     if (threadIdx.x == 0) *a.dp.done = 0u;
   }
 }

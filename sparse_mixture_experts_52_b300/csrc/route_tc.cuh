@@ -350,7 +350,6 @@ k_route_tc(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUten
   if (arrive_last_block(a.dp.done)) {
     __shared__ int s_cnt[kMaxExperts];
     dispatch_finalize(a.dp, s_cnt);
-    if (!a.defer_stats) stats_finalize(stats_args(a, gridDim.x), s_cnt);
     if (threadIdx.x == 0) *a.dp.done = 0u;
   }
 }
