@@ -174,8 +174,47 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <typename TE, int KMAX>
-__global__ void __launch_bounds__(256)
+// Eight consecutive elements of a row kept as loaded (bf16 packed in one
+// 16-byte vector), converted to fp32 only when they are summed.
+template <typename TE>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    v = __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ __forceinline__ void fma_into(float w, float (&acc)[8]) const {
+    const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(w, __uint_as_float(h[i] << 16), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, __uint_as_float(h[i] & 0xffff0000u), acc[2 * i + 1]);
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void fma_into(float w, float (&acc)[8]) const {
+    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+  }
+};
+
+// out[t] = sum_j w[t,j] * y[slot_of[t,j]] + sum_s y_shared[s,t]: one warp per
+// token, fp32 sums in ascending j then s, one rounding.  The rows of up to
+// eight slots (four for fp32; U 16-byte vectors per lane each, kept packed as
+// loaded) are requested together before any is summed, so a warp has up to
+// 8 * U * 512 bytes in flight; 64 registers a thread let every token of a
+// 4096-token batch hold a warp at once.
+template <typename TE, int KMAX, int U>
+__global__ void __launch_bounds__(256, 4)
 k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
           const float* __restrict__ w, const TE* __restrict__ y_shared, int n_shared, int T,
           int k, int d, TE* __restrict__ out) {
@@ -185,20 +224,16 @@ k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
   const int nw = gridDim.x * (blockDim.x >> 5);
   const int nchunk = d / 8;
   for (int t = blockIdx.x * (blockDim.x >> 5) + warp; t < T; t += nw) {
-    int slot[KMAX];
-    float wt[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      slot[j] = -1;
-      wt[j] = 0.f;
-      if (j < k) {
-        slot[j] = __ldg(slot_of + static_cast<int64_t>(t) * k + j);
-        wt[j] = __ldg(w + static_cast<int64_t>(t) * k + j);
-      }
+    // lane j < k holds slot j and its weight; the warp reads them by shuffle
+    int my_slot = -1;
+    float my_w = 0.f;
+    if (lane < k) {
+      my_slot = __ldg(slot_of + static_cast<int64_t>(t) * k + lane);
+      my_w = __ldg(w + static_cast<int64_t>(t) * k + lane);
     }
-    // two 8-element chunks per lane per pass: the loads of both (for every
-    // slot) are in flight together
-    constexpr int U = 2;
+    // slots whose rows are in flight together (fp32 vectors take twice the registers)
+    constexpr int QMAX = sizeof(TE) == 2 ? 8 : 4;
+    constexpr int Q = KMAX < QMAX ? KMAX : QMAX;
     for (int c0 = 0; c0 < nchunk; c0 += 32 * U) {
       float acc[U][8];
 #pragma unroll
@@ -206,18 +241,24 @@ k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k && slot[j] >= 0) {
-          float v[U][8];
+      for (int j0 = 0; j0 < KMAX; j0 += Q) {
+        Raw8<TE> v[Q][U];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          const int s = __shfl_sync(0xffffffffu, my_slot, j0 + q);
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int c = c0 + lane + 32 * u;
-            if (c < nchunk) load8(y + static_cast<int64_t>(slot[j]) * d + c * 8, v[u]);
+            if (s >= 0 && c < nchunk) v[q][u].load(y + static_cast<int64_t>(s) * d + c * 8);
           }
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          const int s = __shfl_sync(0xffffffffu, my_slot, j0 + q);
+          const float wq = __shfl_sync(0xffffffffu, my_w, j0 + q);
 #pragma unroll
           for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = fmaf(wt[j], v[u][i], acc[u][i]);
+            if (s >= 0 && c0 + lane + 32 * u < nchunk) v[q][u].fma_into(wq, acc[u]);
         }
       }
       for (int s = 0; s < n_shared; ++s) {

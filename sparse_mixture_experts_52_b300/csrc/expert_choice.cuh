@@ -389,39 +389,6 @@ k_ec_gather(const int32_t* __restrict__ ec_token, int rows, int row_bytes, int C
   }
 }
 
-// Eight consecutive elements of a row kept as loaded (bf16 packed in one
-// 16-byte vector), converted to fp32 only when they are summed.
-template <typename TE>
-struct Raw8;
-template <>
-struct Raw8<__nv_bfloat16> {
-  uint4 v;
-  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
-    v = __ldg(reinterpret_cast<const uint4*>(p));
-  }
-  __device__ __forceinline__ void fma_into(float w, float (&acc)[8]) const {
-    const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(w, __uint_as_float(h[i] << 16), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(w, __uint_as_float(h[i] & 0xffff0000u), acc[2 * i + 1]);
-    }
-  }
-};
-template <>
-struct Raw8<float> {
-  float4 a, b;
-  __device__ __forceinline__ void load(const float* p) {
-    a = __ldg(reinterpret_cast<const float4*>(p));
-    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  }
-  __device__ __forceinline__ void fma_into(float w, float (&acc)[8]) const {
-    const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
-  }
-};
-
 // out[t] = sum over e ascending with ec_slot[e, t] >= 0 of w[e, t] * y[slot]
 //          + sum_s y_shared[s, t]; fp32 sums, one rounding.  One warp per
 // token: lane l reads the slots and weights of experts l, l + 32, ... (NJ

@@ -964,22 +964,24 @@ moe_status do_combine(const moe_config& c, const void* y_perm, const int32_t* sl
                       const float* w, const void* y_shared, void* out, cudaStream_t st) {
   const int grid = std::max(1, std::min((c.T + 7) / 8, num_sms() * 8));
   const int S = y_shared ? c.n_shared : 0;
-#define MOE_COMBINE(TE, KM)                                                                 \
-  return launch_pdl(k_combine<TE, KM>, dim3(grid), dim3(256), 0, st,                        \
+  // U 16-byte vectors per lane and pass: two for bf16 top-1/2 and top-3/4 rows,
+  // one with more slots in flight (or fp32 rows)
+#define MOE_COMBINE(TE, KM, U)                                                              \
+  return launch_pdl(k_combine<TE, KM, U>, dim3(grid), dim3(256), 0, st,                     \
                     static_cast<const TE*>(y_perm), slot_of, w,                             \
                     static_cast<const TE*>(y_shared), S, c.T, c.k, c.d_model,                \
                     static_cast<TE*>(out))
   const int km = kmax_of(c.k);
   if (c.dtype == MOE_BF16) {
-    if (km == 2) MOE_COMBINE(__nv_bfloat16, 2);
-    if (km == 4) MOE_COMBINE(__nv_bfloat16, 4);
-    if (km == 8) MOE_COMBINE(__nv_bfloat16, 8);
-    MOE_COMBINE(__nv_bfloat16, 16);
+    if (km == 2) MOE_COMBINE(__nv_bfloat16, 2, 2);
+    if (km == 4) MOE_COMBINE(__nv_bfloat16, 4, 2);
+    if (km == 8) MOE_COMBINE(__nv_bfloat16, 8, 1);
+    MOE_COMBINE(__nv_bfloat16, 16, 1);
   }
-  if (km == 2) MOE_COMBINE(float, 2);
-  if (km == 4) MOE_COMBINE(float, 4);
-  if (km == 8) MOE_COMBINE(float, 8);
-  MOE_COMBINE(float, 16);
+  if (km == 2) MOE_COMBINE(float, 2, 1);
+  if (km == 4) MOE_COMBINE(float, 4, 1);
+  if (km == 8) MOE_COMBINE(float, 8, 1);
+  MOE_COMBINE(float, 16, 1);
 #undef MOE_COMBINE
 }
 
