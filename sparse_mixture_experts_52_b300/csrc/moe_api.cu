@@ -418,11 +418,12 @@ DispatchArgs dispatch_args(const moe_config& c, int32_t* crank, int32_t* hist, i
 
 template <int NPL>
 moe_status launch_gate(int km, int nb, cudaStream_t st, const RouteArgs& ra) {
+  constexpr int W = kGateWarps;
   switch (km) {
-    case 2: return launch_pdl(k_gate<NPL, 2>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
-    case 4: return launch_pdl(k_gate<NPL, 4>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
-    case 8: return launch_pdl(k_gate<NPL, 8>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
-    default: return launch_pdl(k_gate<NPL, 16>, dim3(nb), dim3(kRouteThreads), 0, st, ra);
+    case 2: return launch_pdl(k_gate<NPL, 2, W>, dim3(nb), dim3(W * 32), 0, st, ra);
+    case 4: return launch_pdl(k_gate<NPL, 4, W>, dim3(nb), dim3(W * 32), 0, st, ra);
+    case 8: return launch_pdl(k_gate<NPL, 8, W>, dim3(nb), dim3(W * 32), 0, st, ra);
+    default: return launch_pdl(k_gate<NPL, 16, W>, dim3(nb), dim3(W * 32), 0, st, ra);
   }
 }
 

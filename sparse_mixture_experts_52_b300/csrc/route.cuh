@@ -35,6 +35,7 @@ enum : int { DEV_ERR_BAD_EXPERT_INDEX = 8 };   // status bit: an expert index ou
 constexpr int kMaxK = 16;
 constexpr int kRouteWarps = 8;          // warps per routing block
 constexpr int kRouteThreads = kRouteWarps * 32;
+constexpr int kGateWarps = 16;          // warps per block of the gate-from-logits grid
 constexpr int kRouteMaxBlocks = 296;    // partial-sum rows (fixed: layout must not depend on the GPU)
 constexpr int kSmallRouteMaxT = 512;   // the block-per-token router takes T <= this
 constexpr int kChunk = 32;              // tokens per ranking chunk (one warp's lanes)
@@ -290,33 +291,33 @@ __device__ __forceinline__ void gate_token(const float (&l)[NPL], const float (&
 
 // Block epilogue of the statistics: warps' softmax partials summed in warp
 // order into column blockIdx.x of the expert-major [E, gridDim.x] partials;
-// arg-max counts added to the per-expert totals.
-template <int NPL>
+// arg-max counts (integers, so their order does not matter) gathered with
+// shared atomics and added to the per-expert totals.
+template <int NPL, int WARPS = kRouteWarps>
 __device__ __forceinline__ void flush_stats(const LaneStats<NPL>& st, int E, float* p_part,
                                             unsigned int* a_tot) {
-  __shared__ float s_p[kRouteWarps][32 * NPL];
-  __shared__ int s_a[kRouteWarps][32 * NPL];
-  __shared__ float s_z[kRouteWarps];
+  __shared__ float s_p[WARPS][32 * NPL];
+  __shared__ int s_a[32 * NPL];
+  __shared__ float s_z[WARPS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 32 * NPL; i += blockDim.x) s_a[i] = 0;
+  __syncthreads();
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     s_p[warp][lane + 32 * i] = st.p[i];
-    s_a[warp][lane + 32 * i] = st.amax[i];
+    if (st.amax[i]) atomicAdd(&s_a[lane + 32 * i], st.amax[i]);
   }
   if (lane == 0) s_z[warp] = st.z;
   __syncthreads();
   if (threadIdx.x == 0) {   // z-loss row of the partials, warps in order
     float zs = 0.f;
-    for (int w = 0; w < kRouteWarps; ++w) zs += s_z[w];
+    for (int w = 0; w < WARPS; ++w) zs += s_z[w];
     if (zs != 0.f) atomicAdd(p_part + static_cast<int64_t>(E) * gridDim.x + blockIdx.x, zs);
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float ps = 0.f;
-    int as = 0;
-    for (int w = 0; w < kRouteWarps; ++w) {
-      ps += s_p[w][e];
-      as += s_a[w][e];
-    }
+    for (int w = 0; w < WARPS; ++w) ps += s_p[w][e];
+    const int as = s_a[e];
     // a reduction into a slot that is zero and that only this block touches:
     // the value lands at L2 (0 + ps == ps, so the result is exact)
     if (ps != 0.f) atomicAdd(p_part + static_cast<int64_t>(e) * gridDim.x + blockIdx.x, ps);
@@ -394,22 +395,22 @@ __device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t*
   rank_chunk_experts<KMAX>(a, e, g, s_hist);
 }
 
-// Ranks chunks [g0, g1) (warp w takes chunks g0+w, g0+w+8, ...).
-template <int KMAX>
+// Ranks chunks [g0, g1) (warp w takes chunks g0+w, g0+w+WARPS, ...).
+template <int KMAX, int WARPS = kRouteWarps>
 __device__ __forceinline__ void rank_chunks(const DispatchArgs& a, const int32_t* idx, int g0,
                                             int g1) {
-  __shared__ int s_hist[kRouteWarps][kMaxExperts];
+  __shared__ int s_hist[WARPS][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int x = lane; x < a.E; x += 32) s_hist[warp][x] = 0;
   __syncwarp();
-  for (int g = g0 + warp; g < g1; g += kRouteWarps) rank_chunk<KMAX>(a, idx, g, s_hist[warp]);
+  for (int g = g0 + warp; g < g1; g += WARPS) rank_chunk<KMAX>(a, idx, g, s_hist[warp]);
 }
 
 // Ranks every chunk of this block's range.
-template <int KMAX>
+template <int KMAX, int WARPS = kRouteWarps>
 __device__ __forceinline__ void rank_block_chunks(const DispatchArgs& a, const int32_t* idx) {
   const int g0 = blockIdx.x * a.cpb;
-  rank_chunks<KMAX>(a, idx, g0, min(g0 + a.cpb, num_chunks(a.T)));
+  rank_chunks<KMAX, WARPS>(a, idx, g0, min(g0 + a.cpb, num_chunks(a.T)));
 }
 
 // True in the one block that arrives last; every thread of the block must call
@@ -562,11 +563,11 @@ __global__ void __launch_bounds__(256) k_stats(const StatsArgs a) {
 // Common tail of the routing kernels: statistics partials, chunk ranking, and
 // the last block's dispatch finalize (the statistics are reduced by a later
 // grid: stats_reduce).
-template <int NPL, int KMAX>
+template <int NPL, int KMAX, int WARPS = kRouteWarps>
 __device__ __forceinline__ void route_block_tail(const RouteArgs& a, const LaneStats<NPL>& st) {
-  flush_stats<NPL>(st, a.E, a.p_part, a.a_tot);
+  flush_stats<NPL, WARPS>(st, a.E, a.p_part, a.a_tot);
   __syncthreads();   // this block's idx writes are visible to all its warps
-  rank_block_chunks<KMAX>(a.dp, a.idx);
+  rank_block_chunks<KMAX, WARPS>(a.dp, a.idx);
   if (arrive_last_block(a.dp.done)) {
     __shared__ int s_cnt[kMaxExperts];
     dispatch_finalize(a.dp, s_cnt);
@@ -592,9 +593,12 @@ __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// Gate from precomputed logits (tensor-core router), E <= 32 * NPL.
-template <int NPL, int KMAX>
-__global__ void __launch_bounds__(kRouteThreads) k_gate(const RouteArgs a) {
+// Gate from precomputed logits (tensor-core router), E <= 32 * NPL.  WARPS
+// warps a block: a warp gates one token at a time, and the gating of a wide
+// router (E = 256, k = 8) is a chain of shuffles, so more warps per SM hide
+// its latency.
+template <int NPL, int KMAX, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) k_gate(const RouteArgs a) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_gate(const RouteArgs a) {
   st.zero();
   const int t0 = blockIdx.x * a.dp.cpb * kChunk;
   const int t1 = min(t0 + a.dp.cpb * kChunk, a.T);
-  for (int t = t0 + warp; t < t1; t += kRouteWarps) {
+  for (int t = t0 + warp; t < t1; t += WARPS) {
     float l[NPL];
     const float* row = a.logits_in + static_cast<int64_t>(t) * a.ld_in;
 #pragma unroll
@@ -616,7 +620,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_gate(const RouteArgs a) {
     gate_token<NPL>(l, sb, a.E, a.k, a.route, a.renorm, lane,
                     a.idx + static_cast<int64_t>(t) * a.k, a.w + static_cast<int64_t>(t) * a.k, st);
   }
-  route_block_tail<NPL, KMAX>(a, st);
+  route_block_tail<NPL, KMAX, WARPS>(a, st);
 }
 
 // Router logits of one token on the CUDA cores for E <= EP <= 64: lane l sums
