@@ -27,6 +27,16 @@
 // same on every run.  The following CTAs compute those pieces first, so the
 // owner's waits are short.
 //
+// Overlapped projections.  The down-projection may start while the
+// up-projection's last tiles still run: the up-projection's epilogue warps
+// count, per expert group, the hidden tiles they have stored (ready[g], a
+// release add after a proxy fence), and the down-projection's producer waits
+// (acquire, bounded) until group g's count is complete before its first load
+// of a g tile.  The down-projection then skips the grid-dependency wait at its
+// start (it is launched once every up-projection CTA has passed its own, so
+// the dispatch outputs it reads are complete) and waits for the up-projection
+// grid at its end instead; its last CTA clears the counters.
+//
 // Every wait is bounded: a wait that runs out records MOE_DEV_ERR_* in the
 // status word, raises the CTA abort flag, drains what this CTA has in flight
 // and returns, so a bad launch can never hang the GPU.
@@ -57,8 +67,10 @@ enum : int {
   DEV_ERR_WAIT_PRODUCER = 1,
   DEV_ERR_WAIT_MMA = 2,
   DEV_ERR_WAIT_EPILOGUE = 4,
-  DEV_ERR_WAIT_PARTIAL = 16
+  DEV_ERR_WAIT_PARTIAL = 16,
+  DEV_ERR_WAIT_READY = 32
 };
+enum : int { READY_NONE = 0, READY_SIGNAL = 1, READY_WAIT = 2 };
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: any single wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s: draining after a give-up
@@ -78,6 +90,10 @@ struct TcArgs {
   int* flags;                  // [kMaxGemmCtas][4] zero between launches (stream-K)
   const int32_t* scatter_token;  // EPI_SCATTER_BF16: token of each output row
   const float* scatter_w;        // EPI_SCATTER_BF16: gate weight of each token (k = 1)
+  int ready_mode;                // READY_*: overlapped up- and down-projections
+  int* ready;                    // [groups] hidden-tile counters (zero between calls)
+  unsigned int* ready_done;      // READY_WAIT: CTAs finished (zero between calls)
+  int ready_up_tiles;            // READY_WAIT: column tiles of the up-projection per row tile
 };
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uint64_t limit) {
@@ -224,8 +240,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     tmem_alloc(&c.tmem_base, L::TMEM_COLS);
     tmem_relinquish();
   }
-  // everything above overlaps the previous kernel's tail (programmatic launch)
-  griddep_wait();
+  // everything above overlaps the previous kernel's tail (programmatic launch);
+  // an overlapped down-projection waits per group instead (see above)
+  if (args.ready_mode != READY_WAIT) griddep_wait();
   griddep_launch_dependents();
   build_group_table<BM>(gs, n_tiles, c.tb);   // synchronises the block
   tc_fence_before();
@@ -248,6 +265,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) armed[s] = 0;
       bool ok = true;
+      int ready_g = -1;   // last group whose hidden tiles are known complete
       int t, kb0, kb1;
       while (ok && seg.next(t, kb0, kb1)) {
         int g, m_blk, n_blk;
@@ -258,6 +276,22 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         const int bz = routed ? (gs.offsets ? g : 0) : g - gs.E;
         const int arow = c.tb.a_row0[g] + m_blk * BM;
         const int ncol = n_blk * BNO;
+        if (args.ready_mode == READY_WAIT && g != ready_g) {
+          // every hidden tile of group g stored by the up-projection (4 epilogue warps each)
+          const int need = ((c.tb.rows[g] + BM - 1) / BM) * args.ready_up_tiles * 4;
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire_gpu(args.ready + g) < need) {
+            if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicOr(args.err, DEV_ERR_WAIT_READY);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_global();   // the hidden rows are read by TMA (async proxy)
+          ready_g = g;
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&c.empty[stage], phase ^ 1u, abort_flag, args.err,
                                  DEV_ERR_WAIT_PRODUCER, kWaitLimitNs)) {
@@ -510,6 +544,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           }
         }
       }
+      if (args.ready_mode == READY_SIGNAL) {
+        // this warp's rows of the tile are stored: count them for group g
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) red_add_release_gpu(args.ready + g, 1);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.tempty[acc]);
@@ -523,6 +563,24 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+  if (args.ready_mode == READY_WAIT) {
+    griddep_wait();   // this grid completes after the up-projection grid
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned int prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(args.ready_done)
+                   : "memory");
+      s_last = (prev == gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {   // every CTA is past its waits: clear the counters for the next call
+      for (int g = threadIdx.x; g < G; g += blockDim.x) args.ready[g] = 0;
+      if (threadIdx.x == 0) *args.ready_done = 0u;
+    }
   }
 }
 

@@ -34,9 +34,11 @@ constexpr size_t kHeaderBytes = 1 << 20;
 constexpr size_t kRouteCounterOffset = 16;
 constexpr size_t kRankCounterOffset = 20;
 constexpr size_t kStatsCounterOffset = 24;
+constexpr size_t kReadyDoneOffset = 28;   // uint32: overlapped down-projection CTAs finished
 constexpr size_t kTotalsOffset = 1024;    // int32 [E <= 256]
 constexpr size_t kArgmaxOffset = 2048;    // uint32 [E <= 256]
 constexpr size_t kFlagsOffset = 4096;     // int32 [kMaxGemmCtas][4] stream-K flags
+constexpr size_t kReadyOffset = 8192;     // int32 [kMaxGroups] hidden tiles stored per group
 constexpr size_t kPartOffset = 65536;     // fp32 [E + 1 <= 257, blocks <= 512]
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -871,7 +873,8 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
       ma1 = ma0;
       mb1 = mb0;
     }
-    static_assert(kFlagsOffset + kMaxGemmCtas * 4 * sizeof(int) <= kPartOffset, "header layout");
+    static_assert(kFlagsOffset + kMaxGemmCtas * 4 * sizeof(int) <= kReadyOffset, "header layout");
+    static_assert(kReadyOffset + kMaxGroups * sizeof(int) <= kPartOffset, "header layout");
     TcArgs up{};
     up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0, 0};
     up.N = F;
@@ -885,6 +888,14 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     up.streamk = sp_up.streamk;
     up.partial = at<float>(ws, L.sk_part);
     up.flags = at<int>(ws, L.status + kFlagsOffset);
+    // the down-projection may overlap the up-projection's last tiles when
+    // neither splits tiles stream-K (they would share the partial slots)
+    const FfnSplit sp_dn = pick_ffn_split(d, rt, num_sms());
+    const bool overlap = !sp_up.streamk && !sp_dn.streamk;
+    if (overlap) {
+      up.ready_mode = READY_SIGNAL;
+      up.ready = at<int>(ws, L.status + kReadyOffset);
+    }
     const int epi_up = glu ? EPI_SWIGLU_BF16
                            : (c.act == MOE_ACT_SILU ? EPI_SILU_BF16 : EPI_GELU_BF16);
     if ((s = launch_tc(epi_up, ma0, ma1, mb0, mb1, up, bn_up, row_tiles_ub, st)) != MOE_OK)
@@ -892,7 +903,6 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     // down-projection:  y = H W2^T + b2
     CUtensorMap ha, hb0, hb1;
     if (!map_a(&ha, H, F, Tk + S * T)) return MOE_ERR_CUDA;
-    const FfnSplit sp_dn = pick_ffn_split(d, rt, num_sms());
     const int bn_dn = sp_dn.bn;
     if (!map_b(&hb0, in.w2, F, d, c.E, bn_dn)) return MOE_ERR_CUDA;
     if (S > 0) {
@@ -913,6 +923,13 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
     dn.streamk = sp_dn.streamk;
     dn.partial = at<float>(ws, L.sk_part);
     dn.flags = at<int>(ws, L.status + kFlagsOffset);
+    if (overlap) {
+      dn.ready_mode = READY_WAIT;
+      dn.ready = at<int>(ws, L.status + kReadyOffset);
+      dn.ready_done = at<unsigned int>(ws, L.status + kReadyDoneOffset);
+      const int bno_up = glu ? bn_up / 2 : bn_up;   // output columns of an up-projection tile
+      dn.ready_up_tiles = (F + bno_up - 1) / bno_up;
+    }
     if (scatter) {
       dn.out = scatter->out;
       dn.scatter_token = scatter->perm_token;
