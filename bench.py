@@ -363,31 +363,28 @@ def run_ours(args, rank, world, local_rank):
     kept = o["kept"].cpu().tolist()
     byt, flops, n_a, active = algorithmic_ffn(cfg, kept, elem)
 
-    # ---- end to end through the public API (graphed moe_forward), host buffers
+    # ---- end to end through the public API, host buffers: StreamedMoELayer
+    # (graphed moe_forward, the copy-in of step i+1 and the copy-out of step
+    # i-1 overlapping step i on their own streams); every step copies x in from
+    # pinned host memory and out and aux back
     x_host = inp["x"].cpu().pin_memory()
     out_host = torch.empty((T, d), dtype=dt).pin_memory()
     aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
-    glayer = moe.GraphedMoELayer(cfg, inp, device=dev)
-
-    def e2e_step():
-        r = glayer(x_host)
-        out_host.copy_(r["out"], non_blocking=True)
-        aux_host.copy_(r["aux"], non_blocking=True)
-
+    slayer = moe.StreamedMoELayer(cfg, inp, device=dev)
     for _ in range(max(3, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+        slayer.submit(x_host, out_host, aux_host)
+    slayer.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    e0.record(stream)
+    e0.record(slayer.s_in)       # before the first copy-in (the other streams follow it)
     for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+        slayer.submit(x_host, out_host, aux_host)
+    e1.record(slayer.s_out)      # after the last copy-out
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    moe.check_status(glayer.ws)
+    slayer.synchronize()
 
     # ---- max over ranks
     times = torch.tensor([dev_ms, e2e_ms, ffn_ms], dtype=torch.float64, device=dev)
@@ -489,7 +486,7 @@ def emit_ours(args, res, world):
                           "imbalance_ratio": round(max(counts) / (sum(counts) / len(counts)), 3)},
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"],
-                "api": "GraphedMoELayer (moe_forward captured in a CUDA graph), pinned host x in, out+aux back"},
+                "api": "StreamedMoELayer (graphed moe_forward; copy-in of step i+1 and copy-out of step i-1 overlap step i), pinned host x in, out+aux back every step"},
         "parts_ms": {"route": round(res["ro_ms"], 4), "permute": round(res["pe_ms"], 4),
                      "grouped_ffn": round(res["ffn_ms"], 4), "combine": round(res["cb_ms"], 4)},
         "route_permute_combine": {

@@ -106,26 +106,6 @@ struct StatsArgs {
   unsigned int* done;         // last-block counter of the reduction (zero between calls)
 };
 
-__host__ __device__ inline StatsArgs stats_args(const RouteArgs& a, int nb,
-                                                unsigned int* done) {
-  StatsArgs st;
-  st.done = done;
-  st.p_part = a.p_part;
-  st.nb = nb;
-  st.a_tot = a.a_tot;
-  st.counts = a.dp.counts;
-  st.count_all = -1;
-  st.T = a.T;
-  st.E = a.E;
-  st.aux_f = a.aux_f;
-  st.alpha = a.alpha;
-  st.f = a.f;
-  st.P = a.P;
-  st.aux = a.aux;
-  st.z = a.z;
-  return st;
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

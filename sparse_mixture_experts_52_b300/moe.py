@@ -441,3 +441,59 @@ class GraphedMoELayer(MoELayer):
             self.x_static.copy_(x, non_blocking=True)
         self.graph.replay()
         return self._outputs()
+
+
+class StreamedMoELayer:
+    """Layer calls on pinned host tensors with the copies overlapped.
+
+    ``submit(x_host, out_host)`` enqueues one call: the host-to-device copy of
+    x, the graphed moe_forward and the device-to-host copy of the output (and
+    of aux into ``aux_host`` when given), each on its own CUDA stream, ordered
+    by events.  Two graphed layers take turns, so the input copy of call i+1
+    and the output copy of call i-1 run while call i computes, and no call
+    overwrites a buffer that a copy of an earlier call still reads.
+    ``synchronize()`` waits for every submitted call; ``out_host`` of a call is
+    complete after that (or after ``done_event(i)`` has fired).
+    """
+
+    def __init__(self, cfg: dict, inputs: dict, device="cuda"):
+        self.device = torch.device(device)
+        self.layers = [GraphedMoELayer(cfg, inputs, device) for _ in range(2)]
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(self.device) for _ in range(3))
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.ev_in, self.ev_comp, self.ev_out = ev(), ev(), ev()
+        self.calls = 0
+
+    def submit(self, x_host: torch.Tensor, out_host: torch.Tensor,
+               aux_host: Optional[torch.Tensor] = None) -> None:
+        b = self.calls % 2
+        L = self.layers[b]
+        # x_static[b] is free once call - 2 has computed
+        self.s_in.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.s_in):
+            L.x_static.copy_(x_host, non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        # out[b] is free once the output copy of call - 2 has finished
+        self.s_comp.wait_event(self.ev_in[b])
+        self.s_comp.wait_event(self.ev_out[b])
+        with torch.cuda.stream(self.s_comp):
+            L.graph.replay()
+            self.ev_comp[b].record(self.s_comp)
+        self.s_out.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.s_out):
+            out_host.copy_(L.out, non_blocking=True)
+            if aux_host is not None:
+                aux_host.copy_(L.aux, non_blocking=True)
+            self.ev_out[b].record(self.s_out)
+        self.calls += 1
+
+    def done_event(self, i: int) -> torch.cuda.Event:
+        """Event of the output copy of the last call submitted on call i's turn."""
+        return self.ev_out[i % 2]
+
+    def synchronize(self) -> None:
+        self.s_out.synchronize()
+        self.s_comp.synchronize()
+        self.s_in.synchronize()
+        for L in self.layers:
+            check_status(L.ws)

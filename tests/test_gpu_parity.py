@@ -422,3 +422,27 @@ def test_expert_choice_full_workload():
     rep = compare.check_layer(cfg, inp, fw)
     assert moe.expert_capacity(cfg) == 128
     print("switch_expert_choice", rep.summary())
+
+
+def test_streamed_layer_overlapping_copies_match_direct_calls():
+    """StreamedMoELayer runs the copies of neighbouring calls on their own
+    streams; every call's host output must equal a direct call on the same
+    tokens, bit for bit (five calls: both graphed layers are reused)."""
+    cfg = synth.workload("switch_top1_cap", T=1000, d_model=128, d_ff=256, E=16)
+    inp = synth.make_inputs(cfg, device=DEV)
+    ref_layer = moe.MoELayer(cfg, inp, device=DEV)
+    s = moe.StreamedMoELayer(cfg, inp, device=DEV)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    xs = [torch.randn((cfg["T"], cfg["d_model"]), generator=g).to(torch.bfloat16).pin_memory()
+          for _ in range(5)]
+    outs = [torch.empty((cfg["T"], cfg["d_model"]), dtype=torch.bfloat16).pin_memory()
+            for _ in range(5)]
+    auxs = [torch.empty((1,), dtype=torch.float32).pin_memory() for _ in range(5)]
+    for x, o, a in zip(xs, outs, auxs):
+        s.submit(x, o, a)
+    s.synchronize()
+    for x, o, a in zip(xs, outs, auxs):
+        r = ref_layer(x.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(o, r["out"].cpu())
+        assert torch.equal(a, r["aux"].cpu())
