@@ -136,14 +136,8 @@ k_ec_scores(const EcArgs a, const TE* __restrict__ x, const TE* __restrict__ w_g
   flush_stats<NPL>(st, a.E, a.st.p_part, a.st.a_tot);
 }
 
-// Order-preserving map of a logit to an unsigned key: a larger logit gives a
-// larger key, -0 and +0 give the same key and NaN gives 0 (below -inf).
-__device__ __forceinline__ uint32_t ec_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (v != v) return 0u;
-  if ((u & 0x7fffffffu) == 0u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+// Key of a logit for the selection: order_key, and 0 (below -inf) for NaN.
+__device__ __forceinline__ uint32_t ec_key(float v) { return v != v ? 0u : order_key(v); }
 
 // Warp 0 of a select block, after the histogram of digit `shift` of the keys
 // that match `prefix`: finds the digit holding the need-th largest of them and

@@ -117,16 +117,23 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 // arg-max over the warp: larger value wins, the smaller index wins equal values
+// Order-preserving map of a (non-NaN) float to an unsigned key: a larger
+// value gives a larger key, -0 and +0 the same one.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7fffffffu) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Warp-wide (largest v, lowest e among equal v): two warp reductions
+// (redux.sync) instead of a five-step shuffle tree of value-index pairs.
+// v must not be NaN (the callers rank NaN as -inf).
 __device__ __forceinline__ void warp_argmax(float& v, int& e) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oe = __shfl_xor_sync(0xffffffffu, e, o);
-    if (ov > v || (ov == v && oe < e)) {
-      v = ov;
-      e = oe;
-    }
-  }
+  const uint32_t key = order_key(v);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  const uint32_t cand = (key == kmax) ? static_cast<uint32_t>(e) : 0xffffffffu;
+  e = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+  v = __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7fffffffu) : ~kmax);
 }
 
 // Per-lane accumulators of the load-balance statistics for experts lane+32*i.
