@@ -224,6 +224,23 @@ def _timed_graph_loop(graph, flush, stream, steps, before=None):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings over the process group (the
+    slowest replica sets the whole-job time); the values themselves at N = 1."""
+    import torch
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_tokens_per_s(T, world, steps, slowest_ms):
+    """Weak scaling: every replica processes T tokens a step, so the job
+    processes world * T * steps tokens in the slowest replica's time."""
+    return world * T * steps / (slowest_ms / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from sparse_mixture_experts_52_b300 import moe, synth
@@ -387,10 +404,7 @@ def run_ours(args, rank, world, local_rank):
     slayer.synchronize()
 
     # ---- max over ranks
-    times = torch.tensor([dev_ms, e2e_ms, ffn_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    dev_ms, e2e_ms, ffn_ms = [float(v) for v in times.tolist()]
+    dev_ms, e2e_ms, ffn_ms = max_over_ranks([dev_ms, e2e_ms, ffn_ms], world, dev)
 
     res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms,
                ro_ms=ro_ms, pe_ms=pe_ms, cb_ms=cb_ms,
@@ -440,7 +454,7 @@ def emit_ours(args, res, world):
     peaks, peak_src = load_peaks()
     T = cfg["T"]
     ms = res["dev_ms"] / args.steps
-    tokens_s = world * T * args.steps / (res["dev_ms"] / 1e3)
+    tokens_s = whole_job_tokens_per_s(T, world, args.steps, res["dev_ms"])
     ffn_s = res["ffn_ms"] / 1e3
     gbs = res["bytes"] / ffn_s / 1e9
     tfl = res["flops"] / ffn_s / 1e12
@@ -461,7 +475,7 @@ def emit_ours(args, res, world):
     roof["algorithmic_bytes"] = res["bytes"]
     roof["algorithmic_flops"] = res["flops"]
     roof["ms_per_launch"] = round(res["ffn_ms"], 4)
-    e2e_val = world * T * args.steps / (res["e2e_ms"] / 1e3)
+    e2e_val = whole_job_tokens_per_s(T, world, args.steps, res["e2e_ms"])
     rpc_ms = res["ro_ms"] + res["pe_ms"] + res["cb_ms"]
     rpc_gbs = res["rpc_bytes"] / (rpc_ms / 1e3) / 1e9
     counts = res["counts"]
