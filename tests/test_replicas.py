@@ -42,7 +42,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_replicas_take_the_slowest_rank():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of this (threaded) process
         out = m.dict()
         mp.start_processes(_rank_main, args=(world, _free_port(), out), nprocs=world,
                            start_method="spawn")
