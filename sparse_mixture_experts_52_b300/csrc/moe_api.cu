@@ -304,7 +304,10 @@ int64_t est_row_tiles(int64_t n_rows, int E) {
 // widest tile wins.  With few waves (weight streaming) whole tiles go round
 // robin and the width is the one with the smallest estimated makespan: each
 // round costs one tile, whose cost grows with BN (its weight slab) plus a
-// fixed share for A and the epilogue.
+// fixed share for A and the epilogue (40 columns' worth, fitted on B300 with
+// the projections overlapped: it takes 256-wide tiles for the Switch-shaped
+// up-projection and 128-wide ones for the decode-shaped one, both faster in
+// same-session A/B than the other choice).
 struct FfnSplit {
   int bn, streamk;
 };
@@ -318,7 +321,7 @@ FfnSplit pick_ffn_split(int N, int64_t row_tiles, int sms) {
     if (bn > wide) continue;
     const int64_t tiles = row_tiles * ((N + bn - 1) / bn);
     const int64_t rounds = (tiles + sms - 1) / sms;
-    const int64_t cost = rounds * (bn + 16);
+    const int64_t cost = rounds * (bn + 40);
     if (cost < best_cost) {
       best_cost = cost;
       best = bn;
