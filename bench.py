@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--dispatch-only", action="store_true",
+                    help="run moe_route, moe_permute and moe_combine three times on the "
+                         "workload's token batch (no expert weights) and exit: the command "
+                         "for per-kernel ncu captures of those steps at full size")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=None)
     return ap.parse_args()
@@ -222,6 +226,39 @@ def _timed_graph_loop(graph, flush, stream, steps, before=None):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_dispatch_only(args):
+    """Routing, dispatch and combine of one workload's token batch, three
+    times, through the step entry points; no expert weights are allocated
+    (the combine sums seeded rows standing in for the expert outputs)."""
+    import torch
+    from sparse_mixture_experts_52_b300 import moe, synth
+
+    cfg = synth.workload(args.workload)
+    if moe.expert_choice(cfg):
+        raise SystemExit("--dispatch-only covers the top-k routing forms")
+    T, d, E, k, S = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"], cfg.get("n_shared", 0)
+    dt = moe.TORCH_DTYPES[cfg["dtype"]]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    rnd = lambda shape, std=1.0: (torch.randn(shape, generator=g, device="cuda") * std).to(dt)
+    x, w_g = rnd((T, d)), rnd((d, E), d ** -0.5)
+    sb = (torch.randn((E,), generator=g, device="cuda") * cfg.get("select_bias_std", 0.0)
+          if cfg["route"] == "biased_softmax" else None)
+    ws = moe.new_workspace(cfg, "cuda")
+    z = lambda s, t: torch.empty(s, dtype=t, device="cuda")
+    idx, w = z((T, k), torch.int32), z((T, k), torch.float32)
+    f, P, aux = z((E,), torch.float32), z((E,), torch.float32), z((1,), torch.float32)
+    counts, kept, offs = z((E,), torch.int32), z((E,), torch.int32), z((E + 1,), torch.int32)
+    pt, so, xp = z((T * k,), torch.int32), z((T * k,), torch.int32), z((T * k, d), dt)
+    y, ys, out = rnd((T * k, d)), (rnd((S, T, d)) if S else None), z((T, d), dt)
+    for _ in range(3):
+        moe.route(cfg, x, w_g, idx, w, f, P, aux, ws, select_bias=sb)
+        moe.permute(cfg, x, idx, counts, kept, offs, pt, so, xp, ws)
+        moe.combine(cfg, y, so, w, out, y_shared=ys)
+    torch.cuda.synchronize()
+    moe.check_status(ws)
 
 
 def max_over_ranks(values, world, device):
@@ -560,6 +597,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.dispatch_only:
+        run_dispatch_only(args)
         return
     import torch
     if world > 1:
