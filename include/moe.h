@@ -31,7 +31,9 @@
  *    pointer is a DEVICE pointer on the current CUDA device.  The library never
  *    allocates device memory; scratch comes from the caller's workspace `ws`
  *    of at least moe_workspace_size() bytes, initialised once with
- *    moe_workspace_init().
+ *    moe_workspace_init().  A workspace serves one call at a time: calls that
+ *    share one must be ordered (the same stream, or streams joined by
+ *    events), since its header holds counters each call leaves at zero.
  *  - Execution: every call validates its arguments on the host first; on an
  *    error it returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
  *    MOE_ERR_WORKSPACE with NOTHING enqueued.  Otherwise it enqueues kernels on
