@@ -1,19 +1,22 @@
 """Benchmark of the MoE-layer forward pass on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--only]
                     [--impl ours|reference] [--no-cpu-baseline]
 
 A step is one pass of the whole layer (moe_forward: route -> permute ->
 grouped FFN -> combine) over one batch of seeded synthetic tokens, through
-the C ABI, replayed from one CUDA graph.  The
-default workload is the Switch-style top-1 layer with capacity (T=4096,
-768 -> 3072 -> 768, E=64, CF=1.25, bf16).  Prints one JSON line (rank 0).
+the C ABI, replayed from one CUDA graph.  The headline workload is the largest
+one a single GPU holds among the problem statement's: the Mixtral-shaped layer
+(T=8192, 4096 -> 14336 -> 4096, E=8, top-2 on logits, bf16).  Every other
+workload is measured in the same run and printed as a sub-record under
+"workloads" (--only skips them).  Prints one JSON line (rank 0).
 
 Timing: W untimed warm-up steps; then K steps bracketed by a barrier and a
 device synchronise.  L2 is flushed (a 256 MB write) before every step, outside
 the per-step CUDA events whose sum gives the device time.  The grouped FFN
-(the dominant kernel pair, the roofline figure) and the combine are then timed
-the same way from graphs of their own entry points on the same stream.  The
+(the dominant kernel pair, the roofline figure), routing, permute and the
+combine are then timed the same way from graphs of their own entry points on
+the same stream.  The
 end-to-end figure repeats the step through moe_forward with the tokens copied
 in from pinned host memory and the output (and aux) copied back every step.
 
@@ -22,7 +25,8 @@ own GPU (the path has no exchange step); value = all ranks' tokens / the
 slowest rank's time.
 
 --impl reference times the CPU oracle (the plain float64 restatement of the
-pages) on the host cores, on a bounded token sample of the same workload.
+pages) on the host cores, on a bounded token sample of the same workload,
+drawn from the same seeded generator.
 """
 
 from __future__ import annotations
@@ -41,7 +45,12 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "switch_top1_cap"
+DEFAULT_WORKLOAD = "mixtral_top2"
+# the other workloads, measured in the same run as sub-records of the line
+SUB_WORKLOADS = ["switch_top1_cap", "deepseek_v3_top8", "decode_zipf_top2", "tiny_fp32_top2",
+                 "switch_expert_choice", "mixtral_swiglu_top2"]
+HEADLINE_TIMED_MS = 1500.0     # device time of the headline's timed region (auto steps)
+SUB_TIMED_MS = 600.0           # the same for each sub-record
 METRIC = "MoE-layer fwd tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -67,6 +76,8 @@ def parse():
                          "workload's token batch (no expert weights) and exit: the command "
                          "for per-kernel ncu captures of those steps at full size")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true",
+                    help="measure the named workload alone (no sub-records)")
     ap.add_argument("--cpu-rows", type=int, default=None)
     return ap.parse_args()
 
@@ -278,14 +289,38 @@ def whole_job_tokens_per_s(T, world, steps, slowest_ms):
     return world * T * steps / (slowest_ms / 1e3)
 
 
-def run_ours(args, rank, world, local_rank):
+def line_config(cfg, world) -> dict:
+    """The `config` object of a JSON line: the workload as the layer's problem
+    statement names it.  Both arms print the same dict for the same workload."""
+    return {"workload": cfg["name"], "T": cfg["T"], "d_model": cfg["d_model"],
+            "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"], "act": cfg.get("act", "gelu"),
+            "n_shared": cfg.get("n_shared", 0), "capacity_factor": cfg["capacity_factor"],
+            "route": cfg["route"], "dtype": cfg["dtype"], "parallelism": f"replicas x{world}",
+            "l2": "flushed (256 MB write) before every step, outside the step events"}
+
+
+def draw_inputs(cfg, seed, device):
+    """The seeded inputs of one workload.  Both arms draw them with the same
+    generator on the GPU when there is one (the reference arm then copies them
+    to the host), so they route the same numbers."""
     import torch
-    from sparse_mixture_experts_52_b300 import moe, synth
+    from sparse_mixture_experts_52_b300 import synth
+    if device is None:
+        device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    return synth.make_inputs(cfg, device=device, seed=seed)
+
+
+def measure(args, cfg, rank, world, local_rank, steps, timed_ms, cpu_leg):
+    """Times one workload on this rank's GPU: the whole-layer step (a CUDA
+    graph of moe_forward), the grouped FFN, routing, permute and combine each
+    in a graph of their own, and the end-to-end step through the public API
+    with host buffers.  Returns the raw figures (max over ranks)."""
+    import torch
+    from sparse_mixture_experts_52_b300 import moe
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    cfg = synth.workload(args.workload)
-    inp = synth.make_inputs(cfg, device=dev, seed=cfg.get("seed", 0) + rank)
+    inp = draw_inputs(cfg, cfg.get("seed", 0) + rank, dev)
     T, d, E, k, S = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"], cfg.get("n_shared", 0)
     dt = moe.TORCH_DTYPES[cfg["dtype"]]
     elem = 2 if cfg["dtype"] == "bf16" else 4
@@ -301,9 +336,10 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(g_fwd):
         layer(inp["x"])
 
-    # ---- the dominant kernel pair (grouped FFN) and the combine on the same
-    # workspace state, each in its own graph, for the roofline and the split
+    # ---- the dominant kernel pair (grouped FFN), routing, permute and the
+    # combine through their own entry points, each in its own graph
     z = lambda shape, t: torch.empty(shape, dtype=t, device=dev)
+    f32 = torch.float32
     ec = moe.expert_choice(cfg)
     R = moe.routed_rows(cfg)
     o = dict(counts=z((E,), torch.int32), kept=z((E,), torch.int32),
@@ -312,40 +348,11 @@ def run_ours(args, rank, world, local_rank):
              y_perm=z((R, d), dt), out=z((T, d), dt))
     y_sh = z((S, T, d), dt) if S else None
     ws2 = moe.new_workspace(cfg, dev)
-    if ec:
-        # the slot table of the same selection (moe_forward keeps it in its workspace)
-        C = moe.expert_capacity(cfg)
-        o["ec_slot"] = z((E, T), torch.int32)
-        moe.route_expert_choice(cfg, inp["x"], inp["w_g"], z((E, C), torch.int32),
-                                z((E, C), torch.float32), o["ec_slot"], z((E,), torch.float32),
-                                z((E,), torch.float32), z((1,), torch.float32), ws2,
-                                logit_bias=inp.get("logit_bias"))
-        moe.permute_expert_choice(cfg, inp["x"], layer.topk_idx, o["offsets"], o["x_perm"])
-        o["kept"].fill_(C)
-    else:
-        moe.permute(cfg, inp["x"], layer.topk_idx, o["counts"], o["kept"], o["offsets"],
-                    o["perm_token"], o["slot_of"], o["x_perm"], ws2)
-
-    def part_ffn():
-        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws2,
-                        b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
-                        wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
-                        y_shared=y_sh)
-
-    def part_combine():
-        if ec:
-            moe.combine_expert_choice(cfg, o["y_perm"], o["ec_slot"], layer.topk_w, o["out"],
-                                      y_shared=y_sh)
-        else:
-            moe.combine(cfg, o["y_perm"], o["slot_of"], layer.topk_w, o["out"], y_shared=y_sh)
-
-    # routing and dispatch through their own entry points (the whole-layer pass
-    # runs the same kernels, except that its routing grid also ranks the
-    # assignments, which moe_permute does in one more small kernel)
-    f32 = torch.float32
     r_stats = dict(f=z((E,), f32), P=z((E,), f32), aux=z((1,), f32))
     if ec:
-        r_sel = (z((E, C), torch.int32), z((E, C), f32), z((E, T), torch.int32))
+        C = moe.expert_capacity(cfg)
+        o["ec_slot"] = z((E, T), torch.int32)
+        r_sel = (z((E, C), torch.int32), z((E, C), f32), o["ec_slot"])
 
         def part_route():
             moe.route_expert_choice(cfg, inp["x"], inp["w_g"], *r_sel, r_stats["f"],
@@ -354,6 +361,7 @@ def run_ours(args, rank, world, local_rank):
 
         def part_permute():
             moe.permute_expert_choice(cfg, inp["x"], r_sel[0], o["offsets"], o["x_perm"])
+        o["kept"].fill_(C)
     else:
         r_sel = (z((T, k), torch.int32), z((T, k), f32))
 
@@ -366,12 +374,27 @@ def run_ours(args, rank, world, local_rank):
             moe.permute(cfg, inp["x"], r_sel[0], o["counts"], o["kept"], o["offsets"],
                         o["perm_token"], o["slot_of"], o["x_perm"], ws2)
 
+    def part_ffn():
+        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws2,
+                        b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
+                        wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
+                        y_shared=y_sh)
+
+    def part_combine():
+        if ec:
+            moe.combine_expert_choice(cfg, o["y_perm"], o["ec_slot"], r_sel[1], o["out"],
+                                      y_shared=y_sh)
+        else:
+            moe.combine(cfg, o["y_perm"], o["slot_of"], r_sel[1], o["out"], y_shared=y_sh)
+
     part_route()
     part_permute()
     part_ffn()
     part_combine()
     torch.cuda.synchronize(dev)
     moe.check_status(ws2)
+    kept = o["kept"].cpu().tolist()
+    byt, flops, n_a, active = algorithmic_ffn(cfg, kept, elem)
     g_route, g_perm = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     g_ffn, g_comb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_route):
@@ -383,12 +406,12 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(g_comb):
         part_combine()
 
-    w_ms = _timed_graph_loop(g_fwd, flush, stream, max(3, args.warmup))
+    warm = max(3, args.warmup)
+    w_ms = _timed_graph_loop(g_fwd, flush, stream, warm)
     moe.check_status(layer.ws)
-    if args.steps <= 0:
+    if steps <= 0:
         t_step = max(min(w_ms), 1e-3)
-        args.steps = int(min(20000, max(20, math.ceil(1500.0 / t_step))))
-    args.warmup = max(3, args.warmup)
+        steps = int(min(20000, max(20, math.ceil(timed_ms / t_step))))
 
     sampler = ClockSampler(local_rank)
     time.sleep(0.5)
@@ -397,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_wall0 = time.perf_counter()
     sampler.begin()
-    step_ms = _timed_graph_loop(g_fwd, flush, stream, args.steps)
+    step_ms = _timed_graph_loop(g_fwd, flush, stream, steps)
     sampler.end()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
@@ -406,16 +429,14 @@ def run_ours(args, rank, world, local_rank):
     moe.check_status(layer.ws)
     dev_ms = sum(step_ms)
 
-    n_part = max(20, args.steps // 4)
+    n_part = max(20, steps // 4)
     _timed_graph_loop(g_ffn, flush, stream, 3)
     ffn_ms = statistics.fmean(_timed_graph_loop(g_ffn, flush, stream, n_part))
     cb_ms = statistics.fmean(_timed_graph_loop(g_comb, flush, stream, n_part))
     ro_ms = statistics.fmean(_timed_graph_loop(g_route, flush, stream, n_part))
     pe_ms = statistics.fmean(_timed_graph_loop(g_perm, flush, stream, n_part))
     moe.check_status(ws2)
-
-    kept = o["kept"].cpu().tolist()
-    byt, flops, n_a, active = algorithmic_ffn(cfg, kept, elem)
+    del g_route, g_perm, g_ffn, g_comb, o, ws2, y_sh, r_sel, r_stats
 
     # ---- end to end through the public API, host buffers: StreamedMoELayer
     # (graphed moe_forward, the copy-in of step i+1 and the copy-out of step
@@ -425,7 +446,7 @@ def run_ours(args, rank, world, local_rank):
     out_host = torch.empty((T, d), dtype=dt).pin_memory()
     aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
     slayer = moe.StreamedMoELayer(cfg, inp, device=dev)
-    for _ in range(max(3, args.warmup)):
+    for _ in range(warm):
         slayer.submit(x_host, out_host, aux_host)
     slayer.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -433,108 +454,131 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     e0.record(slayer.s_in)       # before the first copy-in (the other streams follow it)
-    for _ in range(args.steps):
+    for _ in range(steps):
         slayer.submit(x_host, out_host, aux_host)
     e1.record(slayer.s_out)      # after the last copy-out
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
     slayer.synchronize()
+    del slayer
 
     # ---- max over ranks
-    dev_ms, e2e_ms, ffn_ms = max_over_ranks([dev_ms, e2e_ms, ffn_ms], world, dev)
+    dev_ms, e2e_ms, ffn_ms, ro_ms, pe_ms, cb_ms = max_over_ranks(
+        [dev_ms, e2e_ms, ffn_ms, ro_ms, pe_ms, cb_ms], world, dev)
 
-    res = dict(cfg=cfg, dev_ms=dev_ms, e2e_ms=e2e_ms, ffn_ms=ffn_ms,
-               ro_ms=ro_ms, pe_ms=pe_ms, cb_ms=cb_ms,
-               rpc_bytes=rpc_bytes(cfg, n_a, elem),
-               bytes=byt, flops=flops,
+    res = dict(cfg=cfg, steps=steps, warmup=warm, dev_ms=dev_ms, e2e_ms=e2e_ms,
+               ffn_ms=ffn_ms, ro_ms=ro_ms, pe_ms=pe_ms, cb_ms=cb_ms,
+               rpc_bytes=rpc_bytes(cfg, n_a, elem), bytes=byt, flops=flops,
                n_a=n_a, active=active, clocks=clocks, wall_s=t_wall,
                counts=layer.counts.cpu().tolist(), aux=float(layer.aux.cpu()[0]),
                h2d=x_host.numel() * x_host.element_size(),
                d2h=out_host.numel() * out_host.element_size() + 4)
-    if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
-            res["cpu"] = cpu_baseline(cfg, inp, args)
+    del layer, g_fwd, x_host, out_host, aux_host, flush
+    if cpu_leg and rank == 0 and world == 1:
+        res["cpu"] = cpu_baseline(cfg, inp, args)
+    del inp
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
     return res
 
 
-def cpu_baseline(cfg, inp, args, reps: int = 1):
-    """The oracle as it stands, on the host cores, on a bounded token sample."""
-    import numpy as np
-    import torch
+def _oracle_seconds(cfg, host, rows):
     from oracle import compare
+    t0 = time.perf_counter()
+    compare.run_oracle(cfg, host, rows=rows)
+    return time.perf_counter() - t0
 
-    rows_n = args.cpu_rows or CPU_SAMPLE_ROWS.get(cfg["name"], 256)
-    rows_n = min(rows_n, cfg["T"])
-    rows = np.arange(rows_n)
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_sample(cfg, args):
+    """Rows (tokens) whose expert FFNs the timed oracle computes, and the
+    description of that sample."""
+    import numpy as np
+    rows_n = min(args.cpu_rows or CPU_SAMPLE_ROWS.get(cfg["name"], 256), cfg["T"])
+    text = (f"float64 numpy oracle: routing, statistics and dispatch of all {cfg['T']} "
+            f"tokens, expert FFNs of the first {rows_n} tokens; value = {rows_n} tokens / "
+            f"wall time")
+    return np.arange(rows_n), text
+
+
+def cpu_baseline(cfg, inp, args):
+    """The oracle as it stands, on the host cores, on a bounded token sample:
+    once with every core this process may run on (BLAS threads = the affinity
+    mask) and once single-threaded.  `value` is the all-cores figure."""
+    import torch
+    rows, text = cpu_sample(cfg, args)
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    threads = None
+    cores = host_cores()
     try:
-        from threadpoolctl import threadpool_info
-        threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=None)
-    except Exception:
-        threads = None
-    times = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
-        compare.run_oracle(cfg, host, rows=rows)
-        times.append(time.perf_counter() - t0)
-    t = min(times)
-    return {"value": rows_n / t, "unit": "tokens/s", "cores": threads or os.cpu_count(),
-            "kind": "oracle", "seconds": t,
-            "sample": (f"float64 numpy oracle: routing, statistics and dispatch of all "
-                       f"{cfg['T']} tokens, expert FFNs of the first {rows_n} tokens; "
-                       f"value = {rows_n} tokens / wall time")}
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    runs = {}
+    for n in (cores, 1):
+        if threadpool_limits is None:      # no thread control: one run at the default
+            runs[n] = _oracle_seconds(cfg, host, rows)
+            break
+        with threadpool_limits(limits=n):
+            runs[n] = _oracle_seconds(cfg, host, rows)
+    out = {"value": len(rows) / runs[cores], "unit": "tokens/s", "cores": cores,
+           "kind": "oracle", "seconds": runs[cores], "sample": text}
+    if 1 in runs and cores != 1:
+        out["single_thread"] = {"value": len(rows) / runs[1], "unit": "tokens/s", "cores": 1,
+                                "seconds": runs[1]}
+    return out
 
 
-def emit_ours(args, res, world):
+def record(res, world, peaks, peak_src) -> dict:
+    """The measured figures of one workload as JSON fields."""
     cfg = res["cfg"]
-    peaks, peak_src = load_peaks()
-    T = cfg["T"]
-    ms = res["dev_ms"] / args.steps
-    tokens_s = whole_job_tokens_per_s(T, world, args.steps, res["dev_ms"])
+    T, steps = cfg["T"], res["steps"]
+    ms = res["dev_ms"] / steps
+    tokens_s = whole_job_tokens_per_s(T, world, steps, res["dev_ms"])
     ffn_s = res["ffn_ms"] / 1e3
     gbs = res["bytes"] / ffn_s / 1e9
     tfl = res["flops"] / ffn_s / 1e12
     t_hbm = res["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    # a timed region of seconds runs under the power cap: its tensor fraction is
+    # taken against the sustained peak; the burst (dense) peak is reported beside it
     long_region = res["dev_ms"] > 1000.0
-    tc_peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    tc_dense = peaks["bf16_tflops"]
+    tc_peak = peaks["bf16_tflops_sustained"] if long_region else tc_dense
     t_tc = res["flops"] / (tc_peak * 1e12)
-    traffic = profiled_traffic(cfg["name"])
     if cfg["dtype"] == "bf16" and t_tc > t_hbm:
         roof = {"bound": "tensor", "achieved": round(tfl, 2), "peak": tc_peak,
-                "unit": "TFLOP/s", "frac": round(tfl / tc_peak, 4)}
+                "unit": "TFLOP/s", "frac": round(tfl / tc_peak, 4),
+                "frac_dense": round(tfl / tc_dense, 4)}
     else:
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = traffic
-    roof["kernel"] = "grouped FFN (tcgen05 up-proj+GELU and down-proj launches)"
-    roof["peak_source"] = f"{peak_src} ({'sustained' if long_region and roof['unit'] == 'TFLOP/s' else 'burst'})"
+    roof["traffic"] = profiled_traffic(cfg["name"])
+    roof["kernel"] = "grouped FFN (tcgen05 up-projection + activation and down-projection)"
+    sustained = long_region and roof["unit"] == "TFLOP/s"
+    roof["peak_source"] = f"{peak_src} ({'sustained' if sustained else 'burst'})"
     roof["algorithmic_bytes"] = res["bytes"]
     roof["algorithmic_flops"] = res["flops"]
     roof["ms_per_launch"] = round(res["ffn_ms"], 4)
-    e2e_val = whole_job_tokens_per_s(T, world, args.steps, res["e2e_ms"])
+    e2e_val = whole_job_tokens_per_s(T, world, steps, res["e2e_ms"])
     rpc_ms = res["ro_ms"] + res["pe_ms"] + res["cb_ms"]
     rpc_gbs = res["rpc_bytes"] / (rpc_ms / 1e3) / 1e9
     counts = res["counts"]
-    line = {
-        "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": cfg["dtype"], "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))",
-        "config": {"workload": cfg["name"], "T": T, "d_model": cfg["d_model"],
-                   "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"],
-                   "act": cfg.get("act", "gelu"),
-                   "n_shared": cfg.get("n_shared", 0), "capacity_factor": cfg["capacity_factor"],
-                   "route": cfg["route"], "parallelism": f"replicas x{world}",
-                   "l2": "flushed (256 MB write) before every step, outside the step events"},
+    mean_count = max(sum(counts) / len(counts), 1e-30)
+    return {
+        "value": round(tokens_s, 1), "unit": "tokens/s", "steps": steps,
+        "warmup": res["warmup"], "ms_per_step": round(ms, 4), "dtype": cfg["dtype"],
+        "config": line_config(cfg, world),
         "roofline": roof,
         "grouped_ffn": {"tflops": round(tfl, 2), "gbs": round(gbs, 1),
                         "tensor_frac": round(tfl / tc_peak, 4),
+                        "tensor_frac_dense": round(tfl / tc_dense, 4),
                         "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
                         "rows": res["n_a"], "active_experts": res["active"]},
         "routing_stats": {"aux": res["aux"], "max_count": max(counts),
                           "min_count": min(counts),
-                          "imbalance_ratio": round(max(counts) / (sum(counts) / len(counts)), 3)},
+                          "imbalance_ratio": round(max(counts) / mean_count, 3)},
         "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"],
                 "api": "StreamedMoELayer (graphed moe_forward; copy-in of step i+1 and copy-out of step i-1 overlap step i), pinned host x in, out+aux back every step"},
@@ -545,46 +589,71 @@ def emit_ours(args, res, world):
             "achieved": round(rpc_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(rpc_gbs / peaks["hbm_gbs"], 4),
             "api": "moe_route + moe_permute + moe_combine (each in its own CUDA graph, L2 flushed)"},
-        "gpu_launches": kernel_launches_per_step(cfg) * args.steps,
+        "gpu_launches": kernel_launches_per_step(cfg) * steps,
         "clocks": res["clocks"],
         "wall_s_timed": round(res["wall_s"], 3),
     }
+
+
+def run_ours(args, rank, world, local_rank) -> dict:
+    """The headline workload, then (unless --only) every other workload as a
+    sub-record of the same line."""
+    from sparse_mixture_experts_52_b300 import synth
+
+    peaks, peak_src = load_peaks()
+    cfg = synth.workload(args.workload)
+    res = measure(args, cfg, rank, world, local_rank, args.steps, HEADLINE_TIMED_MS,
+                  cpu_leg=not args.no_cpu_baseline)
+    rec = record(res, world, peaks, peak_src)
+    line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": rec["steps"], "warmup": rec["warmup"], "ms_per_step": rec["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": rec["dtype"], "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))"}
+    line.update({k: v for k, v in rec.items() if k not in line})
     if "cpu" in res:
         line["cpu_baseline"] = res["cpu"]
-    print(json.dumps(line), flush=True)
+    if not args.only:
+        subs = {}
+        for name in SUB_WORKLOADS:
+            if name == cfg["name"]:
+                continue
+            r = measure(args, synth.workload(name), rank, world, local_rank, 0, SUB_TIMED_MS,
+                        cpu_leg=False)
+            subs[name] = record(r, world, peaks, peak_src)
+        line["workloads"] = subs
+    return line
 
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
-    """The oracle timed as it stands on the host cores (rank 0 only)."""
+    """The oracle timed as it stands on the host cores (rank 0 only), on the
+    same config and the same seeded inputs as our arm."""
     if rank != 0:
         return
     import torch
     from sparse_mixture_experts_52_b300 import synth
 
     cfg = synth.workload(args.workload)
-    inp = synth.make_inputs(cfg, device="cpu")
-    cpu = None
+    inp = draw_inputs(cfg, cfg.get("seed", 0), None)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    del inp
+    rows, text = cpu_sample(cfg, args)
     samples = []
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(cfg, inp, args)
+        t = _oracle_seconds(cfg, host, rows)
         if i >= args.warmup:
-            samples.append(r["seconds"])
-            cpu = r
+            samples.append(t)
     t = sum(samples)
-    rows = cpu["value"] * cpu["seconds"]
-    value = rows * args.steps / t
+    value = len(rows) * max(args.steps, 1) / max(t, 1e-12)
     line = {"metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "ms_per_step": round(1e3 * t / max(args.steps, 1), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded: x~N(0,1), weights~N(0,1/fan_in))",
-            "config": {"workload": cfg["name"], "T": cfg["T"], "d_model": cfg["d_model"],
-                       "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"],
-                       "act": cfg.get("act", "gelu")},
+            "config": line_config(cfg, world),
             "impl": "reference",
-            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
-                             "cores": cpu["cores"], "kind": "oracle", "sample": cpu["sample"]},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": host_cores(),
+                             "kind": "oracle", "sample": text},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -606,9 +675,9 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        res = run_ours(args, rank, world, local_rank)
+        line = run_ours(args, rank, world, local_rank)
         if rank == 0:
-            emit_ours(args, res, world)
+            print(json.dumps(line), flush=True)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

@@ -112,6 +112,11 @@ typedef struct {
   float aux_alpha;         /* alpha of the aux loss                         */
   int32_t aux_f;           /* moe_aux_f                                     */
   int32_t act;             /* moe_act: the experts' hidden activation        */
+  int32_t y_f32;           /* 0: the expert outputs (y_perm, y_shared) are in
+                              dtype; 1: they are fp32 (a bf16 layer then rounds
+                              its expert outputs once, in the combine, instead
+                              of twice).  Read by moe_grouped_ffn, moe_combine,
+                              moe_combine_expert_choice and moe_forward.     */
 } moe_config;
 
 /* Bytes of workspace the entry points below need for `cfg` (host only). */
@@ -191,10 +196,11 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
  *   F1 = 2F for MOE_ACT_SWIGLU (gate rows, then up rows) and F otherwise.
  *   Shared experts (cfg.n_shared > 0): x [T,d], ws1 [S,F1,d], wsb1 [S,F1] or
  *   NULL, ws2 [S,d,F], wsb2 [S,d] or NULL, output y_shared [S,T,d] dtype.
- *   Output y_perm [T*k, d] dtype: row r = FFN_e(x_perm[r]) for the expert e
+ *   Output y_perm [T*k, d]: row r = FFN_e(x_perm[r]) for the expert e
  *   whose range holds r; rows >= offsets[E] unspecified.  Both GEMMs
- *   accumulate in fp32; the hidden activation [rows, F] (in `ws`) and the
- *   expert outputs are rounded once to dtype. */
+ *   accumulate in fp32; the hidden activation [rows, F] (in `ws`) is rounded
+ *   once to dtype, the expert outputs y_perm and y_shared once to dtype, or
+ *   stored in fp32 when cfg->y_f32 = 1. */
 moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                            const void* w1, const void* b1, const void* w2, const void* b2,
                            const void* x, const void* ws1, const void* wsb1,
@@ -205,7 +211,8 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int3
 /* Gate-weighted un-permute: out[t] = sum_{j: slot_of[t*k+j] >= 0}
  * topk_w[t,j] * y_perm[slot_of[t*k+j]] + sum_s y_shared[s,t], accumulated in
  * fp32 in ascending j then s, stored once in dtype.  y_perm [T*k, d] and
- * y_shared [S,T,d] are in dtype; y_shared may be NULL when n_shared = 0. */
+ * y_shared [S,T,d] are in dtype (fp32 when cfg->y_f32 = 1); y_shared may be
+ * NULL when n_shared = 0. */
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_of,
                        const float* topk_w, const void* y_shared, void* out,
                        moe_stream stream);

@@ -112,11 +112,27 @@ class Report:
 
 
 def _near_tie_and_override(ref: om.ForwardResult, gpu_idx: np.ndarray):
+    """Near-tie tokens, and the device's choice for those among them where it
+    differs from the oracle's.  Such a choice must still be a valid top-k up to
+    the margin: k distinct experts in [0, E), each scoring at least the k-th
+    best score minus NEAR_TIE, listed in descending score up to NEAR_TIE."""
     nt = np.nonzero(ref.gate.margin < NEAR_TIE)[0]
     override = {}
+    E = ref.gate.p.shape[1]
     for t in nt:
-        if not np.array_equal(gpu_idx[t], ref.gate.idx[t]):
-            override[int(t)] = gpu_idx[t].astype(np.int64)
+        if np.array_equal(gpu_idx[t], ref.gate.idx[t]):
+            continue
+        g = np.asarray(gpu_idx[t]).astype(np.int64)
+        k = g.size
+        assert np.all((g >= 0) & (g < E)) and len(set(g.tolist())) == k, \
+            f"token {t}: device experts {g.tolist()} are not k distinct experts"
+        sc = ref.gate.score[t]
+        kth = np.sort(sc)[::-1][k - 1]
+        assert sc[g].min() >= kth - NEAR_TIE, \
+            f"token {t}: device experts {g.tolist()} are not a top-{k} set (scores {sc[g]})"
+        assert np.all(sc[g][:-1] >= sc[g][1:] - NEAR_TIE), \
+            f"token {t}: device experts {g.tolist()} are not in descending score order"
+        override[int(t)] = g
     return [int(t) for t in nt], override
 
 

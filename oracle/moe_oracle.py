@@ -140,6 +140,7 @@ class GateResult:
     w: np.ndarray         # [T,k] float64 gate weights
     p: np.ndarray         # [T,E] float64 unbiased softmax of the logits
     margin: np.ndarray    # [T] selection-score margin (see select_topk)
+    score: Optional[np.ndarray] = None   # [T,E] float64 selection score (p, l or p + b)
 
 
 def gate(logits: np.ndarray, cfg: OracleConfig,
@@ -188,7 +189,7 @@ def gate(logits: np.ndarray, cfg: OracleConfig,
             w = sel / sel.sum(axis=-1, keepdims=True)   # R16: sum >= max p > 0
         else:
             w = sel
-    return GateResult(idx=idx, w=w, p=p, margin=margin)
+    return GateResult(idx=idx, w=w, p=p, margin=margin, score=score)
 
 
 # --------------------------------------------------------------------------

@@ -13,6 +13,8 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = [
     "-std=c++17", "-O3", "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
     "-gencode", "arch=compute_103a,code=sm_103a",
+    # device code optimised and assembled in parallel partitions (all host cores)
+    "-split-compile=0",
     "-I", os.path.join(ROOT, "include"),
     "-I", os.path.join(HERE, "csrc"),
 ]

@@ -208,16 +208,18 @@ struct Raw8<float> {
 };
 
 // out[t] = sum_j w[t,j] * y[slot_of[t,j]] + sum_s y_shared[s,t]: one warp per
-// token, fp32 sums in ascending j then s, one rounding.  The rows of up to
+// token, fp32 sums in ascending j then s, one rounding.  The expert outputs
+// (TY) are in the layer dtype, or fp32 for a bf16 layer that keeps them so;
+// out is in the layer dtype (TO).  The rows of up to
 // eight slots (four for fp32; U 16-byte vectors per lane each, kept packed as
 // loaded) are requested together before any is summed, so a warp has up to
 // 8 * U * 512 bytes in flight; 64 registers a thread let every token of a
 // 4096-token batch hold a warp at once.
-template <typename TE, int KMAX, int U>
+template <typename TY, typename TO, int KMAX, int U>
 __global__ void __launch_bounds__(256, 4)
-k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
-          const float* __restrict__ w, const TE* __restrict__ y_shared, int n_shared, int T,
-          int k, int d, TE* __restrict__ out) {
+k_combine(const TY* __restrict__ y, const int32_t* __restrict__ slot_of,
+          const float* __restrict__ w, const TY* __restrict__ y_shared, int n_shared, int T,
+          int k, int d, TO* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -232,7 +234,7 @@ k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
       my_w = __ldg(w + static_cast<int64_t>(t) * k + lane);
     }
     // slots whose rows are in flight together (fp32 vectors take twice the registers)
-    constexpr int QMAX = sizeof(TE) == 2 ? 8 : 4;
+    constexpr int QMAX = sizeof(TY) == 2 ? 8 : 4;
     constexpr int Q = KMAX < QMAX ? KMAX : QMAX;
     for (int c0 = 0; c0 < nchunk; c0 += 32 * U) {
       float acc[U][8];
@@ -242,7 +244,7 @@ k_combine(const TE* __restrict__ y, const int32_t* __restrict__ slot_of,
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
 #pragma unroll
       for (int j0 = 0; j0 < KMAX; j0 += Q) {
-        Raw8<TE> v[Q][U];
+        Raw8<TY> v[Q][U];
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
           const int s = __shfl_sync(0xffffffffu, my_slot, j0 + q);

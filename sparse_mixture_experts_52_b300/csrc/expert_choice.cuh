@@ -390,13 +390,14 @@ k_ec_gather(const int32_t* __restrict__ ec_token, int rows, int row_bytes, int C
 // table is given, else the weights from the [E, C] list through the slots),
 // then the rows of the taken experts are summed in ascending expert order,
 // the loads of two experts' rows (U 16-byte vectors per lane each) in flight
-// together.
-template <typename TE, int U, int NJ>
+// together.  TY: the expert outputs' type (the layer dtype, or fp32 for a
+// bf16 layer that keeps them so); TO: the layer dtype.
+template <typename TY, typename TO, int U, int NJ>
 __global__ void __launch_bounds__(256, 3)
-k_ec_combine(const TE* __restrict__ y, const int32_t* __restrict__ ec_slot,
+k_ec_combine(const TY* __restrict__ y, const int32_t* __restrict__ ec_slot,
              const float* __restrict__ ec_wt, const float* __restrict__ ec_w,
-             const TE* __restrict__ y_shared, int n_shared, int T, int E, int d,
-             TE* __restrict__ out) {
+             const TY* __restrict__ y_shared, int n_shared, int T, int E, int d,
+             TO* __restrict__ out) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -439,7 +440,7 @@ k_ec_combine(const TE* __restrict__ y, const int32_t* __restrict__ ec_slot,
               w[q] = __shfl_sync(0xffffffffu, wt[j], b);
             }
           }
-          Raw8<TE> v[Q][U];
+          Raw8<TY> v[Q][U];
 #pragma unroll
           for (int q = 0; q < Q; ++q)
 #pragma unroll

@@ -48,7 +48,8 @@
 
 namespace moe {
 
-// Epilogues: fp32 logits (router); GELU(acc + b1) or SiLU(acc + b1) in bf16
+// Epilogues: acc (+ bias) in fp32 (router logits, without bias; expert outputs
+// kept in fp32); GELU(acc + b1) or SiLU(acc + b1) in bf16
 // (up-projection); acc + b2 in bf16 (down-projection); the down-projection
 // fused with the top-1 combine: out[token of the row] = w[token] * (acc + b2)
 // in bf16; and SwiGLU, where the tile's BN accumulator columns are two halves
@@ -455,7 +456,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         orow = tok;
       }
       const __nv_bfloat16* bias = nullptr;
-      if (EPI != EPI_F32) {
+      {
         const int64_t bstride = GLU ? 2 * static_cast<int64_t>(args.N) : args.N;
         if (routed && args.bias0) bias = args.bias0 + static_cast<int64_t>(gs.offsets ? g : 0) * bstride;
         if (!routed && args.bias1) bias = args.bias1 + static_cast<int64_t>(g - gs.E) * bstride;
@@ -491,7 +492,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
         add_partials(cc, v);
-        if (EPI != EPI_F32 && bias) {
+        if (bias) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (col + i < args.N) v[i] += __bfloat162float(bias[col + i]);

@@ -50,6 +50,8 @@ inline int next_pow2_min16(int v) {
 }
 
 inline size_t elem_bytes(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+// expert outputs (y_perm, y_shared): the layer dtype, or fp32 when cfg.y_f32
+inline size_t y_bytes(const moe_config& c) { return c.y_f32 ? 4 : elem_bytes(c); }
 
 moe_status validate(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -64,6 +66,7 @@ moe_status validate(const moe_config* c) {
   if (c->aux_f != MOE_AUX_TOPK_COUNT && c->aux_f != MOE_AUX_ARGMAX) return MOE_ERR_INVALID_ARG;
   if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_INVALID_ARG;
   if (c->has_bias != 0 && c->has_bias != 1) return MOE_ERR_INVALID_ARG;
+  if (c->y_f32 != 0 && c->y_f32 != 1) return MOE_ERR_INVALID_ARG;
   if (c->act < MOE_ACT_GELU || c->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha))
     return MOE_ERR_INVALID_ARG;
@@ -160,8 +163,8 @@ Layout make_layout(const moe_config& c) {
   L.ec_wt = take(ec ? E * T * 4 : 0);
   L.x_perm = take(rows * d * eb);
   L.H = take((rows + S * T) * F * eb);
-  L.Y = take(rows * d * eb);
-  L.Ys = take(S * T * d * eb);
+  L.Y = take(rows * d * y_bytes(c));
+  L.Ys = take(S * T * d * y_bytes(c));
   // stream-K partial tiles of the tensor-core FFN: one 128 x 256 fp32 slot per CTA
   L.sk_part = take(c.dtype == MOE_BF16 ? static_cast<size_t>(kMaxGemmCtas) * 128 * 256 * 4 : 0);
   L.total = off;
@@ -712,17 +715,17 @@ moe_status do_permute_ec(const moe_config& c, const void* x, const int32_t* ec_t
                     static_cast<const uint8_t*>(x), static_cast<uint8_t*>(x_perm), offsets);
 }
 
-template <typename TE, int U>
+template <typename TY, typename TO, int U>
 moe_status launch_ec_combine(const moe_config& c, int grid, const void* y_perm,
                              const int32_t* ec_slot, const float* ec_wt, const float* ec_w,
                              const void* y_shared, int S, void* out, cudaStream_t st) {
   auto go = [&](auto kern) {
-    return launch_pdl(kern, dim3(grid), dim3(256), 0, st, static_cast<const TE*>(y_perm),
-                      ec_slot, ec_wt, ec_w, static_cast<const TE*>(y_shared), S, c.T, c.E,
-                      c.d_model, static_cast<TE*>(out));
+    return launch_pdl(kern, dim3(grid), dim3(256), 0, st, static_cast<const TY*>(y_perm),
+                      ec_slot, ec_wt, ec_w, static_cast<const TY*>(y_shared), S, c.T, c.E,
+                      c.d_model, static_cast<TO*>(out));
   };
-  if (c.E <= 64) return go(k_ec_combine<TE, U, 2>);   // two groups of 32 experts per lane
-  return go(k_ec_combine<TE, U, kMaxExperts / 32>);
+  if (c.E <= 64) return go(k_ec_combine<TY, TO, U, 2>);   // two groups of 32 experts per lane
+  return go(k_ec_combine<TY, TO, U, kMaxExperts / 32>);
 }
 
 // bf16 rows: up to three 16-byte vectors per lane and pass (the whole row in
@@ -731,12 +734,16 @@ moe_status launch_ec_combine_dt(const moe_config& c, int grid, const void* y_per
                                 const int32_t* ec_slot, const float* ec_wt, const float* ec_w,
                                 const void* y_shared, int S, void* out, cudaStream_t st) {
   if (c.dtype != MOE_BF16)
-    return launch_ec_combine<float, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+    return launch_ec_combine<float, float, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S,
+                                              out, st);
   using B = __nv_bfloat16;
+  if (c.y_f32)   // fp32 expert outputs of a bf16 layer
+    return launch_ec_combine<float, B, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S,
+                                          out, st);
   const int u = std::min(3, (c.d_model / 8 + 31) / 32);
-  if (u <= 1) return launch_ec_combine<B, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
-  if (u == 2) return launch_ec_combine<B, 2>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
-  return launch_ec_combine<B, 3>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+  if (u <= 1) return launch_ec_combine<B, B, 1>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+  if (u == 2) return launch_ec_combine<B, B, 2>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
+  return launch_ec_combine<B, B, 3>(c, grid, y_perm, ec_slot, ec_wt, ec_w, y_shared, S, out, st);
 }
 
 // ec_wt: the [E, T] weight table k_ec_select wrote in the workspace, or null
@@ -939,7 +946,8 @@ moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& i
       dn.scatter_w = scatter->w;
       return launch_tc(EPI_SCATTER_BF16, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
     }
-    return launch_tc(EPI_BIAS_BF16, ha, ha, hb0, hb1, dn, bn_dn, row_tiles_ub, st);
+    return launch_tc(c.y_f32 ? EPI_F32 : EPI_BIAS_BF16, ha, ha, hb0, hb1, dn, bn_dn,
+                     row_tiles_ub, st);
   }
   // fp32: CUDA-core grouped GEMMs
   const int64_t tiles_ub = (Tk + S * T + 63) / 64 + c.E + S;
@@ -987,22 +995,29 @@ moe_status do_combine(const moe_config& c, const void* y_perm, const int32_t* sl
   const int S = y_shared ? c.n_shared : 0;
   // U 16-byte vectors per lane and pass: two for bf16 top-1/2 and top-3/4 rows,
   // one with more slots in flight (or fp32 rows)
-#define MOE_COMBINE(TE, KM, U)                                                              \
-  return launch_pdl(k_combine<TE, KM, U>, dim3(grid), dim3(256), 0, st,                     \
-                    static_cast<const TE*>(y_perm), slot_of, w,                             \
-                    static_cast<const TE*>(y_shared), S, c.T, c.k, c.d_model,                \
-                    static_cast<TE*>(out))
+#define MOE_COMBINE(TY, TO, KM, U)                                                          \
+  return launch_pdl(k_combine<TY, TO, KM, U>, dim3(grid), dim3(256), 0, st,                 \
+                    static_cast<const TY*>(y_perm), slot_of, w,                             \
+                    static_cast<const TY*>(y_shared), S, c.T, c.k, c.d_model,                \
+                    static_cast<TO*>(out))
   const int km = kmax_of(c.k);
-  if (c.dtype == MOE_BF16) {
-    if (km == 2) MOE_COMBINE(__nv_bfloat16, 2, 2);
-    if (km == 4) MOE_COMBINE(__nv_bfloat16, 4, 2);
-    if (km == 8) MOE_COMBINE(__nv_bfloat16, 8, 1);
-    MOE_COMBINE(__nv_bfloat16, 16, 1);
+  using B = __nv_bfloat16;
+  if (c.dtype == MOE_BF16 && !c.y_f32) {
+    if (km == 2) MOE_COMBINE(B, B, 2, 2);
+    if (km == 4) MOE_COMBINE(B, B, 4, 2);
+    if (km == 8) MOE_COMBINE(B, B, 8, 1);
+    MOE_COMBINE(B, B, 16, 1);
   }
-  if (km == 2) MOE_COMBINE(float, 2, 1);
-  if (km == 4) MOE_COMBINE(float, 4, 1);
-  if (km == 8) MOE_COMBINE(float, 8, 1);
-  MOE_COMBINE(float, 16, 1);
+  if (c.dtype == MOE_BF16) {   // fp32 expert outputs, bf16 layer output
+    if (km == 2) MOE_COMBINE(float, B, 2, 1);
+    if (km == 4) MOE_COMBINE(float, B, 4, 1);
+    if (km == 8) MOE_COMBINE(float, B, 8, 1);
+    MOE_COMBINE(float, B, 16, 1);
+  }
+  if (km == 2) MOE_COMBINE(float, float, 2, 1);
+  if (km == 4) MOE_COMBINE(float, float, 4, 1);
+  if (km == 8) MOE_COMBINE(float, float, 8, 1);
+  MOE_COMBINE(float, float, 16, 1);
 #undef MOE_COMBINE
 }
 

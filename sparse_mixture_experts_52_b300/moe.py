@@ -41,7 +41,7 @@ class Config(ctypes.Structure):
         ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
         ("route", ctypes.c_int32), ("renorm", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("has_bias", ctypes.c_int32), ("aux_alpha", ctypes.c_float), ("aux_f", ctypes.c_int32),
-        ("act", ctypes.c_int32),
+        ("act", ctypes.c_int32), ("y_f32", ctypes.c_int32),
     ]
 
 
@@ -63,7 +63,14 @@ def make_config(cfg: dict) -> Config:
     c.aux_f = AUX_F[af] if isinstance(af, str) else int(af)
     a = cfg.get("act", "gelu")
     c.act = ACTS[a] if isinstance(a, str) else int(a)
+    c.y_f32 = int(cfg.get("y_f32", 0))
     return c
+
+
+def y_dtype(cfg: dict) -> torch.dtype:
+    """Element type of the expert outputs y_perm / y_shared: the layer dtype,
+    or fp32 when the configuration keeps them so (``y_f32``)."""
+    return torch.float32 if cfg.get("y_f32", 0) else TORCH_DTYPES[cfg["dtype"]]
 
 
 def w1_rows(cfg: dict) -> int:
@@ -265,13 +272,13 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
     _want(w2, "w2", (E, d, F), dt)
     _want(b1, "b1", (E, F1), dt, allow_none=not cfg.get("has_bias", 0))
     _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
-    _want(y_perm, "y_perm", (R, d), dt)
+    _want(y_perm, "y_perm", (R, d), y_dtype(cfg))
     if S:
         _want(x, "x", (T, d), dt)
         _want(ws1, "ws1", (S, F1, d), dt)
         _want(wsb1, "wsb1", (S, F1), dt, allow_none=True)
         _want(ws2, "ws2", (S, d, F), dt)
-        _want(y_shared, "y_shared", (S, T, d), dt)
+        _want(y_shared, "y_shared", (S, T, d), y_dtype(cfg))
     _call("moe_grouped_ffn", ctypes.byref(make_config(cfg)), _p(x_perm), _p(offsets), _p(w1),
           _p(b1), _p(w2), _p(b2), _p(x), _p(ws1), _p(wsb1), _p(ws2), _p(wsb2), _p(y_perm),
           _p(y_shared), _p(ws), ws.numel(), _stream(stream))
@@ -314,12 +321,12 @@ def combine_expert_choice(cfg, y_perm, ec_slot, ec_w, out, y_shared=None, stream
     T, d, E, S = cfg["T"], cfg["d_model"], cfg["E"], cfg.get("n_shared", 0)
     C = expert_capacity(cfg)
     dt = TORCH_DTYPES[cfg["dtype"]]
-    _want(y_perm, "y_perm", (E * C, d), dt)
+    _want(y_perm, "y_perm", (E * C, d), y_dtype(cfg))
     _want(ec_slot, "ec_slot", (E, T), torch.int32)
     _want(ec_w, "ec_w", (E, C), torch.float32)
     _want(out, "out", (T, d), dt)
     if S:
-        _want(y_shared, "y_shared", (S, T, d), dt)
+        _want(y_shared, "y_shared", (S, T, d), y_dtype(cfg))
     _call("moe_combine_expert_choice", ctypes.byref(make_config(cfg)), _p(y_perm), _p(ec_slot),
           _p(ec_w), _p(y_shared), _p(out), _stream(stream))
 
@@ -327,12 +334,12 @@ def combine_expert_choice(cfg, y_perm, ec_slot, ec_w, out, y_shared=None, stream
 def combine(cfg, y_perm, slot_of, topk_w, out, y_shared=None, stream=None):
     T, d, k, S = cfg["T"], cfg["d_model"], cfg["k"], cfg.get("n_shared", 0)
     dt = TORCH_DTYPES[cfg["dtype"]]
-    _want(y_perm, "y_perm", (T * k, d), dt)
+    _want(y_perm, "y_perm", (T * k, d), y_dtype(cfg))
     _want(slot_of, "slot_of", (T * k,), torch.int32)
     _want(topk_w, "topk_w", (T, k), torch.float32)
     _want(out, "out", (T, d), dt)
     if S:
-        _want(y_shared, "y_shared", (S, T, d), dt)
+        _want(y_shared, "y_shared", (S, T, d), y_dtype(cfg))
     _call("moe_combine", ctypes.byref(make_config(cfg)), _p(y_perm), _p(slot_of), _p(topk_w),
           _p(y_shared), _p(out), _stream(stream))
 

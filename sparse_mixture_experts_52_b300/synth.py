@@ -71,7 +71,7 @@ WORKLOADS["switch_expert_choice"] = dict(WORKLOADS["switch_top1_cap"], route="ex
 
 LAYER_KEYS = ("T", "d_model", "d_ff", "E", "k", "n_shared", "capacity_factor",
               "min_capacity", "route", "renorm", "dtype", "has_bias",
-              "aux_alpha", "aux_f", "act")
+              "aux_alpha", "aux_f", "act", "y_f32")
 
 
 def workload(name: str, **overrides) -> dict:

@@ -41,10 +41,22 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_config_struct_layout(lib):
     # 15 four-byte fields, no padding
-    assert ctypes.sizeof(moe.Config) == 60
+    assert ctypes.sizeof(moe.Config) == 64
     assert moe.Config.capacity_factor.offset == 24
     assert moe.Config.aux_f.offset == 52
     assert moe.Config.act.offset == 56
+    assert moe.Config.y_f32.offset == 60
+
+
+def test_expert_output_type_flag_is_validated(lib):
+    n = ctypes.c_size_t(0)
+    sizes = {}
+    for y, want in ((0, 0), (1, 0), (2, 1), (-1, 1)):
+        c = moe.make_config(synth.workload("mixtral_top2", T=256, y_f32=y))
+        assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == want, y
+        sizes[y] = n.value
+    # fp32 expert outputs take twice the bytes of the bf16 ones in the workspace
+    assert sizes[1] > sizes[0]
 
 
 def test_activation_value_is_validated(lib):

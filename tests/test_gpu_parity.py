@@ -34,6 +34,7 @@ def run_steps(cfg, inp):
     """route -> permute -> grouped_ffn -> combine through the four entry points."""
     T, d, E, k, S = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"], cfg.get("n_shared", 0)
     dt = moe.TORCH_DTYPES[cfg["dtype"]]
+    yt = moe.y_dtype(cfg)
     ws = moe.new_workspace(cfg, DEV)
     z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
     o = dict(logits=z((T, E), torch.float32), topk_idx=z((T, k), torch.int32),
@@ -42,8 +43,8 @@ def run_steps(cfg, inp):
              z_loss=z((1,), torch.float32), counts=z((E,), torch.int32),
              kept=z((E,), torch.int32), offsets=z((E + 1,), torch.int32),
              perm_token=z((T * k,), torch.int32), slot_of=z((T * k,), torch.int32),
-             x_perm=z((T * k, d), dt), y_perm=z((T * k, d), dt), out=z((T, d), dt))
-    o["y_shared"] = z((S, T, d), dt) if S else None
+             x_perm=z((T * k, d), dt), y_perm=z((T * k, d), yt), out=z((T, d), dt))
+    o["y_shared"] = z((S, T, d), yt) if S else None
     moe.route(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["f"], o["P"], o["aux"],
               ws, logit_bias=inp.get("logit_bias"), select_bias=inp.get("select_bias"),
               logits=o["logits"], z_loss=o["z_loss"])
@@ -125,6 +126,15 @@ SMALL = {
                                       E=8, k=2, has_bias=1, nonzero_bias=True, act="swiglu"),
     "swiglu_top1_fused_combine": dict(name="switch_top1_cap", T=1000, d_model=128, d_ff=256,
                                       E=16, k=1, renorm=1, act="swiglu"),
+    # raw top-1 gate values (down to 1/E): outputs reach 11x their RMS, so the
+    # step-wise path keeps the expert outputs in fp32 (one rounding, in the
+    # combine, as the fused path has)
+    "swiglu_top1_raw_gate_y_f32": dict(name="switch_top1_cap", T=1000, d_model=128, d_ff=256,
+                                       E=16, k=1, renorm=0, act="swiglu", y_f32=1),
+    # fp32 expert outputs through moe_forward's own combine (top-2), with a
+    # shared expert and biases
+    "y_f32_top2_shared_bias": dict(name="deepseek_v3_top8", T=300, d_model=128, d_ff=256, E=8,
+                                   k=2, has_bias=1, nonzero_bias=True, y_f32=1),
     "swiglu_fp32_bias": dict(name="tiny_fp32_top2", T=300, d_model=64, d_ff=96, E=8, k=2,
                              nonzero_bias=True, act="swiglu"),
     "silu_fp32": dict(name="tiny_fp32_top2", T=200, d_model=64, d_ff=80, E=4, k=2, act="silu"),
@@ -171,11 +181,56 @@ def test_full_workload_all_tokens(name):
     print(name, rep.summary())
 
 
-@pytest.mark.parametrize("name,nrows", [("mixtral_top2", 48), ("deepseek_v3_top8", 24),
-                                        ("mixtral_swiglu_top2", 24)])
-def test_full_workload_sampled_tokens(name, nrows):
-    """Routing, statistics and dispatch on every token; the layer output on a
-    fixed sample of tokens (no capacity limit, so each token's output depends
+def _pick_split(N, row_tiles, sms=148):
+    """The tile width and stream-K choice of the library's expert-FFN GEMMs
+    (the host-side rule of the tcgen05 grouped GEMM, restated here to find the
+    tiles its stream-K tail covers)."""
+    wide = 256 if N >= 256 else (128 if N >= 128 else 64)
+    if row_tiles * -(-N // wide) >= 8 * sms:
+        return wide, True
+    return wide, False
+
+
+def stream_k_tail_tokens(cfg, offsets, perm_token, sms=148):
+    """Tokens whose rows lie in the tiles that the up- or down-projection
+    splits stream-K (the last waves of a many-wave GEMM): the first and last
+    row of every such tile.  A model of the library's schedule: group-major
+    tiles, then column block, then 128-row block; whole waves round robin,
+    the last one to two waves' tiles split by k-iterations."""
+    T, d, F, E, k, S = (cfg["T"], cfg["d_model"], cfg["d_ff"], cfg["E"], cfg["k"],
+                        cfg.get("n_shared", 0))
+    glu = cfg.get("act", "gelu") == "swiglu"
+    n_rows = T * k
+    rt = max(-(-n_rows // 128) + E // 2, min(E, n_rows)) + S * -(-T // 128)
+    rows = [int(offsets[g + 1] - offsets[g]) for g in range(E)] + [T] * S
+    toks = set()
+    for N_pick, N_out, halve in ((2 * F if glu else F, F, glu), (d, d, False)):
+        bn, sk = _pick_split(N_pick, rt, sms)
+        if not sk:
+            continue
+        bno = bn // 2 if halve else bn
+        n_tiles = -(-N_out // bno)
+        grid = min(sms, 160)
+        starts = np.concatenate([[0], np.cumsum([-(-r // 128) * n_tiles for r in rows])])
+        total = int(starts[-1])
+        waves = total // grid
+        dp = (waves - 1) * grid if waves >= 2 else 0
+        for t in range(dp, total):
+            g = int(np.searchsorted(starts, t, side="right") - 1)
+            mt = -(-rows[g] // 128)
+            m_blk = (t - int(starts[g])) % mt
+            r0, r1 = m_blk * 128, min(m_blk * 128 + 128, rows[g]) - 1
+            for r in (r0, r1):
+                toks.add(int(perm_token[offsets[g] + r]) if g < E else r)
+    return sorted(toks)
+
+
+@pytest.mark.parametrize("name", ["mixtral_top2", "deepseek_v3_top8", "mixtral_swiglu_top2"])
+def test_full_workload_sampled_tokens(name):
+    """Routing, statistics and dispatch on every token; the layer output on
+    1024 tokens: every token whose rows open or close a tile of the stream-K
+    tail (the last waves, whose k-blocks several CTAs share), the rest spread
+    evenly over the batch (no capacity limit, so each token's output depends
     only on its own routing)."""
     cfg = synth.workload(name)
     inp = synth.make_inputs(cfg, device=DEV)
@@ -184,9 +239,19 @@ def test_full_workload_sampled_tokens(name, nrows):
     moe.check_status(layer.ws)
     fw = {k: _np(v) for k, v in r.items()}
     T = cfg["T"]
-    rows = sorted(set(np.linspace(0, T - 1, nrows).astype(int).tolist()))
+    ref0 = compare.run_oracle(cfg, inp, rows=[0])
+    tail = stream_k_tail_tokens(cfg, ref0.disp.offsets, ref0.disp.perm_token)
+    assert tail, "the full-size workload should split its last waves stream-K"
+    if len(tail) > 512:
+        tail = [tail[i] for i in np.linspace(0, len(tail) - 1, 512).astype(int)]
+    rows = set(tail)
+    for t in np.linspace(0, T - 1, 1024).astype(int):
+        if len(rows) >= 1024:
+            break
+        rows.add(int(t))
+    rows = sorted(rows)
     rep = compare.check_layer(cfg, inp, fw, rows=rows)
-    print(name, rep.summary())
+    print(name, f"tail tokens {len(tail)}", rep.summary())
     del layer, inp
     torch.cuda.empty_cache()
 
@@ -316,14 +381,15 @@ def run_steps_ec(cfg, inp):
     T, d, E, S = cfg["T"], cfg["d_model"], cfg["E"], cfg.get("n_shared", 0)
     C = moe.expert_capacity(cfg)
     dt = moe.TORCH_DTYPES[cfg["dtype"]]
+    yt = moe.y_dtype(cfg)
     ws = moe.new_workspace(cfg, DEV)
     z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
     o = dict(logits=z((T, E), torch.float32), topk_idx=z((E, C), torch.int32),
              topk_w=z((E, C), torch.float32), ec_slot=z((E, T), torch.int32),
              f=z((E,), torch.float32), P=z((E,), torch.float32), aux=z((1,), torch.float32),
              z_loss=z((1,), torch.float32), offsets=z((E + 1,), torch.int32),
-             x_perm=z((E * C, d), dt), y_perm=z((E * C, d), dt), out=z((T, d), dt))
-    o["y_shared"] = z((S, T, d), dt) if S else None
+             x_perm=z((E * C, d), dt), y_perm=z((E * C, d), yt), out=z((T, d), dt))
+    o["y_shared"] = z((S, T, d), yt) if S else None
     moe.route_expert_choice(cfg, inp["x"], inp["w_g"], o["topk_idx"], o["topk_w"], o["ec_slot"],
                             o["f"], o["P"], o["aux"], ws, logit_bias=inp.get("logit_bias"),
                             logits=o["logits"], z_loss=o["z_loss"])
@@ -366,6 +432,9 @@ EC_SMALL = {
     "ec_shared_e64_swiglu": dict(name="deepseek_v3_top8", T=600, d_model=128, d_ff=128, E=64,
                                  route="expert_choice", capacity_factor=4.0, act="swiglu",
                                  select_bias_std=0.0),
+    "ec_shared_y_f32": dict(name="deepseek_v3_top8", T=400, d_model=128, d_ff=128, E=16,
+                            route="expert_choice", capacity_factor=2.0, select_bias_std=0.0,
+                            y_f32=1),
     "ec_argmax_f_min_capacity": dict(name="switch_expert_choice", T=256, d_model=64, d_ff=64,
                                      E=8, capacity_factor=0.01, min_capacity=5,
                                      aux_f="argmax"),
