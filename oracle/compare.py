@@ -51,7 +51,8 @@ def oracle_config(cfg: dict) -> om.OracleConfig:
         min_capacity=int(cfg.get("min_capacity", 0)), route=cfg["route"],
         renorm=bool(cfg.get("renorm", 1)),
         aux_alpha=float(np.float32(cfg.get("aux_alpha", 0.01))),
-        aux_f=cfg.get("aux_f", om.AUX_TOPK_COUNT), act=cfg.get("act", om.ACT_GELU))
+        aux_f=cfg.get("aux_f", om.AUX_TOPK_COUNT), act=cfg.get("act", om.ACT_GELU),
+        experts=cfg.get("experts", "dense"))
 
 
 def np64(t) -> Optional[np.ndarray]:

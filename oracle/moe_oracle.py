@@ -81,6 +81,7 @@ class OracleConfig:
     aux_alpha: float = 0.01
     aux_f: str = AUX_TOPK_COUNT
     act: str = ACT_GELU
+    experts: str = "dense"          # "dense" or "mxfp8" (R22: MX FP8 expert operands)
 
 
 # --------------------------------------------------------------------------
@@ -335,6 +336,43 @@ def expert_ffn(xe: np.ndarray, w1: np.ndarray, b1: Optional[np.ndarray],
     return y
 
 
+def expert_ffn_mxfp8(xe: np.ndarray, w1: np.ndarray, b1: Optional[np.ndarray],
+                     w2: np.ndarray, b2: Optional[np.ndarray], act: str = ACT_GELU) -> np.ndarray:
+    """The expert FFN with MX FP8 operands (R22).
+
+    Both contractions take their two operands MX-quantised along the
+    contraction axis: x rows and W1 rows along d for the first, the hidden
+    activation's rows and W2 rows along d_ff for the second.  The hidden
+    activation act(x W1^T + b1) is formed in float64 from the quantised
+    operands, rounded to float32 (the precision in which the kernels hold it
+    when they quantise it) and quantised.  Biases are not quantised.  The
+    products and sums are float64."""
+    from . import mxfp8 as mx
+    xq = mx.fake_quant(xe)
+    w1q = mx.fake_quant(w1)
+    h = xq @ w1q.T
+    if b1 is not None:
+        h = h + np.asarray(b1, np.float64)
+    if act == ACT_GELU:
+        h = gelu(h)
+    elif act == ACT_SILU:
+        h = silu(h)
+    elif act == ACT_SWIGLU:
+        F = h.shape[1] // 2
+        h = silu(h[:, :F]) * h[:, F:]
+    else:
+        raise ValueError(f"unknown activation {act!r}")
+    hq = mx.fake_quant(h.astype(np.float32))
+    y = hq @ mx.fake_quant(w2).T
+    if b2 is not None:
+        y = y + np.asarray(b2, np.float64)
+    return y
+
+
+def _ffn_of(cfg: OracleConfig):
+    return expert_ffn_mxfp8 if cfg.experts == "mxfp8" else expert_ffn
+
+
 # --------------------------------------------------------------------------
 # Load-balance statistics.  [BEE] load_balance_loss; [BAIDU] gate step 3;
 # [CH7] §7.4 L_balance = N * sum f_i p_i.
@@ -438,13 +476,13 @@ def moe_forward(cfg: OracleConfig, x: np.ndarray, w_g: np.ndarray,
         if ii.size == 0:
             continue
         w1, b1, w2, b2 = experts(e)
-        y = expert_ffn(x64_rows[ii], w1, b1, w2, b2, act=cfg.act)
+        y = _ffn_of(cfg)(x64_rows[ii], w1, b1, w2, b2, act=cfg.act)
         wt = g.w[rows[ii], jj][:, None]
         np.add.at(out, ii, wt * y)          # index_add_ of the weighted outputs
 
     for s in range(cfg.n_shared):
         w1, b1, w2, b2 = shared(s)
-        out += expert_ffn(x64_rows, w1, b1, w2, b2, act=cfg.act)
+        out += _ffn_of(cfg)(x64_rows, w1, b1, w2, b2, act=cfg.act)
 
     return ForwardResult(logits=logits, gate=g, disp=disp, C=C, f=f, P=P,
                          aux=aux, rows=rows, out=out, extra={"z_loss": z})
@@ -479,10 +517,10 @@ def _expert_choice_forward(cfg, x, logits, experts, shared, rows, override):
         ii = np.array([a for a, _ in pick], np.int64)
         jj = np.array([b for _, b in pick], np.int64)
         w1, b1, w2, b2 = experts(e)
-        y = expert_ffn(x64_rows[ii], w1, b1, w2, b2, act=cfg.act)
+        y = _ffn_of(cfg)(x64_rows[ii], w1, b1, w2, b2, act=cfg.act)
         np.add.at(out, ii, ec.w[e, jj][:, None] * y)
     for s in range(cfg.n_shared):
         w1, b1, w2, b2 = shared(s)
-        out += expert_ffn(x64_rows, w1, b1, w2, b2, act=cfg.act)
+        out += _ffn_of(cfg)(x64_rows, w1, b1, w2, b2, act=cfg.act)
     return ForwardResult(logits=logits, gate=None, disp=disp, C=C, f=f, P=P, aux=aux,
                          rows=rows, out=out, extra={"z_loss": z, "ec": ec})
