@@ -504,6 +504,56 @@ def cpu_sample(cfg, args):
     return np.arange(rows_n), text
 
 
+class BlasThreads:
+    """Sets the thread count of the BLAS library numpy loaded, through its own
+    set/get entry points (OpenBLAS builds export them under a few names), for
+    the duration of a `with` block.  `available` is False when no such library
+    or entry point is found."""
+    NAMES = [("scipy_openblas_set_num_threads64_", "scipy_openblas_get_num_threads64_"),
+             ("openblas_set_num_threads64_", "openblas_get_num_threads64_"),
+             ("openblas_set_num_threads", "openblas_get_num_threads")]
+
+    def __init__(self, n: int):
+        import ctypes
+        import numpy  # noqa: F401  (loads its BLAS)
+        self.n, self.set, self.get, self.old = n, None, None, None
+        paths = []
+        try:
+            with open("/proc/self/maps") as fh:
+                for line in fh:
+                    p = line.split()[-1]
+                    name = os.path.basename(p)
+                    if "openblas" in name and ".so" in name and p not in paths:
+                        paths.append(p)
+        except OSError:
+            pass
+        for p in paths:
+            try:
+                lib = ctypes.CDLL(p)
+            except OSError:
+                continue
+            for s_name, g_name in self.NAMES:
+                if hasattr(lib, s_name) and hasattr(lib, g_name):
+                    self.set, self.get = getattr(lib, s_name), getattr(lib, g_name)
+                    self.set.argtypes, self.get.restype = [ctypes.c_int], ctypes.c_int
+                    return
+
+    @property
+    def available(self) -> bool:
+        return self.set is not None
+
+    def __enter__(self):
+        if self.available:
+            self.old = int(self.get())
+            self.set(int(self.n))
+        return self
+
+    def __exit__(self, *exc):
+        if self.available and self.old is not None:
+            self.set(self.old)
+        return False
+
+
 def cpu_baseline(cfg, inp, args):
     """The oracle as it stands, on the host cores, on a bounded token sample:
     once with every core this process may run on (BLAS threads = the affinity
@@ -513,16 +563,14 @@ def cpu_baseline(cfg, inp, args):
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     cores = host_cores()
     why = None
-    try:
-        from threadpoolctl import threadpool_limits
-    except ImportError as e:
-        threadpool_limits, why = None, f"threadpoolctl: {e}"
     runs = {}
     for n in (cores, 1):
-        if threadpool_limits is None:      # no thread control: one run at the default
+        ctl = BlasThreads(n)
+        if not ctl.available:      # no thread control: one run at the library's default
             runs[n] = _oracle_seconds(cfg, host, rows)
+            why = "no BLAS thread-count entry point found"
             break
-        with threadpool_limits(limits=n):
+        with ctl:
             runs[n] = _oracle_seconds(cfg, host, rows)
     out = {"value": len(rows) / runs[cores], "unit": "tokens/s", "cores": cores,
            "kind": "oracle", "seconds": runs[cores], "sample": text}
