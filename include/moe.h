@@ -87,6 +87,14 @@ typedef enum {
   MOE_AUX_ARGMAX = 1        /* f_i = (#tokens whose largest logit is i) / T */
 } moe_aux_f;
 
+/* Storage of the expert weights w1, w2 (see moe_quantize_mxfp8). */
+typedef enum {
+  MOE_EXPERT_DENSE = 0,   /* in cfg.dtype                                       */
+  MOE_EXPERT_MXFP8 = 1    /* MX FP8: e4m3 codes + one power-of-two scale per 32
+                             elements along K, one packed buffer per tensor; the
+                             activations are quantised the same way on the fly  */
+} moe_expert_fmt;
+
 typedef enum {
   MOE_ACT_GELU = 0,     /* GELU_erf(h), h = x W1^T + b1                       */
   MOE_ACT_SILU = 1,     /* h * sigmoid(h)                                     */
@@ -117,6 +125,9 @@ typedef struct {
                               its expert outputs once, in the combine, instead
                               of twice).  Read by moe_grouped_ffn, moe_combine,
                               moe_combine_expert_choice and moe_forward.     */
+  int32_t expert_fmt;      /* moe_expert_fmt.  MOE_EXPERT_MXFP8 needs dtype bf16,
+                              top-k routing, n_shared = 0, and d_model and d_ff
+                              multiples of 128 (else MOE_ERR_UNSUPPORTED).   */
 } moe_config;
 
 /* Bytes of workspace the entry points below need for `cfg` (host only). */
@@ -216,6 +227,32 @@ moe_status moe_grouped_ffn(const moe_config* cfg, const void* x_perm, const int3
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_of,
                        const float* topk_w, const void* y_shared, void* out,
                        moe_stream stream);
+
+/* MX FP8 expert weights ("AI-Research-SKILLs MoE 训练实战…全指南" §9.2 names FP8
+ * serving of MoE layers; the format read here is the OCP Microscaling one):
+ * every 32 consecutive elements of a weight row along K share a scale 2^s,
+ * s = floor(log2(max |w|)) - 8 clamped to [-127, 127] (-127 for an all-zero
+ * block), stored as the byte s + 127; each element is w / 2^s rounded to the
+ * nearest e4m3 value (ties to even, saturating at +-448).
+ *
+ * moe_mxfp8_weight_bytes (host only): bytes of one packed tensor of G experts'
+ * [N, K] weights: G*N*K code bytes, then G*N*K/32 scale bytes.  N and K must
+ * be multiples of 128.
+ *
+ * moe_quantize_mxfp8: packs bf16 weights w [G, N, K] (device) into `packed`
+ * (device, moe_mxfp8_weight_bytes bytes), stream-ordered.  Codes: [G, N, K]
+ * row-major.  Scales: 512-byte blocks, block (g, k / 128, n / 128) at
+ * ((g * K/128 + k/128) * N/128 + n/128) * 512, the scale of row n and k-block
+ * j = (k / 32) % 4 at byte 16 (n % 32) + 4 ((n % 128) / 32) + j of its block.
+ * glu = 1 packs a SwiGLU w1 ([2F, K]: gate rows, then up rows) with its rows
+ * interleaved in 64-row halves -- packed row 128 t + i is gate row 64 t + i
+ * for i < 64, up row F + 64 t + i - 64 otherwise -- which is the order the
+ * layer reads; glu = 0 keeps the row order.  Pass the packed w1 / w2 to
+ * moe_forward or moe_grouped_ffn with cfg.expert_fmt = MOE_EXPERT_MXFP8 (b1
+ * and b2 stay in dtype, in their natural order). */
+moe_status moe_mxfp8_weight_bytes(int32_t G, int32_t N, int32_t K, size_t* bytes);
+moe_status moe_quantize_mxfp8(const void* w, int32_t G, int32_t N, int32_t K, int32_t glu,
+                              void* packed, moe_stream stream);
 
 /* Tokens per expert (host only): the capacity C of the configuration, or -1
  * when the top-k routing has no capacity limit (capacity_factor <= 0).  Under

@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include "groups.cuh"
+#include "mxfp8.cuh"
 #include "route.cuh"
 
 namespace moe {
@@ -30,18 +31,26 @@ namespace moe {
 // fused into the down-projection), tokens with no kept assignment get their
 // zero output row here (zero_out), and one extra block reduces the routing
 // statistics meanwhile.
-template <int KMAX>
+//
+// MXQ: the rows go out as MX FP8 for the block-scaled expert GEMM instead
+// (bf16 rows, d a multiple of 128): each token's row is quantised once (32-
+// element blocks over four lanes' 16-byte vectors) and its codes and scale
+// bytes are written to the padded row of each kept slot: expert e's rows start
+// at 128 * (row blocks of the experts before it), rank r inside.
+template <int KMAX, bool MXQ = false>
 __global__ void __launch_bounds__(256)
 k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
           const int32_t* __restrict__ hist, const int32_t* __restrict__ kept,
           const int32_t* __restrict__ offsets, int T, int k, int E, int ncs, int tpb,
           int row_bytes, const uint8_t* __restrict__ x, uint8_t* __restrict__ x_perm,
           int32_t* __restrict__ perm_token, int32_t* __restrict__ slot_of,
-          uint8_t* __restrict__ zero_out, const StatsArgs st) {
+          uint8_t* __restrict__ zero_out, const StatsArgs st, uint8_t* __restrict__ xq_sf,
+          int64_t sf_rb) {
   __shared__ int s_pre[kMaxExperts];
   __shared__ int s_list[32 * kMaxK];
   __shared__ unsigned int s_mark[kMaxExperts / 32];
   __shared__ int s_n;
+  __shared__ int s_poff[MXQ ? kMaxExperts + 1 : 1];
   griddep_wait();
   griddep_launch_dependents();
   if (st.p_part) {   // the last stats_blocks(E, 8) blocks reduce the routing statistics
@@ -52,6 +61,7 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
       return;
     }
   }
+  if constexpr (MXQ) padded_offsets(nullptr, kept, E, s_poff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * tpb, t1 = min(t0 + tpb, T);
   const int g = t0 / kChunk;
@@ -100,13 +110,14 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
       if (c < nvec) v[i] = __ldg(src + c);
     }
     // lane j < k resolves slot j; the warp then shares the k slots
-    int my_slot = -1;
+    int my_slot = -1, my_prow = -1;
     if (lane < k) {
       const int64_t a = static_cast<int64_t>(t) * k + lane;
       const int e = __ldg(idx + a);
       if (e >= 0 && e < E) {
         const int r = s_pre[e] + __ldg(crank + a);
         my_slot = (r < __ldg(kept + e)) ? __ldg(offsets + e) + r : -1;
+        if constexpr (MXQ) my_prow = my_slot >= 0 ? s_poff[e] + r : -1;
       }
       slot_of[a] = my_slot;
       if (my_slot >= 0 && perm_token) perm_token[my_slot] = t;
@@ -122,6 +133,34 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
         uint4* o = reinterpret_cast<uint4*>(zero_out + static_cast<int64_t>(t) * row_bytes);
         for (int c = lane; c < nvec; c += 32) o[c] = make_uint4(0u, 0u, 0u, 0u);
       }
+    }
+    if constexpr (MXQ) {
+      int prow[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) prow[j] = __shfl_sync(0xffffffffu, my_prow, j);
+      const int d = row_bytes / 2;   // bf16 elements; codes are one byte each
+      for (int c0 = 0; c0 < nvec; c0 += 32 * PF) {
+#pragma unroll
+        for (int i = 0; i < PF; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c0 > 0) v[i] = c < nvec ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          else if (c >= nvec) v[i] = make_uint4(0u, 0u, 0u, 0u);
+          uint32_t sbyte;
+          const uint2 q = mx_quant8(v[i], sbyte);   // every lane: the block takes 4 lanes
+          if (c < nvec) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+              if (j < k && prow[j] >= 0) {
+                *reinterpret_cast<uint2*>(x_perm + static_cast<int64_t>(prow[j]) * d + c * 8) = q;
+                if ((lane & 3) == 0)   // k-block c / 4: stage c / 16, byte (c / 4) % 4
+                  xq_sf[mx_sf_offset(static_cast<int64_t>(c >> 4) * sf_rb + (prow[j] >> 7),
+                                     prow[j]) + ((c >> 2) & 3)] = static_cast<uint8_t>(sbyte);
+              }
+            }
+          }
+        }
+      }
+      continue;
     }
     for (int c0 = 0; c0 < nvec; c0 += 32 * PF) {
       if (c0 > 0) {

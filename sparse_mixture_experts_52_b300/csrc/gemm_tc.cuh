@@ -37,6 +37,23 @@
 // the dispatch outputs it reads are complete) and waits for the up-projection
 // grid at its end instead; its last CTA clears the counters.
 //
+// MX FP8 operands (MX = true).  A and B hold e4m3 codes; every 32 K-elements
+// of every A row and B row share an E8M0 scale (the OCP Microscaling form).
+// A stage then covers 128 K-elements (128 bytes per row, as a bf16 stage of
+// 64), and brings, besides the two code boxes, one 512-byte block of scale
+// bytes per 128 rows of A and of B (a bulk copy each).  Those blocks are
+// stored pre-interleaved for the tensor core: byte (i, c, j) of a block, at
+// offset 16 i + 4 c + j, is the scale of row 32 c + i for the stage's k-block
+// j.  The MMA thread copies them into tensor memory (tcgen05.cp 32x128b,
+// replicated into the four lane quarters), so that row m's scale for k-block
+// j sits in lane m, column base + m / 32, byte j; the four k-blocks of a stage
+// are four block-scaled MMAs of K = 32 selecting bytes 0..3.  The routed rows
+// of A (and of a hidden activation the kernel writes) start at 128-row
+// aligned ("padded") offsets, so every tile's rows are one scale block.  An
+// up-projection with MX output quantises its tile of the hidden activation in
+// the epilogue: each thread holds one row, takes the largest magnitude of
+// every 32 columns, and writes e4m3 codes plus the scale bytes.
+//
 // Every wait is bounded: a wait that runs out records MOE_DEV_ERR_* in the
 // status word, raises the CTA abort flag, drains what this CTA has in flight
 // and returns, so a bad launch can never hang the GPU.
@@ -62,8 +79,13 @@ enum : int {
   EPI_BIAS_BF16 = 2,
   EPI_SCATTER_BF16 = 3,
   EPI_SILU_BF16 = 4,
-  EPI_SWIGLU_BF16 = 5
+  EPI_SWIGLU_BF16 = 5,
+  EPI_GELU_MX = 6,      // the activations of the up-projection, MX FP8 output
+  EPI_SILU_MX = 7,
+  EPI_SWIGLU_MX = 8
 };
+__host__ __device__ constexpr bool epi_glu(int e) { return e == EPI_SWIGLU_BF16 || e == EPI_SWIGLU_MX; }
+__host__ __device__ constexpr bool epi_mx_out(int e) { return e >= EPI_GELU_MX; }
 enum : int {
   DEV_ERR_WAIT_PRODUCER = 1,
   DEV_ERR_WAIT_MMA = 2,
@@ -95,6 +117,14 @@ struct TcArgs {
   int* ready;                    // [groups] hidden-tile counters (zero between calls)
   unsigned int* ready_done;      // READY_WAIT: CTAs finished (zero between calls)
   int ready_up_tiles;            // READY_WAIT: column tiles of the up-projection per row tile
+  // MX FP8 operands
+  const uint8_t* sfa;            // A scale blocks [K/128][sfa_rb][512]
+  int64_t sfa_rb;                // 128-row blocks of the (padded) A rows
+  const uint8_t* sfb;            // B scale blocks [groups][K/128][sfb_nb][512]
+  int sfb_nb;                    // 128-row blocks of one group's B rows
+  uint8_t* sf_out;               // MX output: scale blocks [N/128][sf_out_rb][512]
+  int64_t sf_out_rb;
+  int pad_rows;                  // bit 0: routed A rows start at padded offsets; bit 1: output rows
 };
 
 __device__ __forceinline__ bool wait_timeout(uint64_t* bar, uint32_t parity, uint64_t limit) {
@@ -168,13 +198,19 @@ struct SegIter {
   }
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool MX = false>
 struct TcSmem {
-  static constexpr int BM = 128, BK = 64;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  // a stage is 128 bytes of K per row: 64 bf16 or 128 e4m3 elements
+  static constexpr int BM = 128, BK = MX ? 128 : 64;
+  static constexpr uint32_t A_BYTES = BM * 128;
+  static constexpr uint32_t B_BYTES = BN * 128;
+  static constexpr uint32_t SF_BYTES = MX ? 512 * (1 + BN / 128) : 0;   // A, then B scale blocks
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+  // MX: the double-buffered accumulator, then a ring of scale columns (A at
+  // 2 BN + 8 s, B at 2 BN + 64 + 8 s: 8-column aligned)
+  static constexpr uint32_t TMEM_COLS = MX ? 512 : ((2 * BN < 32) ? 32 : 2 * BN);
+  static constexpr uint32_t SFA_COL = 2 * BN, SFB_COL = 2 * BN + 64;
+  static_assert(!MX || (BN == 128 && STAGES <= 8), "MX tiles: 128 wide, at most 8 stages");
   struct Ctrl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -190,13 +226,14 @@ struct TcSmem {
   }
 };
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool MX = false>
 __global__ void __launch_bounds__(192, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
           const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
           const TcArgs args) {
-  using L = TcSmem<BN, STAGES>;
+  using L = TcSmem<BN, STAGES, MX>;
   constexpr int BM = L::BM, BK = L::BK;
+  static_assert(!epi_mx_out(EPI) || MX, "an MX output comes from MX operands");
   constexpr int NCC = BN / 16;   // 16-column chunks of a tile
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert((BN & (BN - 1)) == 0, "TMEM columns must be a power of two");
@@ -206,12 +243,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * L::A_BYTES;
+  uint8_t* sSF = sB + STAGES * L::B_BYTES;   // MX scale blocks of every stage
   auto& c = *reinterpret_cast<typename L::Ctrl*>(smem + STAGES * L::STAGE_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const GroupSpec& gs = args.gs;
   const int G = gs.E + gs.n_shared;
-  constexpr bool GLU = EPI == EPI_SWIGLU_BF16;
+  constexpr bool GLU = epi_glu(EPI);
+  constexpr bool MXO = epi_mx_out(EPI);
   constexpr int BNO = GLU ? BN / 2 : BN;   // output columns of a tile
   const int n_tiles = (args.N + BNO - 1) / BNO;
   const int KB = (args.K + BK - 1) / BK;
@@ -246,6 +285,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   if (args.ready_mode != READY_WAIT) griddep_wait();
   griddep_launch_dependents();
   build_group_table<BM>(gs, n_tiles, c.tb);   // synchronises the block
+  if (args.pad_rows) {
+    // routed groups at 128-row aligned offsets: the row blocks of the groups before
+    for (int g = threadIdx.x; g < gs.E; g += blockDim.x) {
+      const int prow = (c.tb.tile_start[g] / n_tiles) * BM;
+      if (args.pad_rows & 1) c.tb.a_row0[g] = prow;
+      if (args.pad_rows & 2) c.tb.out_row0[g] = prow;
+    }
+    __syncthreads();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -301,10 +349,23 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           }
           mbar_arrive_expect_tx(&c.full[stage], L::STAGE_BYTES);
           tma_load_2d(sA + stage * L::A_BYTES, ma, &c.full[stage], kb * BK, arow);
-          tma_load_3d(sB + stage * L::B_BYTES, mb, &c.full[stage], kb * BK, ncol, bz);
-          if (GLU)   // the up projection's rows into the second half of the B tile
-            tma_load_3d(sB + stage * L::B_BYTES + (BN / 2) * BK * 2, mb, &c.full[stage], kb * BK,
-                        args.N + ncol, bz);
+          if constexpr (MX) {
+            // SwiGLU weights are packed with gate and up rows interleaved in
+            // 64-row halves, so a tile's B rows are one box of BN rows
+            const int brow = GLU ? n_blk * BN : ncol;
+            tma_load_3d(sB + stage * L::B_BYTES, mb, &c.full[stage], kb * BK, brow, bz);
+            uint8_t* sf = sSF + stage * L::SF_BYTES;
+            bulk_load(sf, args.sfa + (static_cast<int64_t>(kb) * args.sfa_rb + arow / BM) * 512,
+                      512, &c.full[stage]);
+            bulk_load(sf + 512,
+                      args.sfb + ((static_cast<int64_t>(bz) * KB + kb) * args.sfb_nb + brow / 128) * 512,
+                      512, &c.full[stage]);
+          } else {
+            tma_load_3d(sB + stage * L::B_BYTES, mb, &c.full[stage], kb * BK, ncol, bz);
+            if (GLU)   // the up projection's rows into the second half of the B tile
+              tma_load_3d(sB + stage * L::B_BYTES + (BN / 2) * BK * 2, mb, &c.full[stage],
+                          kb * BK, args.N + ncol, bz);
+          }
 #pragma unroll
           for (int s = 0; s < STAGES; ++s) armed[s] += (s == stage) ? 1u : 0u;
           if (++stage == STAGES) {
@@ -346,11 +407,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * L::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * L::B_BYTES);
+          if constexpr (MX) {
+            // this stage's scale blocks into its tensor-memory columns, then
+            // four block-scaled MMAs of K = 32 (bytes 0..3 of those columns)
+            const uint32_t sf = smem_u32(sSF + stage * L::SF_BYTES);
+            const uint32_t ta = tmem_base + L::SFA_COL + 8u * stage;
+            const uint32_t tb = tmem_base + L::SFB_COL + 8u * stage;
+            tmem_cp_32x128b_x4(ta, sdesc_sf_32x16(sf));
+            tmem_cp_32x128b_x4(tb, sdesc_sf_32x16(sf + 512));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_bf16_f32(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32),
-                          sdesc_kmajor_sw128(b0 + kk * 32), idesc,
-                          (kb > kb0 || kk != 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_mxf8(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32), sdesc_kmajor_sw128(b0 + kk * 32),
+                        idesc_mxf8(BM, BN, kk, kk), ta, tb, (kb > kb0 || kk != 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              umma_bf16_f32(d_tmem, sdesc_kmajor_sw128(a0 + kk * 32),
+                            sdesc_kmajor_sw128(b0 + kk * 32), idesc,
+                            (kb > kb0 || kk != 0) ? 1u : 0u);
+            }
           }
           umma_commit(&c.empty[stage]);   // frees this smem stage once read
           issued = true;
@@ -477,8 +552,86 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         }
       };
       constexpr int NOUT = GLU ? NCC / 2 : NCC;   // 16-column output chunks
+      if constexpr (MXO) {
+        // ---- the hidden activation in MX FP8: 32-column blocks of this row
+        uint32_t sfw = 0;   // the blocks' scale bytes, byte j = block j of the 128-column stage
 #pragma unroll 1
-      for (int cc = 0; cc < NOUT; ++cc) {
+        for (int cb = 0; cb < NOUT / 2; ++cb) {
+          float v[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cc = 2 * cb + h;
+            uint32_t r[16], ru[GLU ? 16 : 1];
+            tmem_ld_32x32b_x16(trow + cc * 16, r);
+            tmem_wait_ld(r);
+            if constexpr (GLU) {
+              tmem_ld_32x32b_x16(trow + (cc + NCC / 2) * 16, ru);
+              tmem_wait_ld(ru);
+            }
+            const int col = n_blk * BNO + cc * 16;
+            float a[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(r[i]);
+            add_partials(cc, a);
+            if (bias) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) a[i] += __bfloat162float(bias[col + i]);
+            }
+            if constexpr (GLU) {
+              float u[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) u[i] = __uint_as_float(ru[i]);
+              add_partials(cc + NCC / 2, u);
+              if (bias) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] += __bfloat162float(bias[args.N + col + i]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) a[i] = silu(a[i]) * u[i];
+            } else if (EPI == EPI_SILU_MX) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) a[i] = silu(a[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) a[i] = gelu_erf(a[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[16 * h + i] = a[i];
+          }
+          const int col = n_blk * BNO + cb * 32;
+          if (!valid) continue;
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+          float inv;
+          const uint32_t sbyte = mx_scale(amax, inv);
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            pk[i] = static_cast<uint32_t>(cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv)) |
+                    (static_cast<uint32_t>(cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv)) << 16);
+          uint8_t* o = static_cast<uint8_t*>(args.out) + orow * args.ldo + col;
+          *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(o + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          sfw |= sbyte << (8 * ((col >> 5) & 3));
+        }
+        if (valid) {
+          // this row's scale bytes of the tile's columns, in the interleaved
+          // block of its 128 rows and its 128-column stage
+          const int col0 = n_blk * BNO;
+          uint8_t* sfp = args.sf_out +
+                         ((static_cast<int64_t>(col0 >> 7) * args.sf_out_rb + (orow >> 7)) * 512) +
+                         (orow & 31) * 16 + ((orow & 127) >> 5) * 4;
+          if constexpr (BNO >= 128) {
+            *reinterpret_cast<uint32_t*>(sfp) = sfw;
+          } else {
+            const int j0 = (col0 >> 5) & 3;
+            *reinterpret_cast<uint16_t*>(sfp + j0) = static_cast<uint16_t>(sfw >> (8 * j0));
+          }
+        }
+      }
+#pragma unroll 1
+      for (int cc = 0; cc < (MXO ? 0 : NOUT); ++cc) {
         uint32_t r[16], ru[GLU ? 16 : 1];
         tmem_ld_32x32b_x16(trow + cc * 16, r);
         tmem_wait_ld(r);

@@ -16,6 +16,7 @@
 #include "expert_choice.cuh"
 #include "gemm_tc.cuh"
 #include "groups.cuh"
+#include "mxfp8.cuh"
 #include "route.cuh"
 #include "route_tc.cuh"
 
@@ -67,6 +68,8 @@ moe_status validate(const moe_config* c) {
   if (c->renorm != 0 && c->renorm != 1) return MOE_ERR_INVALID_ARG;
   if (c->has_bias != 0 && c->has_bias != 1) return MOE_ERR_INVALID_ARG;
   if (c->y_f32 != 0 && c->y_f32 != 1) return MOE_ERR_INVALID_ARG;
+  if (c->expert_fmt != MOE_EXPERT_DENSE && c->expert_fmt != MOE_EXPERT_MXFP8)
+    return MOE_ERR_INVALID_ARG;
   if (c->act < MOE_ACT_GELU || c->act > MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha))
     return MOE_ERR_INVALID_ARG;
@@ -80,7 +83,18 @@ moe_status validate(const moe_config* c) {
   // 16-byte rows for vector loads and TMA strides
   if (c->d_model % 8 != 0 || c->d_ff % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_F32 && c->E > 64) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_fmt == MOE_EXPERT_MXFP8 &&
+      (c->dtype != MOE_BF16 || c->route == MOE_ROUTE_EXPERT_CHOICE || c->n_shared != 0 ||
+       c->d_model % 128 != 0 || c->d_ff % 128 != 0))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+bool mx_experts(const moe_config& c) { return c.expert_fmt == MOE_EXPERT_MXFP8; }
+
+// Rows of the MX activations: each expert's rows start at a multiple of 128.
+int64_t mx_padded_rows(const moe_config& c) {
+  return (static_cast<int64_t>(c.T) * c.k + 127 * static_cast<int64_t>(c.E) + 127) / 128 * 128;
 }
 
 int capacity_of(const moe_config& c) {
@@ -113,6 +127,8 @@ struct Layout {
   size_t idx, w, counts, kept, offsets, perm_token, slot_of, f, P, aux;
   size_t scoresT, tok_stats, ec_token, ec_w, ec_slot, ec_wt;   // Expert Choice
   size_t x_perm, H, Y, Ys, sk_part, total;
+  size_t xq, xq_sf, hq, hq_sf;   // MX FP8 experts: codes and scale blocks (padded rows)
+  int64_t mx_rows;
   int nb, E_pad;
   bool tc_router;   // the top-k router runs on the tensor cores
   bool tc_logits;   // the logits buffer and transposed W_g exist
@@ -167,6 +183,12 @@ Layout make_layout(const moe_config& c) {
   L.Ys = take(S * T * d * y_bytes(c));
   // stream-K partial tiles of the tensor-core FFN: one 128 x 256 fp32 slot per CTA
   L.sk_part = take(c.dtype == MOE_BF16 ? static_cast<size_t>(kMaxGemmCtas) * 128 * 256 * 4 : 0);
+  L.mx_rows = mx_experts(c) ? mx_padded_rows(c) : 0;
+  const size_t mr = static_cast<size_t>(L.mx_rows);
+  L.xq = take(mr * d);
+  L.xq_sf = take(mr * d / 32);
+  L.hq = take(mr * F);
+  L.hq_sf = take(mr * F / 32);
   L.total = off;
   return L;
 }
@@ -268,31 +290,73 @@ bool map_b(CUtensorMap* m, const void* base, int64_t K, int64_t N, int64_t G, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MX FP8 codes [rows, K] bytes, box = 128 rows x 128 bytes, 128-byte swizzle
+bool map_u8_a(CUtensorMap* m, const void* base, int64_t K, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(std::max<int64_t>(rows, 1))};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MX FP8 codes [G, N, K] bytes, box = 1 x 128 rows x 128 bytes
+bool map_u8_b(CUtensorMap* m, const void* base, int64_t K, int64_t N, int64_t G) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(std::max<int64_t>(G, 1))};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- GEMM launch
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool MX = false>
 moe_status launch_tc_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                           const CUtensorMap& b1, const TcArgs& args, int64_t row_tiles_ub,
                           cudaStream_t st) {
-  constexpr size_t smem = TcSmem<BN, STAGES>::bytes();
+  constexpr size_t smem = TcSmem<BN, STAGES, MX>::bytes();
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, EPI>,
+    if (cudaFuncSetAttribute(k_gemm_tc<BN, STAGES, EPI, MX>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
-  constexpr int BNO = (EPI == EPI_SWIGLU_BF16) ? BN / 2 : BN;   // output columns per tile
+  constexpr int BNO = epi_glu(EPI) ? BN / 2 : BN;   // output columns per tile
   const int64_t n_tiles = (args.N + BNO - 1) / BNO;
   const int64_t ub = std::max<int64_t>(1, row_tiles_ub * n_tiles);
   // stream-K: one CTA per SM (at most one partial slot each) whatever the tile
   // count; round-robin: no more CTAs than tiles
   const int grid = args.streamk ? std::min(num_sms(), kMaxGemmCtas)
                                 : static_cast<int>(std::min<int64_t>(ub, num_sms()));
-  return launch_pdl(k_gemm_tc<BN, STAGES, EPI>, dim3(grid), dim3(192), smem, st, a0, a1, b0, b1,
-                    args);
+  return launch_pdl(k_gemm_tc<BN, STAGES, EPI, MX>, dim3(grid), dim3(192), smem, st, a0, a1, b0,
+                    b1, args);
+}
+
+// The block-scaled MX FP8 GEMMs: 128-wide tiles, 6 stages (33 KB each).
+moe_status launch_tc_mx(int epi, const CUtensorMap& a0, const CUtensorMap& b0,
+                        const TcArgs& args, int64_t row_tiles_ub, cudaStream_t st) {
+#define MOE_MX_EPI(EPI) \
+  if (epi == EPI) return launch_tc_inst<128, 6, EPI, true>(a0, a0, b0, b0, args, row_tiles_ub, st);
+  MOE_MX_EPI(EPI_GELU_MX)
+  MOE_MX_EPI(EPI_SILU_MX)
+  MOE_MX_EPI(EPI_SWIGLU_MX)
+  MOE_MX_EPI(EPI_BIAS_BF16)
+  MOE_MX_EPI(EPI_F32)
+  MOE_MX_EPI(EPI_SCATTER_BF16)
+#undef MOE_MX_EPI
+  return MOE_ERR_UNSUPPORTED;
 }
 
 // Row tiles (128 rows) of a grouped GEMM over n_rows expert-ordered rows in
@@ -759,11 +823,14 @@ moe_status do_combine_ec(const moe_config& c, const void* y_perm, const int32_t*
 // Slot resolution and row gather from the ranks a routing or ranking grid
 // left.  Tokens per block: the largest of 32, 16, 8, 4 that still gives at
 // least two blocks per SM.
+// MX: x_perm receives MX FP8 codes at padded rows and xq_sf their scale
+// blocks (sf_rb row blocks) instead of bf16 rows.
 moe_status launch_permute(const moe_config& c, const int32_t* idx, const int32_t* crank,
                           const int32_t* hist, const int32_t* kept, const int32_t* offsets,
                           int32_t* perm_token, int32_t* slot_of, const void* x, void* x_perm,
                           cudaStream_t st, void* zero_out = nullptr,
-                          const StatsArgs& stats = StatsArgs{}) {
+                          const StatsArgs& stats = StatsArgs{}, uint8_t* xq_sf = nullptr,
+                          int64_t sf_rb = 0) {
   const int row_bytes = c.d_model * static_cast<int>(elem_bytes(c));
   int tpb = 32;
   while (tpb > 4 && (c.T + tpb - 1) / tpb < 2 * num_sms()) tpb >>= 1;
@@ -773,15 +840,23 @@ moe_status launch_permute(const moe_config& c, const int32_t* idx, const int32_t
   const int ncs = chunk_stride(c.T);
   const auto* xb = static_cast<const uint8_t*>(x);
   auto* xp = static_cast<uint8_t*>(x_perm);
-#define MOE_PERMUTE(KM)                                                                     \
-  launch_pdl(k_permute<KM>, dim3(grid), dim3(256), 0, st, idx, crank, hist, kept, offsets, \
-             c.T, c.k, c.E, ncs, tpb, row_bytes, xb, xp, perm_token, slot_of,             \
-             static_cast<uint8_t*>(zero_out), stats)
+#define MOE_PERMUTE(KM, MXQ)                                                                \
+  launch_pdl(k_permute<KM, MXQ>, dim3(grid), dim3(256), 0, st, idx, crank, hist, kept,      \
+             offsets, c.T, c.k, c.E, ncs, tpb, row_bytes, xb, xp, perm_token, slot_of,     \
+             static_cast<uint8_t*>(zero_out), stats, xq_sf, sf_rb)
+  if (xq_sf) {
+    switch (kmax_of(c.k)) {
+      case 2: return MOE_PERMUTE(2, true);
+      case 4: return MOE_PERMUTE(4, true);
+      case 8: return MOE_PERMUTE(8, true);
+      default: return MOE_PERMUTE(16, true);
+    }
+  }
   switch (kmax_of(c.k)) {
-    case 2: return MOE_PERMUTE(2);
-    case 4: return MOE_PERMUTE(4);
-    case 8: return MOE_PERMUTE(8);
-    default: return MOE_PERMUTE(16);
+    case 2: return MOE_PERMUTE(2, false);
+    case 4: return MOE_PERMUTE(4, false);
+    case 8: return MOE_PERMUTE(8, false);
+    default: return MOE_PERMUTE(16, false);
   }
 #undef MOE_PERMUTE
 }
@@ -842,6 +917,7 @@ int32_t* noalloc_scratch(cudaStream_t st) {
 struct FfnIn {
   const void *x_perm, *w1, *b1, *w2, *b2, *x, *ws1, *wsb1, *ws2, *wsb2;
   const int32_t* offsets;
+  bool x_quantized;   // MX experts: the workspace already holds x_perm as MX FP8
 };
 
 // The top-1 combine fused into the down-projection (bf16, k = 1, no shared
@@ -852,8 +928,102 @@ struct FfnScatter {
   const float* w;             // [T] gate weights
 };
 
+// The grouped FFN on MX FP8 operands: the expert-ordered rows (quantised by
+// the permute, or here from the caller's bf16 x_perm) and the hidden
+// activation at 128-row aligned group offsets in the workspace, the packed
+// weights, block-scaled tcgen05 MMAs.  Routed experts only.
+moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn& in,
+                     void* y_perm, cudaStream_t st, const FfnScatter* scatter) {
+  const int64_t Tk = routed_rows(c);
+  const int d = c.d_model, F = c.d_ff, E = c.E;
+  const bool glu = c.act == MOE_ACT_SWIGLU;
+  const int F1 = glu ? 2 * F : F;
+  const int64_t R = L.mx_rows, RB = L.mx_rows / 128;
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  uint8_t* xq_sf = at<uint8_t>(ws, L.xq_sf);
+  uint8_t* hq = at<uint8_t>(ws, L.hq);
+  uint8_t* hq_sf = at<uint8_t>(ws, L.hq_sf);
+  moe_status s;
+  if (!in.x_quantized) {
+    const int grid = static_cast<int>(std::min<int64_t>((Tk + 7) / 8, num_sms() * 8));
+    if ((s = launch_pdl(k_quant_rows_mx, dim3(std::max(grid, 1)), dim3(256), 0, st,
+                        static_cast<const __nv_bfloat16*>(in.x_perm), in.offsets, E, d, RB, xq,
+                        xq_sf)) != MOE_OK)
+      return s;
+  }
+  const uint8_t* w1 = static_cast<const uint8_t*>(in.w1);
+  const uint8_t* w2 = static_cast<const uint8_t*>(in.w2);
+  CUtensorMap ma, mb, ha, hb;
+  if (!map_u8_a(&ma, xq, d, R) || !map_u8_b(&mb, w1, d, F1, E) || !map_u8_a(&ha, hq, F, R) ||
+      !map_u8_b(&hb, w2, F, d, E))
+    return MOE_ERR_CUDA;
+  const int64_t row_tiles_ub = (Tk + 127) / 128 + E;
+  const int64_t rt = est_row_tiles(Tk, E);
+  const int sms = num_sms();
+  // whole tiles round robin unless there are 8 waves or more: stream-K tail
+  const bool sk_up = rt * (F1 / 128) >= 8 * static_cast<int64_t>(sms);
+  const bool sk_dn = rt * (d / 128) >= 8 * static_cast<int64_t>(sms);
+  const bool overlap = !sk_up && !sk_dn;
+  TcArgs up{};
+  up.gs = GroupSpec{in.offsets, E, 0, 0, c.T, 0, 0, 0, 0};
+  up.N = F;
+  up.K = d;
+  up.out = hq;
+  up.out1 = hq;
+  up.ldo = F;
+  up.bias0 = static_cast<const __nv_bfloat16*>(c.has_bias ? in.b1 : nullptr);
+  up.err = at<int>(ws, L.status);
+  up.streamk = sk_up;
+  up.partial = at<float>(ws, L.sk_part);
+  up.flags = at<int>(ws, L.status + kFlagsOffset);
+  up.sfa = xq_sf;
+  up.sfa_rb = RB;
+  up.sfb = w1 + static_cast<int64_t>(E) * F1 * d;
+  up.sfb_nb = F1 / 128;
+  up.sf_out = hq_sf;
+  up.sf_out_rb = RB;
+  up.pad_rows = 3;
+  if (overlap) {
+    up.ready_mode = READY_SIGNAL;
+    up.ready = at<int>(ws, L.status + kReadyOffset);
+  }
+  const int epi_up = glu ? EPI_SWIGLU_MX : (c.act == MOE_ACT_SILU ? EPI_SILU_MX : EPI_GELU_MX);
+  if ((s = launch_tc_mx(epi_up, ma, mb, up, row_tiles_ub, st)) != MOE_OK) return s;
+  TcArgs dn{};
+  dn.gs = GroupSpec{in.offsets, E, 0, 0, c.T, 0, 0, 0, 0};
+  dn.N = d;
+  dn.K = F;
+  dn.out = y_perm;
+  dn.out1 = y_perm;
+  dn.ldo = d;
+  dn.bias0 = static_cast<const __nv_bfloat16*>(c.has_bias ? in.b2 : nullptr);
+  dn.err = at<int>(ws, L.status);
+  dn.streamk = sk_dn;
+  dn.partial = at<float>(ws, L.sk_part);
+  dn.flags = at<int>(ws, L.status + kFlagsOffset);
+  dn.sfa = hq_sf;
+  dn.sfa_rb = RB;
+  dn.sfb = w2 + static_cast<int64_t>(E) * d * F;
+  dn.sfb_nb = d / 128;
+  dn.pad_rows = 1;
+  if (overlap) {
+    dn.ready_mode = READY_WAIT;
+    dn.ready = at<int>(ws, L.status + kReadyOffset);
+    dn.ready_done = at<unsigned int>(ws, L.status + kReadyDoneOffset);
+    dn.ready_up_tiles = F / (glu ? 64 : 128);
+  }
+  if (scatter) {
+    dn.out = scatter->out;
+    dn.scatter_token = scatter->perm_token;
+    dn.scatter_w = scatter->w;
+    return launch_tc_mx(EPI_SCATTER_BF16, ha, hb, dn, row_tiles_ub, st);
+  }
+  return launch_tc_mx(c.y_f32 ? EPI_F32 : EPI_BIAS_BF16, ha, hb, dn, row_tiles_ub, st);
+}
+
 moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& in, void* y_perm,
                   void* y_shared, cudaStream_t st, const FfnScatter* scatter = nullptr) {
+  if (mx_experts(c)) return do_ffn_mx(c, L, ws, in, y_perm, st, scatter);
   const int64_t T = c.T, Tk = routed_rows(c), S = c.n_shared;
   const int d = c.d_model, F = c.d_ff;
   void* H = at<uint8_t>(ws, L.H);
@@ -1225,17 +1395,46 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const void* w_g,
   // top-1 bf16 layers without shared experts: the combine is fused into the
   // down-projection (and the permute writes the zero rows of dropped tokens)
   const bool fused_combine = c.dtype == MOE_BF16 && c.k == 1 && c.n_shared == 0;
+  // MX FP8 experts: the permute writes the rows quantised, at padded offsets
+  const bool mx = mx_experts(c);
   if ((s = launch_permute(c, idx, at<int32_t>(ws, L.crank), at<int32_t>(ws, L.hist), kept,
-                          offsets, perm_token, slot_of, x, x_perm, st,
-                          fused_combine ? out : nullptr, sa)) != MOE_OK)
+                          offsets, perm_token, slot_of, x, mx ? at<void>(ws, L.xq) : x_perm, st,
+                          fused_combine ? out : nullptr, sa,
+                          mx ? at<uint8_t>(ws, L.xq_sf) : nullptr, L.mx_rows / 128)) != MOE_OK)
     return s;
-  FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets};
+  FfnIn in{x_perm, w1, b1, w2, b2, x, ws1, wsb1, ws2, wsb2, offsets, mx};
   if (fused_combine) {
     const FfnScatter sc{out, perm_token, w};
     return do_ffn(c, L, ws, in, Y, Ys, st, &sc);
   }
   if ((s = do_ffn(c, L, ws, in, Y, Ys, st)) != MOE_OK) return s;
   return do_combine(c, Y, slot_of, w, c.n_shared > 0 ? Ys : nullptr, out, st);
+}
+
+moe_status moe_mxfp8_weight_bytes(int32_t G, int32_t N, int32_t K, size_t* bytes) {
+  if (!bytes || G < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  const size_t codes = static_cast<size_t>(G) * N * K;
+  *bytes = codes + codes / 32;
+  return MOE_OK;
+}
+
+moe_status moe_quantize_mxfp8(const void* w, int32_t G, int32_t N, int32_t K, int32_t glu,
+                              void* packed, moe_stream stream) {
+  size_t bytes = 0;
+  moe_status s = moe_mxfp8_weight_bytes(G, N, K, &bytes);
+  if (s != MOE_OK) return s;
+  if (!w || !packed || (glu != 0 && glu != 1)) return MOE_ERR_INVALID_ARG;
+  if (glu && N % 256 != 0) return MOE_ERR_UNSUPPORTED;   // two halves of whole 128-row tiles
+  const int64_t rows = static_cast<int64_t>(G) * N;
+  if (rows > static_cast<int64_t>(INT_MAX) * 8) return MOE_ERR_UNSUPPORTED;
+  uint8_t* codes = static_cast<uint8_t*>(packed);
+  const int grid = static_cast<int>((rows + 7) / 8);
+  k_quant_weights_mx<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(w), G, N, K, glu, codes,
+      codes + static_cast<size_t>(G) * N * K);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status moe_expert_capacity(const moe_config* cfg, int32_t* C) {

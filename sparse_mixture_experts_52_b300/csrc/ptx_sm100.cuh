@@ -204,4 +204,82 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// ---------------------------------------------------------------- MX FP8
+// Non-tensor bulk copy global -> shared (16-byte aligned, size a multiple of
+// 16), completing on `bar` with complete_tx.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte block of scale bytes stored
+// contiguously (no swizzle: 8-row x 16-byte core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t sdesc_sf_32x16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(128 >> 4) << 16;             // leading byte offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;             // stride byte offset: next 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  return d;                                               // layout type 0: no swizzle
+}
+
+// 32 lanes x 128 bits from shared memory into tensor-memory columns
+// [taddr, taddr + 4), the same 32 rows copied into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * SA) * (B * SB)^T: e4m3 x e4m3 -> fp32 with one E8M0 scale
+// per 32 K-elements of every A row and every B row (K = 32 per instruction).
+// The scales come from tensor memory: A row m from lane m, column
+// sfa + m/32; B row n from column sfb + n/32 of the lane quarter of the output
+// row; byte `id` of the 32-bit column in both (the ids are in idesc).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A = B = e4m3,
+// K-major, E8M0 scales; sf ids select the byte of the scale column.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, uint32_t sfa_id,
+                                                  uint32_t sfb_id) {
+  return (sfb_id << 4)                               // B scale byte
+         | (0u << 7) | (0u << 10)                    // A, B: e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale type: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (sfa_id << 29);                           // A scale byte
+}
+
+// Two fp32 values to two e4m3 codes (round to nearest even, saturating at
+// +-448): `lo` in the low byte.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// MX block scale of a block whose largest magnitude is `amax` (fp32):
+// s = floor(log2 amax) - 8 clamped to >= -127 (an all-zero or subnormal
+// maximum gives -127).  Returns the scale byte s + 127 and sets `inv` = 2^-s.
+__device__ __forceinline__ uint32_t mx_scale(float amax, float& inv) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);   // biased exponent
+  int s = e - 127 - 8;
+  if (s < -127) s = -127;
+  inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  return static_cast<uint32_t>(s + 127);
+}
+
 }  // namespace moe

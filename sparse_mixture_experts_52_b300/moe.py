@@ -20,6 +20,7 @@ ROUTES = {"softmax_topk": 0, "topk_softmax": 1, "biased_softmax": 2, "expert_cho
 DTYPES = {"f32": 0, "bf16": 1}
 AUX_F = {"topk_count": 0, "argmax": 1}
 ACTS = {"gelu": 0, "silu": 1, "swiglu": 2}
+EXPERT_FMTS = {"dense": 0, "mxfp8": 1}
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -41,7 +42,7 @@ class Config(ctypes.Structure):
         ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
         ("route", ctypes.c_int32), ("renorm", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("has_bias", ctypes.c_int32), ("aux_alpha", ctypes.c_float), ("aux_f", ctypes.c_int32),
-        ("act", ctypes.c_int32), ("y_f32", ctypes.c_int32),
+        ("act", ctypes.c_int32), ("y_f32", ctypes.c_int32), ("expert_fmt", ctypes.c_int32),
     ]
 
 
@@ -64,7 +65,14 @@ def make_config(cfg: dict) -> Config:
     a = cfg.get("act", "gelu")
     c.act = ACTS[a] if isinstance(a, str) else int(a)
     c.y_f32 = int(cfg.get("y_f32", 0))
+    f = cfg.get("experts", "dense")
+    c.expert_fmt = EXPERT_FMTS[f] if isinstance(f, str) else int(f)
     return c
+
+
+def mx_experts(cfg: dict) -> bool:
+    """True when the expert weights are packed MX FP8 buffers."""
+    return cfg.get("experts", "dense") in ("mxfp8", EXPERT_FMTS["mxfp8"])
 
 
 def y_dtype(cfg: dict) -> torch.dtype:
@@ -99,6 +107,10 @@ _SIGNATURES = {
                                 ctypes.c_size_t, _P],
     "moe_permute_expert_choice": [_CFG, _P, _P, _P, _P, _P],
     "moe_combine_expert_choice": [_CFG, _P, _P, _P, _P, _P, _P],
+    "moe_mxfp8_weight_bytes": [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                               ctypes.POINTER(ctypes.c_size_t)],
+    "moe_quantize_mxfp8": [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                           _P, _P],
 }
 
 
@@ -151,6 +163,39 @@ def _want(t: Optional[torch.Tensor], name: str, shape, dtype, allow_none=False):
         raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+# ------------------------------------------------------------------ MX FP8 weights
+def mxfp8_weight_bytes(G: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t(0)
+    _call("moe_mxfp8_weight_bytes", int(G), int(N), int(K), ctypes.byref(n))
+    return int(n.value)
+
+
+def quantize_mxfp8(w: torch.Tensor, glu: bool = False, stream=None) -> torch.Tensor:
+    """moe_quantize_mxfp8: packs bf16 expert weights [G, N, K] into one uint8
+    buffer (e4m3 codes, then the scale blocks); glu interleaves the gate and up
+    halves of a SwiGLU w1 in 64-row halves."""
+    if w.dim() != 3 or w.dtype != torch.bfloat16 or not w.is_cuda or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [G, N, K] bf16 CUDA tensor")
+    G, N, K = w.shape
+    out = torch.empty(mxfp8_weight_bytes(G, N, K), dtype=torch.uint8, device=w.device)
+    _call("moe_quantize_mxfp8", _p(w), int(G), int(N), int(K), int(bool(glu)), _p(out),
+          _stream(stream))
+    return out
+
+
+def _want_weights(cfg, w1, w2, dt):
+    """Expert weights: [E, F1, d] and [E, d, F] in dtype, or their packed MX
+    FP8 buffers."""
+    d, F, E = cfg["d_model"], cfg["d_ff"], cfg["E"]
+    F1 = w1_rows(cfg)
+    if mx_experts(cfg):
+        _want(w1, "w1", (mxfp8_weight_bytes(E, F1, d),), torch.uint8)
+        _want(w2, "w2", (mxfp8_weight_bytes(E, d, F),), torch.uint8)
+    else:
+        _want(w1, "w1", (E, F1, d), dt)
+        _want(w2, "w2", (E, d, F), dt)
 
 
 # ------------------------------------------------------------------ workspace
@@ -268,8 +313,7 @@ def grouped_ffn(cfg, x_perm, offsets, w1, w2, y_perm, ws, b1=None, b2=None, x=No
     R = routed_rows(cfg)
     _want(x_perm, "x_perm", (R, d), dt)
     _want(offsets, "offsets", (E + 1,), torch.int32)
-    _want(w1, "w1", (E, F1, d), dt)
-    _want(w2, "w2", (E, d, F), dt)
+    _want_weights(cfg, w1, w2, dt)
     _want(b1, "b1", (E, F1), dt, allow_none=not cfg.get("has_bias", 0))
     _want(b2, "b2", (E, d), dt, allow_none=not cfg.get("has_bias", 0))
     _want(y_perm, "y_perm", (R, d), y_dtype(cfg))
@@ -354,8 +398,7 @@ def forward(cfg, x, w_g, w1, w2, out, ws, b1=None, b2=None, ws1=None, wsb1=None,
     _want(x, "x", (T, d), dt)
     _want(w_g, "w_g", (d, E), dt)
     F1 = w1_rows(cfg)
-    _want(w1, "w1", (E, F1, d), dt)
-    _want(w2, "w2", (E, d, F), dt)
+    _want_weights(cfg, w1, w2, dt)
     _want(b1, "b1", (E, F1), dt, allow_none=True)
     _want(out, "out", (T, d), dt)
     # under Expert Choice topk_idx / topk_w carry the [E, C] taken tokens and weights
@@ -389,6 +432,11 @@ class MoELayer:
         self.cfg = dict(cfg)
         self.w = {k: v for k, v in inputs.items() if k != "x"}
         self.device = torch.device(device)
+        if mx_experts(cfg) and self.w["w1"].dtype != torch.uint8:
+            # MX FP8 experts: pack the bf16 weights once (on the device)
+            glu = cfg.get("act", "gelu") in ("swiglu", ACTS["swiglu"])
+            self.w["w1"] = quantize_mxfp8(self.w["w1"], glu=glu)
+            self.w["w2"] = quantize_mxfp8(self.w["w2"])
         self.ws = new_workspace(self.cfg, self.device)
         T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
         dt = TORCH_DTYPES[cfg["dtype"]]

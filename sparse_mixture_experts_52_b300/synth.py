@@ -69,9 +69,15 @@ WORKLOADS["mixtral_swiglu_top2"] = dict(WORKLOADS["mixtral_top2"], act="swiglu")
 WORKLOADS["switch_expert_choice"] = dict(WORKLOADS["switch_top1_cap"], route="expert_choice",
                                          capacity_factor=2.0, aux_f="topk_count")
 
+# MX FP8 experts (e4m3 weights and activations with 32-element power-of-two
+# block scales): the weight-streaming Switch and decode shapes, where the
+# weight bytes halve, and the compute-bound Mixtral shape.
+for _name in ("switch_top1_cap", "decode_zipf_top2", "mixtral_top2"):
+    WORKLOADS[_name + "_mxfp8"] = dict(WORKLOADS[_name], experts="mxfp8")
+
 LAYER_KEYS = ("T", "d_model", "d_ff", "E", "k", "n_shared", "capacity_factor",
               "min_capacity", "route", "renorm", "dtype", "has_bias",
-              "aux_alpha", "aux_f", "act", "y_f32")
+              "aux_alpha", "aux_f", "act", "y_f32", "experts")
 
 
 def workload(name: str, **overrides) -> dict:

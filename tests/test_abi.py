@@ -41,11 +41,12 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_config_struct_layout(lib):
     # 15 four-byte fields, no padding
-    assert ctypes.sizeof(moe.Config) == 64
+    assert ctypes.sizeof(moe.Config) == 68
     assert moe.Config.capacity_factor.offset == 24
     assert moe.Config.aux_f.offset == 52
     assert moe.Config.act.offset == 56
     assert moe.Config.y_f32.offset == 60
+    assert moe.Config.expert_fmt.offset == 64
 
 
 def test_expert_output_type_flag_is_validated(lib):
@@ -80,7 +81,9 @@ def test_workspace_size_of_every_workload(lib, name):
     eb = 2 if cfg["dtype"] == "bf16" else 4
     # x_perm + H + Y must fit
     assert n >= (T * k * d + (T * k + S * T) * F + T * k * d) * eb
-    assert n < 4 * (T * k * d + (T * k + S * T) * F + T * k * d) * eb + (1 << 24)
+    # MX FP8 experts add codes and scales of the rows at 128-row aligned offsets
+    mx = (T * k + 128 * cfg["E"]) * (d + F) * 33 // 32 if cfg.get("experts") == "mxfp8" else 0
+    assert n < 4 * (T * k * d + (T * k + S * T) * F + T * k * d) * eb + mx + (1 << 24)
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -175,3 +178,24 @@ def test_expert_choice_workspace_holds_its_rows(lib):
     rows = E * moe.expert_capacity(cfg)
     # x_perm + H + Y for the E*C expert rows, plus the [E, T] logits and slot table
     assert moe.workspace_size(cfg) >= rows * (2 * d + F) * 2 + 2 * E * T * 4
+
+
+def test_mx_unsupported_configurations_are_rejected(lib):
+    """MX FP8 experts need a bf16 layer, top-k routing, no shared experts and
+    d_model, d_ff multiples of 128: anything else is MOE_ERR_UNSUPPORTED on
+    the host."""
+    base = synth.workload("mixtral_top2", T=64, d_model=256, d_ff=512, experts="mxfp8")
+    assert moe.workspace_size(base) > 0
+    for bad in (dict(d_model=192), dict(d_ff=320), dict(n_shared=1), dict(dtype="f32"),
+                dict(route="expert_choice", capacity_factor=1.0)):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.workspace_size(dict(base, **bad))
+        assert ei.value.status == 2, bad
+
+
+def test_mxfp8_weight_bytes(lib):
+    assert moe.mxfp8_weight_bytes(8, 256, 128) == 8 * 256 * 128 * 33 // 32
+    for G, N, K in ((8, 200, 128), (8, 256, 96)):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.mxfp8_weight_bytes(G, N, K)
+        assert ei.value.status == 2
