@@ -48,7 +48,8 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "mixtral_top2"
 # the other workloads, measured in the same run as sub-records of the line
 SUB_WORKLOADS = ["switch_top1_cap", "deepseek_v3_top8", "decode_zipf_top2", "tiny_fp32_top2",
-                 "switch_expert_choice", "mixtral_swiglu_top2"]
+                 "switch_expert_choice", "mixtral_swiglu_top2", "switch_top1_cap_mxfp8",
+                 "decode_zipf_top2_mxfp8", "mixtral_top2_mxfp8"]
 HEADLINE_TIMED_MS = 1500.0     # device time of the headline's timed region (auto steps)
 SUB_TIMED_MS = 600.0           # the same for each sub-record
 METRIC = "MoE-layer fwd tokens/s"
@@ -75,6 +76,9 @@ def parse():
                     help="run moe_route, moe_permute and moe_combine three times on the "
                          "workload's token batch (no expert weights) and exit: the command "
                          "for per-kernel ncu captures of those steps at full size")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="run moe_forward W + K times on the workload (eager, no graphs) and "
+                         "exit: the command behind the per-kernel launch lists and captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", action="store_true",
                     help="measure the named workload alone (no sub-records)")
@@ -177,16 +181,25 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
+def mx_experts(cfg) -> bool:
+    return cfg.get("experts", "dense") == "mxfp8"
+
+
 def algorithmic_ffn(cfg, kept, elem):
-    """Bytes and FLOPs the grouped FFN must move / do at least, for this batch."""
+    """Bytes and FLOPs the grouped FFN must move / do at least, for this batch:
+    the active experts' weights once, the rows in, the hidden activation out
+    and back, the expert outputs out.  MX FP8 operands take 1 + 1/32 bytes an
+    element (codes and block scales); the expert outputs stay in the layer
+    dtype."""
     d, F, S, T = cfg["d_model"], cfg["d_ff"], cfg.get("n_shared", 0), cfg["T"]
     F1 = 2 * F if cfg.get("act", "gelu") == "swiglu" else F   # SwiGLU: gate and up rows
     n_a = int(sum(kept))
     active = int(sum(1 for v in kept if v > 0))
-    weights = (active + S) * (F1 + F) * d * elem
-    acts = (n_a + S * T) * (d + F + F + d) * elem
+    op = 33 / 32 if mx_experts(cfg) else elem
+    weights = (active + S) * (F1 + F) * d * op
+    acts = (n_a + S * T) * ((d + F + F) * op + d * elem)
     flops = 2 * (n_a + S * T) * d * (F1 + F)
-    return weights + acts, flops, n_a, active
+    return int(weights + acts), flops, n_a, active
 
 
 def rpc_bytes(cfg, n_a, elem) -> int:
@@ -272,6 +285,20 @@ def run_dispatch_only(args):
     moe.check_status(ws)
 
 
+def run_forward_only(args):
+    """moe_forward on one workload, W + K times in eager mode, then exit."""
+    import torch
+    from sparse_mixture_experts_52_b300 import moe, synth
+
+    cfg = synth.workload(args.workload)
+    inp = draw_inputs(cfg, cfg.get("seed", 0), torch.device("cuda", 0))
+    layer = moe.MoELayer(cfg, inp, device="cuda")
+    for _ in range(max(1, args.warmup + args.steps)):
+        layer(inp["x"])
+    torch.cuda.synchronize()
+    moe.check_status(layer.ws)
+
+
 def max_over_ranks(values, world, device):
     """Element-wise maximum of per-rank timings over the process group (the
     slowest replica sets the whole-job time); the values themselves at N = 1."""
@@ -295,7 +322,8 @@ def line_config(cfg, world) -> dict:
     return {"workload": cfg["name"], "T": cfg["T"], "d_model": cfg["d_model"],
             "d_ff": cfg["d_ff"], "E": cfg["E"], "k": cfg["k"], "act": cfg.get("act", "gelu"),
             "n_shared": cfg.get("n_shared", 0), "capacity_factor": cfg["capacity_factor"],
-            "route": cfg["route"], "dtype": cfg["dtype"], "parallelism": f"replicas x{world}",
+            "route": cfg["route"], "dtype": cfg["dtype"],
+            "experts": cfg.get("experts", "dense"), "parallelism": f"replicas x{world}",
             "l2": "flushed (256 MB write) before every step, outside the step events"}
 
 
@@ -374,9 +402,10 @@ def measure(args, cfg, rank, world, local_rank, steps, timed_ms, cpu_leg):
             moe.permute(cfg, inp["x"], r_sel[0], o["counts"], o["kept"], o["offsets"],
                         o["perm_token"], o["slot_of"], o["x_perm"], ws2)
 
-    def part_ffn():
-        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], inp["w1"], inp["w2"], o["y_perm"], ws2,
-                        b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"], ws1=inp.get("ws1"),
+    def part_ffn():   # the layer's weights: packed MX FP8 buffers for MX experts
+        moe.grouped_ffn(cfg, o["x_perm"], o["offsets"], layer.w["w1"], layer.w["w2"],
+                        o["y_perm"], ws2, b1=inp.get("b1"), b2=inp.get("b2"), x=inp["x"],
+                        ws1=inp.get("ws1"),
                         wsb1=inp.get("wsb1"), ws2=inp.get("ws2"), wsb2=inp.get("wsb2"),
                         y_shared=y_sh)
 
@@ -595,8 +624,11 @@ def record(res, world, peaks, peak_src) -> dict:
     # back-to-back steps for more than 200 ms run under the power cap: their tensor fraction is
     # taken against the sustained peak; the burst (dense) peak is reported beside it
     long_region = res["dev_ms"] > 200.0
-    tc_dense = peaks["bf16_tflops"]
-    tc_peak = peaks["bf16_tflops_sustained"] if long_region else tc_dense
+    # MX FP8 contractions: the measured bf16 peak times the nominal fp8 / bf16
+    # ratio of the tensor cores (4.5 / 2.25 PFLOP/s dense)
+    ratio = 2.0 if mx_experts(cfg) else 1.0
+    tc_dense = peaks["bf16_tflops"] * ratio
+    tc_peak = (peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]) * ratio
     t_tc = res["flops"] / (tc_peak * 1e12)
     if cfg["dtype"] == "bf16" and t_tc > t_hbm:
         roof = {"bound": "tensor", "achieved": round(tfl, 2), "peak": tc_peak,
@@ -608,7 +640,8 @@ def record(res, world, peaks, peak_src) -> dict:
     roof["traffic"] = profiled_traffic(cfg["name"])
     roof["kernel"] = "grouped FFN (tcgen05 up-projection + activation and down-projection)"
     sustained = long_region and roof["unit"] == "TFLOP/s"
-    roof["peak_source"] = f"{peak_src} ({'sustained' if sustained else 'burst'})"
+    roof["peak_source"] = (f"{peak_src} ({'sustained' if sustained else 'burst'})" +
+                           (", bf16 x 2 for fp8" if ratio != 1.0 and roof["unit"] == "TFLOP/s" else ""))
     roof["algorithmic_bytes"] = res["bytes"]
     roof["algorithmic_flops"] = res["flops"]
     roof["ms_per_launch"] = round(res["ffn_ms"], 4)
@@ -619,7 +652,8 @@ def record(res, world, peaks, peak_src) -> dict:
     mean_count = max(sum(counts) / len(counts), 1e-30)
     return {
         "value": round(tokens_s, 1), "unit": "tokens/s", "steps": steps,
-        "warmup": res["warmup"], "ms_per_step": round(ms, 4), "dtype": cfg["dtype"],
+        "warmup": res["warmup"], "ms_per_step": round(ms, 4),
+        "dtype": "mxfp8" if mx_experts(cfg) else cfg["dtype"],
         "config": line_config(cfg, world),
         "roofline": roof,
         "grouped_ffn": {"tflops": round(tfl, 2), "gbs": round(gbs, 1),
@@ -720,6 +754,9 @@ def main():
         return
     if args.dispatch_only:
         run_dispatch_only(args)
+        return
+    if args.forward_only:
+        run_forward_only(args)
         return
     import torch
     if world > 1:

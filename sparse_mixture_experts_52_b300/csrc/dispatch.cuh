@@ -160,8 +160,7 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
           }
         }
       }
-      continue;
-    }
+    } else {
     for (int c0 = 0; c0 < nvec; c0 += 32 * PF) {
       if (c0 > 0) {
 #pragma unroll
@@ -180,6 +179,7 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
               reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(slot[j]) * row_bytes)[c] = v[i];
         }
       }
+    }
     }
   }
 }

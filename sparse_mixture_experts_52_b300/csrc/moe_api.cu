@@ -15,6 +15,7 @@
 #include "dispatch.cuh"
 #include "expert_choice.cuh"
 #include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "groups.cuh"
 #include "mxfp8.cuh"
 #include "route.cuh"
@@ -342,6 +343,70 @@ moe_status launch_tc_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CU
                                 : static_cast<int>(std::min<int64_t>(ub, num_sms()));
   return launch_pdl(k_gemm_tc<BN, STAGES, EPI, MX>, dim3(grid), dim3(192), smem, st, a0, a1, b0,
                     b1, args);
+}
+
+// The CTA-pair GEMM: clusters of two CTAs, as many clusters as can be
+// resident at once (persistent; pairs of SMs, so an SM whose partner is busy
+// or missing stays out), each pair taking 256-row tiles round robin.
+template <int BN, int STAGES, int EPI>
+moe_status launch_tc2_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                           const CUtensorMap& b1, const TcArgs& args, int64_t pair_tiles_ub,
+                           cudaStream_t st) {
+  constexpr size_t smem = Tc2Smem<BN, STAGES>::bytes();
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+  if (max_pairs[dev] == 0) {
+    if (cudaFuncSetAttribute(k_gemm_tc2<BN, STAGES, EPI>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    cfg.gridDim = dim3(2 * num_sms());
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2<BN, STAGES, EPI>, &cfg) != cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    max_pairs[dev] = n;
+  }
+  const int64_t pairs = std::min<int64_t>(std::max<int64_t>(pair_tiles_ub, 1), max_pairs[dev]);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, k_gemm_tc2<BN, STAGES, EPI>, a0, a1, b0, b1, args) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status launch_tc2(int epi, const CUtensorMap& a0, const CUtensorMap& a1,
+                      const CUtensorMap& b0, const CUtensorMap& b1, const TcArgs& args,
+                      int64_t pair_tiles_ub, cudaStream_t st) {
+#define MOE_PAIR_EPI(EPI) \
+  if (epi == EPI) return launch_tc2_inst<256, 6, EPI>(a0, a1, b0, b1, args, pair_tiles_ub, st);
+  MOE_PAIR_EPI(EPI_GELU_BF16)
+  MOE_PAIR_EPI(EPI_SILU_BF16)
+  MOE_PAIR_EPI(EPI_SWIGLU_BF16)
+  MOE_PAIR_EPI(EPI_BIAS_BF16)
+  MOE_PAIR_EPI(EPI_F32)
+  MOE_PAIR_EPI(EPI_SCATTER_BF16)
+#undef MOE_PAIR_EPI
+  return MOE_ERR_UNSUPPORTED;
 }
 
 // The block-scaled MX FP8 GEMMs: 128-wide tiles, 6 stages (33 KB each).
@@ -1021,9 +1086,76 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
   return launch_tc_mx(c.y_f32 ? EPI_F32 : EPI_BIAS_BF16, ha, hb, dn, row_tiles_ub, st);
 }
 
+// Experts holding 512 rows or more on average (compute-bound, many waves of
+// tiles) run on CTA pairs with 256-row tiles; lighter ones on single CTAs,
+// where a 256-row tile would be mostly empty.
+bool use_pair_gemm(const moe_config& c) {
+  return c.dtype == MOE_BF16 && !mx_experts(c) && routed_rows(c) >= 512 * static_cast<int64_t>(c.E);
+}
+
+// The grouped FFN on CTA pairs (bf16): whole 256 x 256 tiles round robin.
+moe_status do_ffn_pair(const moe_config& c, const Layout& L, void* ws, const FfnIn& in,
+                       void* y_perm, void* y_shared, cudaStream_t st, const FfnScatter* scatter) {
+  const int64_t T = c.T, Tk = routed_rows(c), S = c.n_shared;
+  const int d = c.d_model, F = c.d_ff;
+  const bool glu = c.act == MOE_ACT_SWIGLU;
+  const int F1 = glu ? 2 * F : F;
+  void* H = at<uint8_t>(ws, L.H);
+  void* H_shared = static_cast<uint8_t*>(H) + static_cast<size_t>(Tk) * F * 2;
+  const int64_t pair_rows = (Tk + 255) / 256 + c.E + S * ((T + 255) / 256);
+  CUtensorMap ma0, ma1, mb0, mb1;
+  if (!map_a(&ma0, in.x_perm, d, std::max<int64_t>(Tk, 1)) || !map_b(&mb0, in.w1, d, F1, c.E, 128))
+    return MOE_ERR_CUDA;
+  if (S > 0) {
+    if (!map_a(&ma1, in.x, d, T) || !map_b(&mb1, in.ws1, d, F1, S, 128)) return MOE_ERR_CUDA;
+  } else {
+    ma1 = ma0;
+    mb1 = mb0;
+  }
+  TcArgs up{};
+  up.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 1, 0, 0, 0};
+  up.N = F;
+  up.K = d;
+  up.out = H;
+  up.out1 = H_shared;
+  up.ldo = F;
+  up.bias0 = static_cast<const __nv_bfloat16*>(c.has_bias ? in.b1 : nullptr);
+  up.bias1 = static_cast<const __nv_bfloat16*>(c.has_bias ? in.wsb1 : nullptr);
+  up.err = at<int>(ws, L.status);
+  const int epi_up = glu ? EPI_SWIGLU_BF16 : (c.act == MOE_ACT_SILU ? EPI_SILU_BF16 : EPI_GELU_BF16);
+  moe_status s = launch_tc2(epi_up, ma0, ma1, mb0, mb1, up, pair_rows * ((F + (glu ? 127 : 255)) / (glu ? 128 : 256)), st);
+  if (s != MOE_OK) return s;
+  CUtensorMap ha, hb0, hb1;
+  if (!map_a(&ha, H, F, Tk + S * T) || !map_b(&hb0, in.w2, F, d, c.E, 128)) return MOE_ERR_CUDA;
+  if (S > 0) {
+    if (!map_b(&hb1, in.ws2, F, d, S, 128)) return MOE_ERR_CUDA;
+  } else {
+    hb1 = hb0;
+  }
+  TcArgs dn{};
+  dn.gs = GroupSpec{in.offsets, c.E, 0, static_cast<int>(S), c.T, 0, static_cast<int>(Tk), 0, c.T};
+  dn.N = d;
+  dn.K = F;
+  dn.out = y_perm;
+  dn.out1 = y_shared;
+  dn.ldo = d;
+  dn.bias0 = static_cast<const __nv_bfloat16*>(c.has_bias ? in.b2 : nullptr);
+  dn.bias1 = static_cast<const __nv_bfloat16*>(c.has_bias ? in.wsb2 : nullptr);
+  dn.err = at<int>(ws, L.status);
+  const int64_t dn_tiles = pair_rows * ((d + 255) / 256);
+  if (scatter) {
+    dn.out = scatter->out;
+    dn.scatter_token = scatter->perm_token;
+    dn.scatter_w = scatter->w;
+    return launch_tc2(EPI_SCATTER_BF16, ha, ha, hb0, hb1, dn, dn_tiles, st);
+  }
+  return launch_tc2(c.y_f32 ? EPI_F32 : EPI_BIAS_BF16, ha, ha, hb0, hb1, dn, dn_tiles, st);
+}
+
 moe_status do_ffn(const moe_config& c, const Layout& L, void* ws, const FfnIn& in, void* y_perm,
                   void* y_shared, cudaStream_t st, const FfnScatter* scatter = nullptr) {
   if (mx_experts(c)) return do_ffn_mx(c, L, ws, in, y_perm, st, scatter);
+  if (use_pair_gemm(c)) return do_ffn_pair(c, L, ws, in, y_perm, y_shared, st, scatter);
   const int64_t T = c.T, Tk = routed_rows(c), S = c.n_shared;
   const int d = c.d_model, F = c.d_ff;
   void* H = at<uint8_t>(ws, L.H);
