@@ -162,7 +162,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_g,
  *   C)), offsets [E+1] (exclusive scan of kept), perm_token [T*k] (token of
  *   each expert-ordered row; entries >= offsets[E] are unspecified), slot_of
  *   [T*k] (row of assignment t*k+j in x_perm, or -1 when dropped), x_perm
- *   [T*k, d] dtype (rows >= offsets[E] unspecified). */
+ *   [T*k, d] dtype (rows >= offsets[E] unspecified).
+ *   An index outside [0, E), or one repeated in a token's row (after its
+ *   first occurrence), drops that assignment (slot -1, not counted) and sets
+ *   the status word: moe_check_status then returns MOE_ERR_INVALID_ARG. */
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                        int32_t* counts, int32_t* kept, int32_t* offsets,
                        int32_t* perm_token, int32_t* slot_of, void* x_perm,
@@ -191,9 +194,9 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
  *   Concurrency: all calls on one device share the one array, so calls whose
  *   kernels may overlap on the GPU (different streams without ordering) race
  *   and give wrong results; serialise them on one stream.
- *   Errors: as moe_permute, without ws.  An expert index outside [0, E) in
- *   topk_idx drops that assignment (slot -1); unlike the workspace entry
- *   points, no status word reports it. */
+ *   Errors: as moe_permute, without ws.  An expert index outside [0, E) or
+ *   repeated in a token's row drops that assignment (slot -1); unlike the
+ *   workspace entry points, no status word reports it. */
 #define MOE_PERMUTE_NOALLOC_MAX_ASSIGNMENTS 1048576
 #define MOE_PERMUTE_NOALLOC_MAX_CHUNK_COUNTS 1048576
 moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,

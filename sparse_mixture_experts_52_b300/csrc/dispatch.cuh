@@ -111,10 +111,18 @@ k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,
     }
     // lane j < k resolves slot j; the warp then shares the k slots
     int my_slot = -1, my_prow = -1;
+    // a token's expert indices, for the repeated-index check of the ranking
+    const int my_e = lane < k ? __ldg(idx + static_cast<int64_t>(t) * k + lane) : -1;
+    bool repeated = false;
+#pragma unroll
+    for (int jj = 0; jj < KMAX; ++jj) {
+      const int o = __shfl_sync(0xffffffffu, my_e, jj);
+      repeated |= (jj < k && jj < lane && o == my_e);
+    }
     if (lane < k) {
       const int64_t a = static_cast<int64_t>(t) * k + lane;
-      const int e = __ldg(idx + a);
-      if (e >= 0 && e < E) {
+      const int e = my_e;
+      if (e >= 0 && e < E && !repeated) {
         const int r = s_pre[e] + __ldg(crank + a);
         my_slot = (r < __ldg(kept + e)) ? __ldg(offsets + e) + r : -1;
         if constexpr (MXQ) my_prow = my_slot >= 0 ? s_poff[e] + r : -1;

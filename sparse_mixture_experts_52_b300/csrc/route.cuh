@@ -315,52 +315,44 @@ __device__ __forceinline__ void flush_stats(const LaneStats<NPL>& st, int E, flo
 // ---------------------------------------------------------------- ranking
 // Ranks the assignments of chunk `g` (tokens 32g .. 32g+31, lane = token)
 // given each lane's experts e[j] (-1 for none: a token past T or an index
-// outside [0, E)); writes crank and the chunk's entries of hist, and adds its
-// counts to the totals.  s_hist is this warp's zeroed [E] counter row; it is
+// outside [0, E); a token's valid experts are distinct); writes crank and the
+// chunk's entries of hist, and adds its counts to the totals.  s_mask is this
+// warp's zeroed [E] row of token masks: bit l of s_mask[x] says that the
+// chunk's token l chose expert x, so the rank of (t, j) among the chunk's
+// assignments to e[j] is the number of lower lanes in s_mask[e[j]] and the
+// chunk's count of expert x is the number of bits of s_mask[x].  s_mask is
 // zero again on return.
 template <int KMAX>
 __device__ __forceinline__ void rank_chunk_experts(const DispatchArgs& a, const int (&e)[KMAX],
-                                                   int g, int* s_hist) {
+                                                   int g, int* s_mask) {
   const int lane = threadIdx.x & 31;
   const int t = g * kChunk + lane;
   const bool valid_t = t < a.T;
-  int r[KMAX];
+  unsigned int* mask = reinterpret_cast<unsigned int*>(s_mask);
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) r[j] = 0;
-  // r[j] = number of tokens before this lane's in the chunk that chose e[j]
-  for (int src = 0; src < kChunk - 1; ++src) {
-#pragma unroll
-    for (int jj = 0; jj < KMAX; ++jj) {
-      if (jj < a.k) {
-        const int o = __shfl_sync(0xffffffffu, e[jj], src);
-        if (src < lane && o >= 0) {
-#pragma unroll
-          for (int j = 0; j < KMAX; ++j) r[j] += (e[j] == o) ? 1 : 0;
-        }
-      }
-    }
-  }
+  for (int j = 0; j < KMAX; ++j)
+    if (j < a.k && valid_t && e[j] >= 0) atomicOr(mask + e[j], 1u << lane);
+  __syncwarp();
+  const unsigned int lower = (1u << lane) - 1u;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    if (j < a.k && valid_t) {
-      a.crank[static_cast<int64_t>(t) * a.k + j] = r[j];
-      if (e[j] >= 0) atomicAdd(s_hist + e[j], 1);
-    }
+    if (j < a.k && valid_t)
+      a.crank[static_cast<int64_t>(t) * a.k + j] = e[j] >= 0 ? __popc(mask[e[j]] & lower) : 0;
   }
   __syncwarp();
   const int ncs = chunk_stride(a.T);
   for (int x = lane; x < a.E; x += 32) {
-    const int c = s_hist[x];
+    const int c = __popc(mask[x]);
     a.hist[static_cast<int64_t>(x) * ncs + g] = c;
     if (c) atomicAdd(a.totals + x, c);
-    s_hist[x] = 0;
+    mask[x] = 0u;
   }
   __syncwarp();
 }
 
 // The same, reading the experts of the chunk's tokens from `idx` (from L2,
-// ld.cg: this grid may have just written it).  An index outside [0, E) sets
-// the status bit and counts as no expert.
+// ld.cg: this grid may have just written it).  An index outside [0, E), or one
+// a token's row already holds, sets the status bit and counts as no expert.
 template <int KMAX>
 __device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t* idx, int g,
                                            int* s_hist) {
@@ -372,7 +364,10 @@ __device__ __forceinline__ void rank_chunk(const DispatchArgs& a, const int32_t*
     e[j] = -1;
     if (j < a.k && t < a.T) {
       const int v = __ldcg(idx + static_cast<int64_t>(t) * a.k + j);
-      if (v >= 0 && v < a.E) {
+      bool repeated = false;
+#pragma unroll
+      for (int jj = 0; jj < KMAX; ++jj) repeated |= (jj < j && e[jj] == v);
+      if (v >= 0 && v < a.E && !repeated) {
         e[j] = v;
       } else {
         atomicOr(a.err, DEV_ERR_BAD_EXPERT_INDEX);

@@ -353,9 +353,9 @@ def test_invalid_argument_enqueues_nothing():
 
 
 def test_out_of_range_expert_index_is_dropped_and_reported():
-    """moe_permute takes caller-supplied indices: one outside [0, E) drops that
-    assignment (slot -1), the others are dispatched as usual, and the status
-    word reports MOE_ERR_INVALID_ARG."""
+    """moe_permute takes caller-supplied indices: one outside [0, E), or one
+    repeated in its token's row, drops that assignment (slot -1), the others
+    are dispatched as usual, and the status word reports MOE_ERR_INVALID_ARG."""
     cfg = synth.workload("switch_top1_cap", T=96, d_model=64, d_ff=64, E=8, k=2,
                          capacity_factor=0.0, renorm=1, aux_f="topk_count")
     T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
@@ -364,6 +364,7 @@ def test_out_of_range_expert_index_is_dropped_and_reported():
     idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
     idx[5, 1] = E + 3
     idx[40, 0] = -1
+    idx[60, 1] = idx[60, 0]          # a repeated expert: the second occurrence drops
     idx = idx.to(DEV)
     ws = moe.new_workspace(cfg, DEV)
     z = lambda shape, t: torch.empty(shape, dtype=t, device=DEV)
@@ -377,14 +378,23 @@ def test_out_of_range_expert_index_is_dropped_and_reported():
     assert ei.value.status == 1
     moe.check_status(ws)          # the status word was cleared by the read
     slot = o["slot_of"].cpu().view(T, k)
-    assert slot[5, 1] == -1 and slot[40, 0] == -1
+    assert slot[5, 1] == -1 and slot[40, 0] == -1 and slot[60, 1] == -1 and slot[60, 0] >= 0
     good = idx.cpu().clone()
     good[5, 1] = -1
     good[40, 0] = -1
+    good[60, 1] = -1
     want = torch.bincount(good[good >= 0].long(), minlength=E)
     assert torch.equal(o["counts"].cpu(), want.to(torch.int32))
-    assert int(o["offsets"][-1]) == T * k - 2
-    assert int((slot >= 0).sum()) == T * k - 2
+    assert int(o["offsets"][-1]) == T * k - 3
+    assert int((slot >= 0).sum()) == T * k - 3
+    # every kept assignment has a slot of its own, and perm_token inverts it
+    kept = slot[slot >= 0]
+    assert len(set(kept.tolist())) == kept.numel()
+    pt = o["perm_token"].cpu()
+    for t in range(T):
+        for j in range(k):
+            if slot[t, j] >= 0:
+                assert int(pt[slot[t, j]]) == t
 
 
 # ---------------------------------------------------------------- Expert Choice
