@@ -185,12 +185,12 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
  *   return MOE_ERR_UNSUPPORTED with nothing enqueued.
  *   Memory: every GPU that loads the library holds the array (8 MiB plus a
  *   2 KiB header) until the process exits.
- *   Set-up: the first call on a device (with that device current) looks up
- *   the array's device address and clears the header (a block counter and
- *   per-expert totals, which must start at zero) on `stream`; every call
- *   leaves them at zero again.  Make that first call before any stream
- *   capture.  No call allocates (no
- *   cudaMalloc, no cudaFree).
+ *   Set-up: every call looks up the array's device address on the current
+ *   device; the first call on a device -- and the first after a device reset,
+ *   which gives the array a new, undefined copy -- clears the header (a block
+ *   counter and per-expert totals, which must start at zero) on `stream`;
+ *   every call leaves them at zero again.  Make that first call before any
+ *   stream capture.  No call allocates (no cudaMalloc, no cudaFree).
  *   Concurrency: all calls on one device share the one array, so calls whose
  *   kernels may overlap on the GPU (different streams without ordering) race
  *   and give wrong results; serialise them on one stream.

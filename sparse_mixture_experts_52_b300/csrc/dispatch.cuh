@@ -36,7 +36,7 @@ namespace moe {
 // (bf16 rows, d a multiple of 128): each token's row is quantised once (32-
 // element blocks over four lanes' 16-byte vectors) and its codes and scale
 // bytes are written to the padded row of each kept slot: expert e's rows start
-// at 128 * (row blocks of the experts before it), rank r inside.
+// at kPadRows * (row blocks of the experts before it), rank r inside.
 template <int KMAX, bool MXQ = false>
 __global__ void __launch_bounds__(256)
 k_permute(const int32_t* __restrict__ idx, const int32_t* __restrict__ crank,

@@ -48,8 +48,9 @@
 // replicated into the four lane quarters), so that row m's scale for k-block
 // j sits in lane m, column base + m / 32, byte j; the four k-blocks of a stage
 // are four block-scaled MMAs of K = 32 selecting bytes 0..3.  The routed rows
-// of A (and of a hidden activation the kernel writes) start at 128-row
-// aligned ("padded") offsets, so every tile's rows are one scale block.  An
+// of A (and of a hidden activation the kernel writes) start at 256-row
+// aligned ("padded") offsets (kPadRows), so every tile's rows are whole
+// scale blocks.  An
 // up-projection with MX output quantises its tile of the hidden activation in
 // the epilogue: each thread holds one row, takes the largest magnitude of
 // every 32 columns, and writes e4m3 codes plus the scale bytes.
@@ -285,15 +286,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   if (args.ready_mode != READY_WAIT) griddep_wait();
   griddep_launch_dependents();
   build_group_table<BM>(gs, n_tiles, c.tb);   // synchronises the block
-  if (args.pad_rows) {
-    // routed groups at 128-row aligned offsets: the row blocks of the groups before
-    for (int g = threadIdx.x; g < gs.E; g += blockDim.x) {
-      const int prow = (c.tb.tile_start[g] / n_tiles) * BM;
-      if (args.pad_rows & 1) c.tb.a_row0[g] = prow;
-      if (args.pad_rows & 2) c.tb.out_row0[g] = prow;
-    }
-    __syncthreads();
-  }
+  if (args.pad_rows) pad_group_rows(c.tb, gs.E, args.pad_rows);   // MX: padded group starts
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

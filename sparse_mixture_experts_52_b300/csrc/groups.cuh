@@ -89,6 +89,37 @@ __device__ __forceinline__ void build_group_table(const GroupSpec& gs, int n_til
   __syncthreads();
 }
 
+// MX FP8 activations keep every routed group's rows at a multiple of
+// kPadRows (one CTA-pair tile): group g starts at kPadRows * (the blocks of
+// kPadRows rows the groups before it need).
+constexpr int kPadRows = 256;
+
+// Sets a_row0 (bit 0 of `which`) and / or out_row0 (bit 1) of the routed
+// groups to those padded starts.  Every thread of the block must call it.
+__device__ __forceinline__ void pad_group_rows(GroupTable& tb, int E, int which) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int g = base + lane;
+      const int blocks = g < E ? (tb.rows[g] + kPadRows - 1) / kPadRows : 0;
+      int v = blocks;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (g < E) {
+        const int start = (carry + v - blocks) * kPadRows;
+        if (which & 1) tb.a_row0[g] = start;
+        if (which & 2) tb.out_row0[g] = start;
+      }
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
 // Tile t (t < tile_start[G]) -> group g, row block and column block.
 template <int BM>
 __device__ __forceinline__ void decode_tile(const GroupTable& tb, int G, int t, int& g,

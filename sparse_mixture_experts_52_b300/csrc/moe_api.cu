@@ -93,9 +93,10 @@ moe_status validate(const moe_config* c) {
 
 bool mx_experts(const moe_config& c) { return c.expert_fmt == MOE_EXPERT_MXFP8; }
 
-// Rows of the MX activations: each expert's rows start at a multiple of 128.
+// Rows of the MX activations: each expert's rows start at a multiple of kPadRows.
 int64_t mx_padded_rows(const moe_config& c) {
-  return (static_cast<int64_t>(c.T) * c.k + 127 * static_cast<int64_t>(c.E) + 127) / 128 * 128;
+  return (static_cast<int64_t>(c.T) * c.k + (kPadRows - 1) * static_cast<int64_t>(c.E) +
+          kPadRows - 1) / kPadRows * kPadRows;
 }
 
 int capacity_of(const moe_config& c) {
@@ -961,22 +962,24 @@ static __device__ __align__(256) int32_t
     g_noalloc_scratch[kNoallocHeader + kNoallocAssignments + kNoallocChunkCounts];
 
 // Device address of g_noalloc_scratch on the current device, or null when the
-// set-up fails.  The first call on each device looks the address up and clears
-// the header on `st` (stream ordered before the first use).
+// set-up fails.  Every call looks the address up (a host-side query); when it
+// differs from the one this device had before -- the first call, or a new
+// context after a device reset, whose copy of the array starts undefined --
+// the header is cleared on `st`, stream ordered before the first use.
 int32_t* noalloc_scratch(cudaStream_t st) {
   constexpr int kMaxDevices = 64;
-  static int32_t* addr[kMaxDevices] = {};
+  static void* addr[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+  if (addr[dev] != p) {
     if (cudaMemsetAsync(p, 0, kNoallocHeader * sizeof(int32_t), st) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<int32_t*>(p);
+    addr[dev] = p;
   }
-  return addr[dev];
+  return static_cast<int32_t*>(p);
 }
 
 struct FfnIn {
@@ -995,7 +998,7 @@ struct FfnScatter {
 
 // The grouped FFN on MX FP8 operands: the expert-ordered rows (quantised by
 // the permute, or here from the caller's bf16 x_perm) and the hidden
-// activation at 128-row aligned group offsets in the workspace, the packed
+// activation at kPadRows-aligned group offsets in the workspace, the packed
 // weights, block-scaled tcgen05 MMAs.  Routed experts only.
 moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn& in,
                      void* y_perm, cudaStream_t st, const FfnScatter* scatter) {

@@ -15,7 +15,7 @@
 //                      (SwiGLU weights: gate and up rows interleaved in
 //                      64-row halves, so a 128-row tile holds 64 of each)
 //  k_quant_rows_mx     expert-ordered bf16 rows (moe_grouped_ffn's x_perm)
-//                      -> codes + scales at 128-row aligned group offsets
+//                      -> codes + scales at kPadRows-aligned group offsets
 // The whole-layer pass quantises its rows in the permute kernel instead
 // (dispatch.cuh, k_permute with MX output).
 #pragma once
@@ -93,8 +93,9 @@ k_quant_weights_mx(const __nv_bfloat16* __restrict__ w, int G, int N, int K, int
   }
 }
 
-// Padded offsets of E groups: 128 * (row blocks of the groups before), from
-// the group starts `offsets` [E + 1] (or the kept counts when `kept` is given).
+// Padded offsets of E groups: kPadRows * (blocks of kPadRows rows the groups
+// before need), from the group starts `offsets` [E + 1] (or the kept counts
+// when `kept` is given) -- the starts the GEMM derives (pad_group_rows).
 // Every thread of the block must call it; warp 0 computes, the block syncs.
 __device__ __forceinline__ void padded_offsets(const int32_t* offsets, const int32_t* kept,
                                                int E, int* s_poff) {
@@ -105,13 +106,13 @@ __device__ __forceinline__ void padded_offsets(const int32_t* offsets, const int
       const int e = base + lane;
       int n = 0;
       if (e < E) n = kept ? __ldg(kept + e) : __ldg(offsets + e + 1) - __ldg(offsets + e);
-      int v = (n + 127) >> 7;
+      int v = (n + kPadRows - 1) / kPadRows;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += u;
       }
-      if (e < E) s_poff[e + 1] = (carry + v) * 128;
+      if (e < E) s_poff[e + 1] = (carry + v) * kPadRows;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
     if (lane == 0) s_poff[0] = 0;

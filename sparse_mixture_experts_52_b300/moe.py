@@ -272,8 +272,9 @@ def permute(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of, x_perm
           _stream(stream))
 
 
-# limits of moe_permute_noalloc (MOE_PERMUTE_NOALLOC_MAX_* in moe.h): T*k and
-# ceil(T/32)*E
+# limits of moe_permute_noalloc (MOE_PERMUTE_NOALLOC_MAX_* in moe.h): T*k, and
+# the per-chunk expert counts 32*ceil(ceil(T/32)/32)*E (each expert's row of
+# 32-token chunk counts padded to a multiple of 32 chunks)
 PERMUTE_NOALLOC_MAX_ASSIGNMENTS = 1 << 20
 PERMUTE_NOALLOC_MAX_CHUNK_COUNTS = 1 << 20
 
@@ -286,7 +287,7 @@ def permute_noalloc(cfg, x, topk_idx, counts, kept, offsets, perm_token, slot_of
     fixed 8 MiB array inside the library.  The first call on a device must come
     before any stream capture; calls that may overlap on the GPU race, because
     they share that array.  Raises MoEError (MOE_ERR_UNSUPPORTED) when
-    T*k > PERMUTE_NOALLOC_MAX_ASSIGNMENTS or ceil(T/32)*E >
+    T*k > PERMUTE_NOALLOC_MAX_ASSIGNMENTS or 32*ceil(ceil(T/32)/32)*E >
     PERMUTE_NOALLOC_MAX_CHUNK_COUNTS.
     """
     T, d, E, k = cfg["T"], cfg["d_model"], cfg["E"], cfg["k"]
