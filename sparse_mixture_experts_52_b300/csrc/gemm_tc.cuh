@@ -227,6 +227,98 @@ struct TcSmem {
   }
 };
 
+// The up-projection's epilogue with MX FP8 output, for one row of a tile
+// (this thread's TMEM lane): the activation of the tile's BN accumulator
+// columns (for SwiGLU the gate half times SiLU, the up half as the second
+// factor), then per 32 output columns the largest magnitude, the E8M0 scale
+// and the e4m3 codes, stored at row `orow` of the hidden activation, and the
+// row's scale bytes in the interleaved block of its 128 rows and its
+// 128-column stage.  `add` folds in stream-K partials of a 16-column chunk
+// (a no-op without stream-K).  Every lane of the warp must call it (the
+// tensor-memory loads are warp-wide); `valid` only gates the stores.
+template <int EPI, int BN, typename AddPartials>
+__device__ __forceinline__ void mx_store_row(uint32_t trow, int n_blk, bool valid, int64_t orow,
+                                             const __nv_bfloat16* bias, const TcArgs& args,
+                                             AddPartials&& add) {
+  constexpr bool GLU = epi_glu(EPI);
+  constexpr int NCC = BN / 16;
+  constexpr int BNO = GLU ? BN / 2 : BN;
+  constexpr int NOUT = GLU ? NCC / 2 : NCC;
+  uint32_t sfw = 0;   // the blocks' scale bytes, byte j = block j of the 128-column stage
+#pragma unroll 1
+  for (int cb = 0; cb < NOUT / 2; ++cb) {
+    float v[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cc = 2 * cb + h;
+      uint32_t r[16], ru[GLU ? 16 : 1];
+      tmem_ld_32x32b_x16(trow + cc * 16, r);
+      tmem_wait_ld(r);
+      if constexpr (GLU) {
+        tmem_ld_32x32b_x16(trow + (cc + NCC / 2) * 16, ru);
+        tmem_wait_ld(ru);
+      }
+      const int col = n_blk * BNO + cc * 16;
+      float a[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(r[i]);
+      add(cc, a);
+      if (bias) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] += __bfloat162float(bias[col + i]);
+      }
+      if constexpr (GLU) {
+        float u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = __uint_as_float(ru[i]);
+        add(cc + NCC / 2, u);
+        if (bias) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] += __bfloat162float(bias[args.N + col + i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = silu(a[i]) * u[i];
+      } else if (EPI == EPI_SILU_MX) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = silu(a[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = gelu_erf(a[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[16 * h + i] = a[i];
+    }
+    const int col = n_blk * BNO + cb * 32;
+    if (!valid) continue;
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float inv;
+    const uint32_t sbyte = mx_scale(amax, inv);
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      pk[i] = static_cast<uint32_t>(cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv)) |
+              (static_cast<uint32_t>(cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv)) << 16);
+    uint8_t* o = static_cast<uint8_t*>(args.out) + orow * args.ldo + col;
+    *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4*>(o + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    sfw |= sbyte << (8 * ((col >> 5) & 3));
+  }
+  if (valid) {
+    const int col0 = n_blk * BNO;
+    uint8_t* sfp = args.sf_out +
+                   ((static_cast<int64_t>(col0 >> 7) * args.sf_out_rb + (orow >> 7)) * 512) +
+                   (orow & 31) * 16 + ((orow & 127) >> 5) * 4;
+    if constexpr (BNO >= 128) {
+      *reinterpret_cast<uint32_t*>(sfp) = sfw;
+    } else {
+      const int j0 = (col0 >> 5) & 3;
+      *reinterpret_cast<uint16_t*>(sfp + j0) = static_cast<uint16_t>(sfw >> (8 * j0));
+    }
+  }
+}
+
 template <int BN, int STAGES, int EPI, bool MX = false>
 __global__ void __launch_bounds__(192, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
@@ -545,84 +637,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         }
       };
       constexpr int NOUT = GLU ? NCC / 2 : NCC;   // 16-column output chunks
-      if constexpr (MXO) {
-        // ---- the hidden activation in MX FP8: 32-column blocks of this row
-        uint32_t sfw = 0;   // the blocks' scale bytes, byte j = block j of the 128-column stage
-#pragma unroll 1
-        for (int cb = 0; cb < NOUT / 2; ++cb) {
-          float v[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int cc = 2 * cb + h;
-            uint32_t r[16], ru[GLU ? 16 : 1];
-            tmem_ld_32x32b_x16(trow + cc * 16, r);
-            tmem_wait_ld(r);
-            if constexpr (GLU) {
-              tmem_ld_32x32b_x16(trow + (cc + NCC / 2) * 16, ru);
-              tmem_wait_ld(ru);
-            }
-            const int col = n_blk * BNO + cc * 16;
-            float a[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(r[i]);
-            add_partials(cc, a);
-            if (bias) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) a[i] += __bfloat162float(bias[col + i]);
-            }
-            if constexpr (GLU) {
-              float u[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) u[i] = __uint_as_float(ru[i]);
-              add_partials(cc + NCC / 2, u);
-              if (bias) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) u[i] += __bfloat162float(bias[args.N + col + i]);
-              }
-#pragma unroll
-              for (int i = 0; i < 16; ++i) a[i] = silu(a[i]) * u[i];
-            } else if (EPI == EPI_SILU_MX) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) a[i] = silu(a[i]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) a[i] = gelu_erf(a[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[16 * h + i] = a[i];
-          }
-          const int col = n_blk * BNO + cb * 32;
-          if (!valid) continue;
-          float amax = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-          float inv;
-          const uint32_t sbyte = mx_scale(amax, inv);
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            pk[i] = static_cast<uint32_t>(cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv)) |
-                    (static_cast<uint32_t>(cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv)) << 16);
-          uint8_t* o = static_cast<uint8_t*>(args.out) + orow * args.ldo + col;
-          *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(o + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          sfw |= sbyte << (8 * ((col >> 5) & 3));
-        }
-        if (valid) {
-          // this row's scale bytes of the tile's columns, in the interleaved
-          // block of its 128 rows and its 128-column stage
-          const int col0 = n_blk * BNO;
-          uint8_t* sfp = args.sf_out +
-                         ((static_cast<int64_t>(col0 >> 7) * args.sf_out_rb + (orow >> 7)) * 512) +
-                         (orow & 31) * 16 + ((orow & 127) >> 5) * 4;
-          if constexpr (BNO >= 128) {
-            *reinterpret_cast<uint32_t*>(sfp) = sfw;
-          } else {
-            const int j0 = (col0 >> 5) & 3;
-            *reinterpret_cast<uint16_t*>(sfp + j0) = static_cast<uint16_t>(sfw >> (8 * j0));
-          }
-        }
-      }
+      if constexpr (MXO) mx_store_row<EPI, BN>(trow, n_blk, valid, orow, bias, args, add_partials);
 #pragma unroll 1
       for (int cc = 0; cc < (MXO ? 0 : NOUT); ++cc) {
         uint32_t r[16], ru[GLU ? 16 : 1];

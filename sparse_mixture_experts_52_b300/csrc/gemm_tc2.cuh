@@ -20,6 +20,8 @@
 // tiles p, p + P, ... in the group-major order of groups.cuh with 256-row
 // blocks.
 //
+// The block-scaled MX FP8 product runs on its own pair kernel (gemm_mx2.cuh).
+//
 // Every wait is bounded; a wait that runs out records MOE_DEV_ERR_* in the
 // status word and raises the CTA's abort flag; both CTAs still meet at the
 // final cluster barrier (their other waits give up in turn), so a bad launch
@@ -106,10 +108,10 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
 
 template <int BN, int STAGES>
 struct Tc2Smem {
-  static constexpr int BM = 256, BK = 64;                // tile rows (pair), k-step
-  static constexpr uint32_t A_BYTES = 128 * BK * 2;      // this CTA's 128 rows
-  static constexpr uint32_t B_BYTES = (BN / 2) * BK * 2; // this CTA's BN/2 columns
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BM = 256, BK = 64;                // tile rows (pair); K per stage
+  static constexpr uint32_t A_BYTES = 128 * 128;         // this CTA's 128 rows
+  static constexpr uint32_t B_BYTES = (BN / 2) * 128;    // this CTA's BN/2 columns
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;   // bytes of one CTA
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   struct Ctrl {
     uint64_t full[STAGES];    // even CTA: both halves landed
@@ -121,7 +123,9 @@ struct Tc2Smem {
     int abort_flag;
     GroupTable tb;
   };
-  static constexpr size_t bytes() { return 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl); }
+  static constexpr size_t bytes() {
+    return 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+  }
 };
 
 template <int BN, int STAGES, int EPI>
@@ -133,7 +137,7 @@ k_gemm_tc2(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUte
   constexpr int BM = L::BM, BK = L::BK;
   constexpr int NCC = BN / 16;
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
-  static_assert(EPI != EPI_GELU_MX && EPI != EPI_SILU_MX && EPI != EPI_SWIGLU_MX, "bf16 only");
+  static_assert(!epi_mx_out(EPI), "MX outputs come from the MX pair kernel");
   constexpr bool GLU = epi_glu(EPI);
   constexpr int BNO = GLU ? BN / 2 : BN;
 

@@ -16,6 +16,7 @@
 #include "expert_choice.cuh"
 #include "gemm_tc.cuh"
 #include "gemm_tc2.cuh"
+#include "gemm_mx2.cuh"
 #include "groups.cuh"
 #include "mxfp8.cuh"
 #include "route.cuh"
@@ -305,17 +306,32 @@ bool map_u8_a(CUtensorMap* m, const void* base, int64_t K, int64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// MX FP8 codes [G, N, K] bytes, box = 1 x 128 rows x 128 bytes
-bool map_u8_b(CUtensorMap* m, const void* base, int64_t K, int64_t N, int64_t G) {
+// MX FP8 codes [G, N, K] bytes, box = 1 x box_rows x 128 bytes
+bool map_u8_b(CUtensorMap* m, const void* base, int64_t K, int64_t N, int64_t G,
+              int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(std::max<int64_t>(G, 1))};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
-  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MX scale blocks as a tensor of n_blocks blocks of 32 rows x 16 bytes; a box
+// is one 512-byte block, copied as it lies
+bool map_sf_blocks(CUtensorMap* m, const void* base, int64_t n_blocks) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {16, 32, static_cast<cuuint64_t>(std::max<int64_t>(n_blocks, 1))};
+  cuuint64_t strides[2] = {16, 512};
+  cuuint32_t box[3] = {16, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -388,7 +404,8 @@ moe_status launch_tc2_inst(const CUtensorMap& a0, const CUtensorMap& a1, const C
   const int64_t pairs = std::min<int64_t>(std::max<int64_t>(pair_tiles_ub, 1), max_pairs[dev]);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, k_gemm_tc2<BN, STAGES, EPI>, a0, a1, b0, b1, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, k_gemm_tc2<BN, STAGES, EPI>, a0, a1, b0, b1, args) !=
+      cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -407,6 +424,69 @@ moe_status launch_tc2(int epi, const CUtensorMap& a0, const CUtensorMap& a1,
   MOE_PAIR_EPI(EPI_F32)
   MOE_PAIR_EPI(EPI_SCATTER_BF16)
 #undef MOE_PAIR_EPI
+  return MOE_ERR_UNSUPPORTED;
+}
+
+// The block-scaled MX FP8 GEMMs on CTA pairs (gemm_mx2.cuh): 256 x 256 tiles,
+// 6 stages of 33.5 KB a CTA, 320 threads; as many pairs as fit (persistent)
+// up to the number of tiles.  sfa / sfb are the scale-block maps of A and B.
+template <int STAGES, int EPI>
+moe_status launch_mx2_inst(const CUtensorMap& a, const CUtensorMap& sfa, const CUtensorMap& b,
+                           const CUtensorMap& sfb, const TcArgs& args, int64_t pair_tiles_ub,
+                           cudaStream_t st) {
+  constexpr size_t smem = Mx2Smem<STAGES>::bytes();
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(320);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+  if (max_pairs[dev] == 0) {
+    if (cudaFuncSetAttribute(k_gemm_mx2<STAGES, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    cfg.gridDim = dim3(2 * num_sms());
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_mx2<STAGES, EPI>, &cfg) != cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    max_pairs[dev] = n;
+  }
+  const int64_t pairs = std::min<int64_t>(std::max<int64_t>(pair_tiles_ub, 1), max_pairs[dev]);
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, k_gemm_mx2<STAGES, EPI>, a, sfa, b, sfb, args) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status launch_mx2(int epi, const CUtensorMap& a, const CUtensorMap& sfa, const CUtensorMap& b,
+                      const CUtensorMap& sfb, const TcArgs& args, int64_t pair_tiles_ub,
+                      cudaStream_t st) {
+#define MOE_MX2_EPI(EPI) \
+  if (epi == EPI) return launch_mx2_inst<6, EPI>(a, sfa, b, sfb, args, pair_tiles_ub, st);
+  MOE_MX2_EPI(EPI_GELU_MX)
+  MOE_MX2_EPI(EPI_SILU_MX)
+  MOE_MX2_EPI(EPI_SWIGLU_MX)
+  MOE_MX2_EPI(EPI_BIAS_BF16)
+  MOE_MX2_EPI(EPI_F32)
+  MOE_MX2_EPI(EPI_SCATTER_BF16)
+#undef MOE_MX2_EPI
   return MOE_ERR_UNSUPPORTED;
 }
 
@@ -1021,17 +1101,31 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
   }
   const uint8_t* w1 = static_cast<const uint8_t*>(in.w1);
   const uint8_t* w2 = static_cast<const uint8_t*>(in.w2);
-  CUtensorMap ma, mb, ha, hb;
-  if (!map_u8_a(&ma, xq, d, R) || !map_u8_b(&mb, w1, d, F1, E) || !map_u8_a(&ha, hq, F, R) ||
-      !map_u8_b(&hb, w2, F, d, E))
+  // experts of 512 rows or more: CTA pairs with 256 x 256 tiles (weight rows
+  // in 64-row boxes), when both projections' weight rows are whole tiles
+  const bool pair = Tk >= 512 * static_cast<int64_t>(E) && F1 % 256 == 0 && d % 256 == 0;
+  const int b_rows = pair ? 64 : 128;
+  CUtensorMap ma, mb, ha, hb, sxa, sw1, sha, sw2;
+  if (!map_u8_a(&ma, xq, d, R) || !map_u8_b(&mb, w1, d, F1, E, b_rows) ||
+      !map_u8_a(&ha, hq, F, R) || !map_u8_b(&hb, w2, F, d, E, b_rows))
+    return MOE_ERR_CUDA;
+  // the pair kernel loads the scale blocks with TMA: maps over them
+  if (pair && (!map_sf_blocks(&sxa, xq_sf, (d / 128) * RB) ||
+               !map_sf_blocks(&sw1, w1 + static_cast<int64_t>(E) * F1 * d,
+                              static_cast<int64_t>(E) * (d / 128) * (F1 / 128)) ||
+               !map_sf_blocks(&sha, hq_sf, (F / 128) * RB) ||
+               !map_sf_blocks(&sw2, w2 + static_cast<int64_t>(E) * d * F,
+                              static_cast<int64_t>(E) * (F / 128) * (d / 128))))
     return MOE_ERR_CUDA;
   const int64_t row_tiles_ub = (Tk + 127) / 128 + E;
   const int64_t rt = est_row_tiles(Tk, E);
   const int sms = num_sms();
-  // whole tiles round robin unless there are 8 waves or more: stream-K tail
-  const bool sk_up = rt * (F1 / 128) >= 8 * static_cast<int64_t>(sms);
-  const bool sk_dn = rt * (d / 128) >= 8 * static_cast<int64_t>(sms);
-  const bool overlap = !sk_up && !sk_dn;
+  // single CTAs: whole tiles round robin unless there are 8 waves or more
+  // (stream-K tail); CTA pairs: whole tiles only
+  const bool sk_up = !pair && rt * (F1 / 128) >= 8 * static_cast<int64_t>(sms);
+  const bool sk_dn = !pair && rt * (d / 128) >= 8 * static_cast<int64_t>(sms);
+  const bool overlap = !pair && !sk_up && !sk_dn;
+  const int64_t pair_rows = (Tk + 255) / 256 + E;
   TcArgs up{};
   up.gs = GroupSpec{in.offsets, E, 0, 0, c.T, 0, 0, 0, 0};
   up.N = F;
@@ -1056,7 +1150,9 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
     up.ready = at<int>(ws, L.status + kReadyOffset);
   }
   const int epi_up = glu ? EPI_SWIGLU_MX : (c.act == MOE_ACT_SILU ? EPI_SILU_MX : EPI_GELU_MX);
-  if ((s = launch_tc_mx(epi_up, ma, mb, up, row_tiles_ub, st)) != MOE_OK) return s;
+  if ((s = pair ? launch_mx2(epi_up, ma, sxa, mb, sw1, up, pair_rows * (F1 / 256), st)
+                : launch_tc_mx(epi_up, ma, mb, up, row_tiles_ub, st)) != MOE_OK)
+    return s;
   TcArgs dn{};
   dn.gs = GroupSpec{in.offsets, E, 0, 0, c.T, 0, 0, 0, 0};
   dn.N = d;
@@ -1080,13 +1176,14 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
     dn.ready_done = at<unsigned int>(ws, L.status + kReadyDoneOffset);
     dn.ready_up_tiles = F / (glu ? 64 : 128);
   }
+  const int epi_dn = scatter ? EPI_SCATTER_BF16 : (c.y_f32 ? EPI_F32 : EPI_BIAS_BF16);
   if (scatter) {
     dn.out = scatter->out;
     dn.scatter_token = scatter->perm_token;
     dn.scatter_w = scatter->w;
-    return launch_tc_mx(EPI_SCATTER_BF16, ha, hb, dn, row_tiles_ub, st);
   }
-  return launch_tc_mx(c.y_f32 ? EPI_F32 : EPI_BIAS_BF16, ha, hb, dn, row_tiles_ub, st);
+  return pair ? launch_mx2(epi_dn, ha, sha, hb, sw2, dn, pair_rows * (d / 256), st)
+              : launch_tc_mx(epi_dn, ha, hb, dn, row_tiles_ub, st);
 }
 
 // Experts holding 512 rows or more on average (compute-bound, many waves of

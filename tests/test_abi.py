@@ -82,7 +82,8 @@ def test_workspace_size_of_every_workload(lib, name):
     # x_perm + H + Y must fit
     assert n >= (T * k * d + (T * k + S * T) * F + T * k * d) * eb
     # MX FP8 experts add codes and scales of the rows at 128-row aligned offsets
-    mx = (T * k + 128 * cfg["E"]) * (d + F) * 33 // 32 if cfg.get("experts") == "mxfp8" else 0
+    # MX codes and scales of x and h at 256-row aligned expert offsets
+    mx = (T * k + 256 * cfg["E"] + 256) * (d + F) * 33 // 32 if cfg.get("experts") == "mxfp8" else 0
     assert n < 4 * (T * k * d + (T * k + S * T) * F + T * k * d) * eb + mx + (1 << 24)
 
 

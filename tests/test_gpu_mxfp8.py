@@ -113,6 +113,17 @@ SMALL = {
     "top2_y_f32": dict(name="mixtral_top2", T=300, d_model=128, d_ff=256, y_f32=1),
     # many waves: the stream-K tail of both projections
     "stream_k_tail": dict(name="mixtral_top2", T=4096, d_model=256, d_ff=4096),
+    # experts of >= 512 rows: the block-scaled CTA-pair GEMM (256 x 256 tiles)
+    "pair_top2_gelu": dict(name="mixtral_top2", T=2048, d_model=256, d_ff=512),
+    "pair_swiglu": dict(name="mixtral_top2", T=2048, d_model=256, d_ff=256, E=4,
+                        act="swiglu"),
+    "pair_top1_fused_combine": dict(name="switch_top1_cap", T=2048, d_model=256, d_ff=512, E=4),
+    "pair_silu_bias_y_f32": dict(name="mixtral_top2", T=2048, d_model=256, d_ff=256, E=4,
+                                 act="silu", has_bias=1, nonzero_bias=True, y_f32=1),
+    "pair_swiglu_bias_long_k": dict(name="mixtral_top2", T=1536, d_model=512, d_ff=1024, E=4,
+                                    act="swiglu", has_bias=1, nonzero_bias=True),
+    # many rows but weight rows not whole 256-row tiles: the single-CTA kernel
+    "many_rows_ragged_n": dict(name="mixtral_top2", T=2048, d_model=128, d_ff=384, E=4),
 }
 
 
@@ -135,6 +146,19 @@ def test_mx_layer_against_the_quantising_oracle(case):
         # the step-wise path quantises the same rows into the same layout
         assert np.array_equal(st["out"], fw["out"]), "steps and forward differ"
     print(case, rep.summary())
+
+
+def test_mx_full_mixtral_sampled_tokens():
+    """The Mixtral-shaped layer with MX FP8 experts (CTA pairs): routing on
+    every token, the output on 256 tokens spread over the batch."""
+    cfg = synth.workload("mixtral_top2_mxfp8")
+    inp = synth.make_inputs(cfg, device=DEV)
+    fw, layer = run_forward(cfg, inp)
+    rows = sorted(set(np.linspace(0, cfg["T"] - 1, 256).astype(int).tolist()))
+    rep = compare.check_layer(cfg, inp, fw, rows=rows)
+    print("mixtral_top2_mxfp8", rep.summary())
+    del layer, inp
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("name", ["switch_top1_cap_mxfp8", "decode_zipf_top2_mxfp8"])
