@@ -321,16 +321,17 @@ bool map_u8_b(CUtensorMap* m, const void* base, int64_t K, int64_t N, int64_t G,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// MX scale blocks as a tensor of n_blocks blocks of 32 rows x 16 bytes; a box
-// is one 512-byte block, copied as it lies
+// MX scale blocks (n_blocks contiguous 512-byte blocks) as rows of 256 bytes;
+// a box is one block (2 rows), copied as it lies.  Wide rows keep the copy to
+// two 256-byte requests.
 bool map_sf_blocks(CUtensorMap* m, const void* base, int64_t n_blocks) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {16, 32, static_cast<cuuint64_t>(std::max<int64_t>(n_blocks, 1))};
-  cuuint64_t strides[2] = {16, 512};
-  cuuint32_t box[3] = {16, 32, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(2 * std::max<int64_t>(n_blocks, 1))};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 2};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1101,10 +1102,10 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
   }
   const uint8_t* w1 = static_cast<const uint8_t*>(in.w1);
   const uint8_t* w2 = static_cast<const uint8_t*>(in.w2);
-  // experts of 512 rows or more: CTA pairs with 256 x 256 tiles (weight rows
-  // in 64-row boxes), when both projections' weight rows are whole tiles
+  // experts of 512 rows or more: CTA pairs with 256 x 256 tiles, when both
+  // projections' weight rows are whole tiles
   const bool pair = Tk >= 512 * static_cast<int64_t>(E) && F1 % 256 == 0 && d % 256 == 0;
-  const int b_rows = pair ? 64 : 128;
+  const int b_rows = 128;
   CUtensorMap ma, mb, ha, hb, sxa, sw1, sha, sw2;
   if (!map_u8_a(&ma, xq, d, R) || !map_u8_b(&mb, w1, d, F1, E, b_rows) ||
       !map_u8_a(&ha, hq, F, R) || !map_u8_b(&hb, w2, F, d, E, b_rows))
