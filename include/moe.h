@@ -239,14 +239,19 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
  * nearest e4m3 value (ties to even, saturating at +-448).
  *
  * moe_mxfp8_weight_bytes (host only): bytes of one packed tensor of G experts'
- * [N, K] weights: G*N*K code bytes, then G*N*K/32 scale bytes.  N and K must
- * be multiples of 128.
+ * [N, K] weights: G*N*K code bytes, G*N*K/32 scale bytes, then
+ * G*(K/128)*ceil(N/256) scale tile records of 4096 bytes.  N and K must be
+ * multiples of 128.
  *
  * moe_quantize_mxfp8: packs bf16 weights w [G, N, K] (device) into `packed`
  * (device, moe_mxfp8_weight_bytes bytes), stream-ordered.  Codes: [G, N, K]
  * row-major.  Scales: 512-byte blocks, block (g, k / 128, n / 128) at
  * ((g * K/128 + k/128) * N/128 + n/128) * 512, the scale of row n and k-block
  * j = (k / 32) % 4 at byte 16 (n % 32) + 4 ((n % 128) / 32) + j of its block.
+ * Tile records: record (g, k / 128, t) at ((g * K/128 + k/128) * ceil(N/256)
+ * + t) * 4096 holds scale blocks (g, k / 128, 2t) and (g, k / 128, 2t + 1),
+ * each four times in a row (the second all zeros when 2t + 1 = N/128): the
+ * copy a 256-row tile of the CTA-pair GEMM loads in one piece.
  * glu = 1 packs a SwiGLU w1 ([2F, K]: gate rows, then up rows) with its rows
  * interleaved in 64-row halves -- packed row 128 t + i is gate row 64 t + i
  * for i < 64, up row F + 64 t + i - 64 otherwise -- which is the order the

@@ -95,6 +95,9 @@ moe_status validate(const moe_config* c) {
 bool mx_experts(const moe_config& c) { return c.expert_fmt == MOE_EXPERT_MXFP8; }
 
 // Rows of the MX activations: each expert's rows start at a multiple of kPadRows.
+// 4 KB scale tile records of packed MX weights [G, N, K] (mxfp8.cuh)
+int64_t mx_tile_records(int64_t G, int64_t N, int64_t K) { return G * (K / 128) * ((N + 255) / 256); }
+
 int64_t mx_padded_rows(const moe_config& c) {
   return (static_cast<int64_t>(c.T) * c.k + (kPadRows - 1) * static_cast<int64_t>(c.E) +
           kPadRows - 1) / kPadRows * kPadRows;
@@ -322,14 +325,14 @@ bool map_u8_b(CUtensorMap* m, const void* base, int64_t K, int64_t N, int64_t G,
 }
 
 // MX scale blocks (n_blocks contiguous 512-byte blocks) as rows of 256 bytes;
-// a box is one block (2 rows), copied as it lies.  Wide rows keep the copy to
-// two 256-byte requests.
-bool map_sf_blocks(CUtensorMap* m, const void* base, int64_t n_blocks) {
+// a box is `box_blocks` consecutive blocks (8: a 4 KB tile record), copied as
+// they lie.  Wide rows keep a copy to few 256-byte requests.
+bool map_sf_blocks(CUtensorMap* m, const void* base, int64_t n_blocks, int box_blocks = 1) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(2 * std::max<int64_t>(n_blocks, 1))};
   cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {256, 2};
+  cuuint32_t box[2] = {256, static_cast<cuuint32_t>(2 * box_blocks)};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1112,11 +1115,11 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
     return MOE_ERR_CUDA;
   // the pair kernel loads the scale blocks with TMA: maps over them
   if (pair && (!map_sf_blocks(&sxa, xq_sf, (d / 128) * RB) ||
-               !map_sf_blocks(&sw1, w1 + static_cast<int64_t>(E) * F1 * d,
-                              static_cast<int64_t>(E) * (d / 128) * (F1 / 128)) ||
+               !map_sf_blocks(&sw1, w1 + static_cast<int64_t>(E) * F1 * d * 33 / 32,
+                              8 * mx_tile_records(E, F1, d), 8) ||
                !map_sf_blocks(&sha, hq_sf, (F / 128) * RB) ||
-               !map_sf_blocks(&sw2, w2 + static_cast<int64_t>(E) * d * F,
-                              static_cast<int64_t>(E) * (F / 128) * (d / 128))))
+               !map_sf_blocks(&sw2, w2 + static_cast<int64_t>(E) * d * F * 33 / 32,
+                              8 * mx_tile_records(E, d, F), 8)))
     return MOE_ERR_CUDA;
   const int64_t row_tiles_ub = (Tk + 127) / 128 + E;
   const int64_t rt = est_row_tiles(Tk, E);
@@ -1648,7 +1651,7 @@ moe_status moe_mxfp8_weight_bytes(int32_t G, int32_t N, int32_t K, size_t* bytes
   if (!bytes || G < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED;
   const size_t codes = static_cast<size_t>(G) * N * K;
-  *bytes = codes + codes / 32;
+  *bytes = codes + codes / 32 + mx_tile_records(G, N, K) * 4096;
   return MOE_OK;
 }
 
@@ -1662,10 +1665,15 @@ moe_status moe_quantize_mxfp8(const void* w, int32_t G, int32_t N, int32_t K, in
   const int64_t rows = static_cast<int64_t>(G) * N;
   if (rows > static_cast<int64_t>(INT_MAX) * 8) return MOE_ERR_UNSUPPORTED;
   uint8_t* codes = static_cast<uint8_t*>(packed);
+  uint8_t* sf = codes + static_cast<size_t>(G) * N * K;
   const int grid = static_cast<int>((rows + 7) / 8);
-  k_quant_weights_mx<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(w), G, N, K, glu, codes,
-      codes + static_cast<size_t>(G) * N * K);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  k_quant_weights_mx<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), G, N, K, glu,
+                                           codes, sf);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  const int64_t recs = mx_tile_records(G, N, K);
+  k_sf_tiles_mx<<<static_cast<unsigned>((recs * 256 + 255) / 256), 256, 0, st>>>(
+      sf, recs, N / 128, (N + 255) / 256, sf + static_cast<size_t>(G) * N * K / 32);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -93,6 +93,25 @@ k_quant_weights_mx(const __nv_bfloat16* __restrict__ w, int G, int N, int K, int
   }
 }
 
+// Scale tile records of packed weights: for each (expert g, 128-K stage s,
+// 256-row tile t) 4 KB at ((g * KS + s) * NT + t) * 4096 holding blocks 2t and
+// 2t + 1 of the scale blocks, each four times: [b2t x4 | b2t+1 x4] (zeros for
+// a block past the last, N / 128 odd).  One thread a 16-byte row of a copy.
+__global__ void __launch_bounds__(256)
+k_sf_tiles_mx(const uint8_t* __restrict__ sf, int64_t n_records, int NB, int NT,
+              uint8_t* __restrict__ tiles) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_records * 256) return;
+  const int64_t rec = i >> 8;                     // (g * KS + s) * NT + t
+  const int chunk = static_cast<int>(i & 255);    // copy (chunk / 32), row (chunk % 32)
+  const int t = static_cast<int>(rec % NT);
+  const int64_t gs = rec / NT;                    // g * KS + s
+  const int b = 2 * t + (chunk >> 7);
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (b < NB) v = *reinterpret_cast<const uint4*>(sf + (gs * NB + b) * 512 + (chunk & 31) * 16);
+  *reinterpret_cast<uint4*>(tiles + i * 16) = v;
+}
+
 // Padded offsets of E groups: kPadRows * (blocks of kPadRows rows the groups
 // before need), from the group starts `offsets` [E + 1] (or the kept counts
 // when `kept` is given) -- the starts the GEMM derives (pad_group_rows).

@@ -195,7 +195,10 @@ def test_mx_unsupported_configurations_are_rejected(lib):
 
 
 def test_mxfp8_weight_bytes(lib):
-    assert moe.mxfp8_weight_bytes(8, 256, 128) == 8 * 256 * 128 * 33 // 32
+    # codes, scale blocks, then 4 KB scale tile records per (expert, 128-K
+    # stage, 256-row tile)
+    assert moe.mxfp8_weight_bytes(8, 256, 128) == 8 * 256 * 128 * 33 // 32 + 8 * 1 * 1 * 4096
+    assert moe.mxfp8_weight_bytes(2, 384, 256) == 2 * 384 * 256 * 33 // 32 + 2 * 2 * 2 * 4096
     for G, N, K in ((8, 200, 128), (8, 256, 96)):
         with pytest.raises(moe.MoEError) as ei:
             moe.mxfp8_weight_bytes(G, N, K)

@@ -23,7 +23,9 @@ def _np(t):
 def packed_reference(w: np.ndarray, glu: bool):
     """The documented packed layout, built from the oracle's quantiser: codes
     [G, N, K], then 512-byte scale blocks (g, k / 128, n / 128) with the scale
-    of row n, k-block j at byte 16 (n % 32) + 4 ((n % 128) / 32) + j."""
+    of row n, k-block j at byte 16 (n % 32) + 4 ((n % 128) / 32) + j, then
+    4 KB tile records (g, k / 128, n / 256): blocks 2t and 2t + 1 four times
+    each (zeros past the last block)."""
     G, N, K = w.shape
     codes = np.empty((G, N, K), np.uint8)
     sf = np.zeros(G * N * K // 32, np.uint8)
@@ -41,13 +43,22 @@ def packed_reference(w: np.ndarray, glu: bool):
         kb = np.arange(K // 32)[None, :]
         off = ((g * KS + kb // 4) * NB + n // 128) * 512 + (n % 32) * 16 + ((n % 128) // 32) * 4 + kb % 4
         sf[off] = s
-    return codes, sf
+    NT = (NB + 1) // 2
+    blocks = sf.reshape(G, KS, NB, 512)
+    tiles = np.zeros((G, KS, NT, 8, 512), np.uint8)
+    for t in range(NT):
+        for r in range(8):
+            b = 2 * t + r // 4
+            if b < NB:
+                tiles[:, :, t, r] = blocks[:, :, b]
+    return codes, np.concatenate([sf, tiles.reshape(-1)])
 
 
 @pytest.mark.parametrize("glu", [False, True])
 def test_weight_packing_is_bit_exact(glu):
     g = torch.Generator(device=DEV).manual_seed(4)
-    G, N, K = 3, 512, 384
+    # N / 128 odd (dense): the last tile record's second block is zeros
+    G, N, K = 3, (512 if glu else 640), 384
     w = (torch.randn((G, N, K), generator=g, device=DEV) *
          torch.exp2(torch.randint(-6, 6, (G, N, 1), generator=g, device=DEV).float())).to(torch.bfloat16)
     w[0, 5, 32:64] = 0          # an all-zero block
