@@ -701,10 +701,13 @@ moe_status launch_route_small_e(const moe_config& c, cudaStream_t st, const Rout
 // experts that is slower on B300 than the separate gate kernel, which spreads
 // a token's experts over a warp (measured: 36 vs 27 us of routing at T = 4096,
 // E = 64).
+int route_tc_split(const moe_config& c);
+
 bool use_fused_tc_router(const moe_config& c) {
   const int64_t ctas = (static_cast<int64_t>(c.T) + 127) / 128;
   return use_tc_router(c) && c.E <= 16 &&
-         ctas * (c.E + 1) <= static_cast<int64_t>(kMaxExperts + 1) * kRouteMaxRows;
+         ctas * (c.E + 1) <= static_cast<int64_t>(kMaxExperts + 1) * kRouteMaxRows &&
+         route_tc_split(c) > 0;
 }
 
 // Blocks of the routing grid do_route launches (one per token for the
@@ -715,32 +718,92 @@ int route_grid(const moe_config& c, const Layout& L) {
   return L.nb;
 }
 
-template <int EPAD, int KMAX>
-moe_status launch_route_tc_inst(const CUtensorMap& mx, const CUtensorMap& mw, int grid,
-                                const RouteArgs& ra, cudaStream_t st) {
-  constexpr int STAGES = 8;
-  constexpr size_t smem = RouteTcSmem<EPAD, STAGES>::bytes();
+constexpr size_t kRouteTcMaxSmem = 232448 - 2048;   // opt-in shared memory less the static part
+constexpr int kRouteTcMinStages = 4;
+
+// Stages of the fused router's x ring: all the shared memory that the W_g
+// slice, the partials and the control block leave, at most 12.
+template <int S>
+int route_tc_stages(int kbs) {
+  using L = RouteTcSmem<S>;
+  const size_t fixed = L::bytes(kbs, 0);
+  if (fixed >= kRouteTcMaxSmem) return 0;
+  return static_cast<int>(std::min<size_t>(L::kMaxStages, (kRouteTcMaxSmem - fixed) / L::A_BYTES));
+}
+
+// Cluster size of the fused router: enough CTAs per 128-token tile to cover
+// the SMs, and enough for the tile's slice of W_g to leave room for at least
+// four stages; 0 when no size in {1, 2, 4} does.
+int route_tc_split(const moe_config& c) {
+  const int tiles = (c.T + 127) / 128;
+  const int KB = (c.d_model + 63) / 64;
+  const int sms = num_sms();
+  int s = tiles * 5 >= sms * 4 ? 1 : (tiles * 5 >= sms * 2 ? 2 : 4);
+  while (s > 1 && s > KB) s /= 2;   // every rank gets a K block
+  for (; s <= 4 && s <= std::max(KB, 1); s *= 2) {
+    const int kbs = (KB + s - 1) / s;
+    const int st = s == 1 ? route_tc_stages<1>(kbs)
+                          : (s == 2 ? route_tc_stages<2>(kbs) : route_tc_stages<4>(kbs));
+    if (st >= kRouteTcMinStages) return s;
+  }
+  return 0;
+}
+
+template <int KMAX, int S>
+moe_status launch_route_tc_inst(const CUtensorMap& mx, const void* w_g, int w_vec, int tiles,
+                                int KB, const RouteArgs& ra, cudaStream_t st) {
+  const int kbs = (KB + S - 1) / S;
+  const int stages = route_tc_stages<S>(kbs);
+  if (stages < kRouteTcMinStages) return MOE_ERR_UNSUPPORTED;
+  const size_t smem = RouteTcSmem<S>::bytes(kbs, stages);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(k_route_tc<EPAD, KMAX, STAGES>,
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(k_route_tc<KMAX, S>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+                             static_cast<int>(kRouteTcMaxSmem)) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
-  return launch_pdl(k_route_tc<EPAD, KMAX, STAGES>, dim3(grid), dim3(192), smem, st, mx, mw, ra);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * S));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = S > 1 ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, k_route_tc<KMAX, S>, mx, static_cast<const __nv_bfloat16*>(w_g),
+                         w_vec, stages, ra) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
-template <int EPAD>
-moe_status launch_route_tc_k(int km, const CUtensorMap& mx, const CUtensorMap& mw, int grid,
-                             const RouteArgs& ra, cudaStream_t st) {
+template <int KMAX>
+moe_status launch_route_tc_s(int split, const CUtensorMap& mx, const void* w_g, int w_vec,
+                             int tiles, int KB, const RouteArgs& ra, cudaStream_t st) {
+  if (split == 1) return launch_route_tc_inst<KMAX, 1>(mx, w_g, w_vec, tiles, KB, ra, st);
+  if (split == 2) return launch_route_tc_inst<KMAX, 2>(mx, w_g, w_vec, tiles, KB, ra, st);
+  return launch_route_tc_inst<KMAX, 4>(mx, w_g, w_vec, tiles, KB, ra, st);
+}
+
+moe_status launch_route_tc(int km, int split, const CUtensorMap& mx, const void* w_g, int w_vec,
+                           int tiles, int KB, const RouteArgs& ra, cudaStream_t st) {
   switch (km) {
-    case 2: return launch_route_tc_inst<EPAD, 2>(mx, mw, grid, ra, st);
-    case 4: return launch_route_tc_inst<EPAD, 4>(mx, mw, grid, ra, st);
-    case 8: return launch_route_tc_inst<EPAD, 8>(mx, mw, grid, ra, st);
-    default: return launch_route_tc_inst<EPAD, 16>(mx, mw, grid, ra, st);
+    case 2: return launch_route_tc_s<2>(split, mx, w_g, w_vec, tiles, KB, ra, st);
+    case 4: return launch_route_tc_s<4>(split, mx, w_g, w_vec, tiles, KB, ra, st);
+    case 8: return launch_route_tc_s<8>(split, mx, w_g, w_vec, tiles, KB, ra, st);
+    default: return launch_route_tc_s<16>(split, mx, w_g, w_vec, tiles, KB, ra, st);
   }
 }
 
@@ -800,6 +863,16 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
   const int km = kmax_of(c.k);
   moe_status s = MOE_OK;
   if (L.tc_router) {
+    if (use_fused_tc_router(c)) {
+      // a cluster of 1, 2 or 4 CTAs per 128 tokens (split over d), the gating
+      // in the GEMM epilogue; W_g read as it is
+      CUtensorMap mx;
+      if (!map_a(&mx, x, c.d_model, c.T)) return MOE_ERR_CUDA;
+      const int w_vec =
+          (c.E == 8 || c.E == 16) && (reinterpret_cast<uintptr_t>(w_g) & 15) == 0 ? 1 : 0;
+      return launch_route_tc(km, route_tc_split(c), mx, w_g, w_vec, (c.T + 127) / 128,
+                             (c.d_model + 63) / 64, ra, st);
+    }
     __nv_bfloat16* wgT = at<__nv_bfloat16>(ws, L.wgT);
     float* logits_ws = at<float>(ws, L.logits);
     dim3 tgrid((c.d_model + 31) / 32, (L.E_pad + 31) / 32);
@@ -807,16 +880,6 @@ moe_status do_route(const moe_config& c, const Layout& L, void* ws, const void* 
                         static_cast<const __nv_bfloat16*>(w_g), c.d_model, c.E, L.E_pad, wgT)) !=
         MOE_OK)
       return s;
-    if (use_fused_tc_router(c)) {
-      // one CTA per 128 tokens, the gating in the GEMM epilogue
-      CUtensorMap mx, mw;
-      if (!map_a(&mx, x, c.d_model, c.T) || !map_b(&mw, wgT, c.d_model, L.E_pad, 1, L.E_pad))
-        return MOE_ERR_CUDA;
-      const int grid = (c.T + 127) / 128;
-      if (L.E_pad == 16) return launch_route_tc_k<16>(km, mx, mw, grid, ra, st);
-      if (L.E_pad == 32) return launch_route_tc_k<32>(km, mx, mw, grid, ra, st);
-      return launch_route_tc_k<64>(km, mx, mw, grid, ra, st);
-    }
     if ((s = tc_logits_gemm(c, L, ws, x, st)) != MOE_OK) return s;
     ra.logits_in = logits_ws;
     ra.ld_in = L.E_pad;
