@@ -152,7 +152,7 @@ __device__ __forceinline__ void mx2_store_mx(const uint32_t (&a)[8][16], int col
       } else if (EPI == EPI_SILU_MX) {
         x = silu(x);
       } else {
-        x = gelu_erf(x);
+        x = gelu_erf_as(x);
       }
       v[i] = x;
     }
