@@ -57,7 +57,8 @@ L2_FLUSH_BYTES = 256 << 20
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-GEMM_SOURCES = ["gemm_tc.cuh", "gemm_tc2.cuh", "ptx_sm100.cuh", "groups.cuh", "mxfp8.cuh"]
+GEMM_SOURCES = ["gemm_tc.cuh", "gemm_tc2.cuh", "gemm_mx2.cuh", "ptx_sm100.cuh", "groups.cuh",
+                "mxfp8.cuh"]
 # oracle rows (tokens whose FFN output the CPU baseline computes) per workload
 CPU_SAMPLE_ROWS = {"tiny_fp32_top2": 256, "switch_top1_cap": 4096, "mixtral_top2": 128,
                    "deepseek_v3_top8": 16, "decode_zipf_top2": 64, "mixtral_swiglu_top2": 128,
