@@ -251,20 +251,23 @@ struct TcSmem {
 // factor), then per 32 output columns the largest magnitude, the E8M0 scale
 // and the e4m3 codes, stored at row `orow` of the hidden activation, and the
 // row's scale bytes in the interleaved block of its 128 rows and its
-// 128-column stage.  `add` folds in stream-K partials of a 16-column chunk
-// (a no-op without stream-K).  Every lane of the warp must call it (the
-// tensor-memory loads are warp-wide); `valid` only gates the stores.
+// 128-column stage.  The thread takes the tile's 32-column output blocks
+// [cb0, cb1) (two warps share a lane quarter, each half the blocks).  `add`
+// folds in stream-K partials of a 16-column chunk (a no-op without stream-K).
+// Every lane of the warp must call it (the tensor-memory loads are
+// warp-wide); `valid` only gates the stores.
 template <int EPI, int BN, typename AddPartials>
-__device__ __forceinline__ void mx_store_row(uint32_t trow, int n_blk, bool valid, int64_t orow,
-                                             const __nv_bfloat16* bias, const TcArgs& args,
-                                             AddPartials&& add) {
+__device__ __forceinline__ void mx_store_row(uint32_t trow, int n_blk, int cb0, int cb1, bool valid,
+                                             int64_t orow, const __nv_bfloat16* bias,
+                                             const TcArgs& args, AddPartials&& add) {
   constexpr bool GLU = epi_glu(EPI);
   constexpr int NCC = BN / 16;
   constexpr int BNO = GLU ? BN / 2 : BN;
   constexpr int NOUT = GLU ? NCC / 2 : NCC;
+  static_assert(NOUT % 2 == 0, "whole 32-column blocks");
   uint32_t sfw = 0;   // the blocks' scale bytes, byte j = block j of the 128-column stage
 #pragma unroll 1
-  for (int cb = 0; cb < NOUT / 2; ++cb) {
+  for (int cb = cb0; cb < cb1; ++cb) {
     float v[32];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -323,22 +326,26 @@ __device__ __forceinline__ void mx_store_row(uint32_t trow, int n_blk, bool vali
     *reinterpret_cast<uint4*>(o + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     sfw |= sbyte << (8 * ((col >> 5) & 3));
   }
-  if (valid) {
+  if (valid) {   // this thread's blocks' bytes of the row's 4-byte scale word
     const int col0 = n_blk * BNO;
     uint8_t* sfp = args.sf_out +
                    ((static_cast<int64_t>(col0 >> 7) * args.sf_out_rb + (orow >> 7)) * 512) +
                    (orow & 31) * 16 + ((orow & 127) >> 5) * 4;
-    if constexpr (BNO >= 128) {
-      *reinterpret_cast<uint32_t*>(sfp) = sfw;
-    } else {
-      const int j0 = (col0 >> 5) & 3;
-      *reinterpret_cast<uint16_t*>(sfp + j0) = static_cast<uint16_t>(sfw >> (8 * j0));
+    for (int cb = cb0; cb < cb1; ++cb) {
+      const int j = ((col0 + 32 * cb) >> 5) & 3;
+      sfp[j] = static_cast<uint8_t>(sfw >> (8 * j));
     }
   }
 }
 
+// Epilogue warps: four, one per TMEM lane quarter; MX kernels take eight,
+// two per lane quarter splitting the tile's columns (their quantising
+// epilogue, alone on a scheduler, was the bottleneck of short-K tiles).
+template <bool MX>
+__host__ __device__ constexpr int tc_epi_warps() { return MX ? 8 : 4; }
+
 template <int BN, int STAGES, int EPI, bool MX = false>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * tc_epi_warps<MX>(), 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
           const __grid_constant__ CUtensorMap mB0, const __grid_constant__ CUtensorMap mB1,
           const TcArgs args) {
@@ -373,7 +380,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&c.tfull[a], 1);
-      mbar_init(&c.tempty[a], 4);
+      mbar_init(&c.tempty[a], tc_epi_warps<MX>());
     }
     mbar_init(&c.drain, 1);
     c.abort_flag = 0;
@@ -404,7 +411,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   const int total = c.tb.tile_start[G];
   volatile int* abort_flag = &c.abort_flag;
   SkSplit split;
-  split.init(total, KB, args.streamk);
+  split.init(total, KB, MX ? 0 : args.streamk);   // MX: two warps a lane quarter, no stream-K
   SegIter seg;
   seg.init(split, KB);
 
@@ -430,7 +437,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         const int ncol = n_blk * BNO;
         if (args.ready_mode == READY_WAIT && g != ready_g) {
           // every hidden tile of group g stored by the up-projection (4 epilogue warps each)
-          const int need = ((c.tb.rows[g] + BM - 1) / BM) * args.ready_up_tiles * 4;
+          const int need =
+              ((c.tb.rows[g] + BM - 1) / BM) * args.ready_up_tiles * tc_epi_warps<MX>();
           const uint64_t t0 = global_timer_ns();
           while (ld_acquire_gpu(args.ready + g) < need) {
             if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
@@ -550,6 +558,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = MX ? (warp - 2) >> 2 : 0;   // MX: which half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
     int t, kb0, kb1;
@@ -655,9 +664,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUten
         }
       };
       constexpr int NOUT = GLU ? NCC / 2 : NCC;   // 16-column output chunks
-      if constexpr (MXO) mx_store_row<EPI, BN>(trow, n_blk, valid, orow, bias, args, add_partials);
+      // 16-column output chunks of this warp: all, or (MX) its half
+      const int cc_lo = MX ? half * (NOUT / 2) : 0;
+      const int cc_hi = MX ? cc_lo + NOUT / 2 : NOUT;
+      if constexpr (MXO)
+        mx_store_row<EPI, BN>(trow, n_blk, cc_lo / 2, cc_hi / 2, valid, orow, bias, args,
+                              add_partials);
 #pragma unroll 1
-      for (int cc = 0; cc < (MXO ? 0 : NOUT); ++cc) {
+      for (int cc = cc_lo; cc < (MXO ? cc_lo : cc_hi); ++cc) {
         uint32_t r[16], ru[GLU ? 16 : 1];
         tmem_ld_32x32b_x16(trow + cc * 16, r);
         tmem_wait_ld(r);

@@ -362,7 +362,8 @@ moe_status launch_tc_inst(const CUtensorMap& a0, const CUtensorMap& a1, const CU
   // count; round-robin: no more CTAs than tiles
   const int grid = args.streamk ? std::min(num_sms(), kMaxGemmCtas)
                                 : static_cast<int>(std::min<int64_t>(ub, num_sms()));
-  return launch_pdl(k_gemm_tc<BN, STAGES, EPI, MX>, dim3(grid), dim3(192), smem, st, a0, a1, b0,
+  return launch_pdl(k_gemm_tc<BN, STAGES, EPI, MX>, dim3(grid), dim3(64 + 32 * tc_epi_warps<MX>()),
+                    smem, st, a0, a1, b0,
                     b1, args);
 }
 
@@ -1185,12 +1186,9 @@ moe_status do_ffn_mx(const moe_config& c, const Layout& L, void* ws, const FfnIn
                               8 * mx_tile_records(E, d, F), 8)))
     return MOE_ERR_CUDA;
   const int64_t row_tiles_ub = (Tk + 127) / 128 + E;
-  const int64_t rt = est_row_tiles(Tk, E);
-  const int sms = num_sms();
-  // single CTAs: whole tiles round robin unless there are 8 waves or more
-  // (stream-K tail); CTA pairs: whole tiles only
-  const bool sk_up = !pair && rt * (F1 / 128) >= 8 * static_cast<int64_t>(sms);
-  const bool sk_dn = !pair && rt * (d / 128) >= 8 * static_cast<int64_t>(sms);
+  // whole tiles round robin (the MX kernels split no tile stream-K: their
+  // eight epilogue warps share a lane quarter two by two)
+  const bool sk_up = false, sk_dn = false;
   const bool overlap = !pair && !sk_up && !sk_dn;
   const int64_t pair_rows = (Tk + 255) / 256 + E;
   TcArgs up{};
