@@ -1097,7 +1097,9 @@ moe_status permute_from_idx(const moe_config& c, const DispatchArgs& dp, const v
 // point needs no caller workspace and allocates nothing.  Host code must not
 // pass `g_noalloc_scratch` itself to a kernel (in host code the name is only a
 // host-side stand-in): the device address comes from cudaGetSymbolAddress,
-// looked up once per device with that device current.  Layout in int32
+// looked up on every call with the device current; the header is cleared
+// whenever that address changes (the first call, or a new context after a
+// device reset).  Layout in int32
 // words: [0, 512) header (status word at 0, the ranking grid's block counter
 // at 4 and the per-expert totals at [256, 512): all must start at zero), then
 // the in-chunk ranks (T*k entries), then the per-chunk counts (E rows of
