@@ -181,3 +181,29 @@ def test_mx_full_workload_all_tokens(name):
     print(name, rep.summary())
     del layer, inp
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode,T", [("empty_experts", 2048), ("all_to_one", 2048),
+                                    ("empty_experts", 300)])
+def test_mx_skewed_routing(mode, T):
+    """Skewed routing on the MX FP8 kernels: empty experts between busy ones
+    (zero-row groups among the 256-row aligned group offsets) and one expert
+    taking every token; T = 2048 runs the CTA-pair GEMM, T = 300 the
+    single-CTA one."""
+    cfg = synth.workload("mixtral_top2", experts="mxfp8", T=T, d_model=256, d_ff=256, E=4)
+    inp = synth.make_inputs(cfg, device=DEV)
+    lb = torch.zeros(4, device=DEV)
+    if mode == "empty_experts":
+        lb[1] = -30.0
+        lb[3] = -30.0
+    else:
+        lb[2] = 30.0
+    inp["logit_bias"] = lb
+    fw, layer = run_forward(cfg, inp)
+    rows = None if T <= 1000 else sorted(set(np.linspace(0, T - 1, 512).astype(int).tolist()))
+    rep = compare.check_layer(cfg, inp, fw, rows=rows)
+    if mode == "empty_experts":
+        assert fw["counts"][1] == 0 and fw["counts"][3] == 0
+    else:
+        assert fw["counts"][2] == T
+    print(mode, T, rep.summary())

@@ -109,10 +109,12 @@ SMALL = {
                               renorm=1, aux_f="topk_count"),
     "mixtral_small_tc_router": dict(name="mixtral_top2", T=600, d_model=256, d_ff=512),
     "mixtral_small_warp_router": dict(name="mixtral_top2", T=200, d_model=256, d_ff=512),
-    # the fused tensor-core router: one CTA per 128 tokens (16384 tokens), a
-    # cluster of 4 splitting d = 320 unevenly (E = 16, two 16-byte W_g loads
-    # a row), and E = 6 (W_g rows of 12 bytes, element loads)
+    # the fused tensor-core router: one CTA per 128 tokens (16384 tokens),
+    # clusters of 2 with a ragged last tile (8000 tokens), a cluster of 4
+    # splitting d = 320 unevenly (E = 16, two 16-byte W_g loads a row), and
+    # E = 6 (W_g rows of 12 bytes, element loads)
     "tc_router_no_split": dict(name="mixtral_top2", T=16384, d_model=256, d_ff=128),
+    "tc_router_split2_ragged_t": dict(name="mixtral_top2", T=8000, d_model=256, d_ff=128),
     "tc_router_e16_split4_ragged_d": dict(name="mixtral_top2", T=4096, d_model=320, d_ff=128,
                                           E=16, k=4),
     "tc_router_e6_scalar_w": dict(name="mixtral_top2", T=1024, d_model=192, d_ff=128, E=6),
