@@ -118,6 +118,11 @@ SMALL = {
     "tc_router_e16_split4_ragged_d": dict(name="mixtral_top2", T=4096, d_model=320, d_ff=128,
                                           E=16, k=4),
     "tc_router_e6_scalar_w": dict(name="mixtral_top2", T=1024, d_model=192, d_ff=128, E=6),
+    # the tensor-core router's three launches (transposed W_g, logits GEMM,
+    # gating grid) at E = 64 and E = 32
+    "tc_router_e64_top1": dict(name="switch_top1_cap", T=1024, d_model=256, d_ff=128, E=64),
+    "tc_router_e32_biased": dict(name="deepseek_v3_top8", T=1024, d_model=256, d_ff=128, E=32,
+                                 k=4, n_shared=0),
     "softmax_topk_k3_ragged": dict(name="mixtral_top2", route="softmax_topk", T=333,
                                    d_model=200, d_ff=328, E=12, k=3),
     "deepseek_small_e256": dict(name="deepseek_v3_top8", T=256, d_model=128, d_ff=64),
